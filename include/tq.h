@@ -1,0 +1,181 @@
+/*
+ * tq.h -- C ABI of the quantized-KV decode-attention library (libtq.so).
+ *
+ * The library implements single-step (decode) attention over a TurboQuant-style
+ * quantized KV cache and the encode/append that fills that cache, as hand-written
+ * CUDA kernels for sm_103a (GB300).
+ *
+ * What the operations compute (sources: turboquant_plus "SMEM Pre-Dequant
+ * Experiment", sections "What Was Changed" and "What Would Actually Work
+ * (Hypotheses)"; mlxcel pull request #369 "route Turbo4Asym decode through
+ * dequant-SDPA", sections Problem, Change and Result):
+ *
+ *   Each 128-dim K or V head vector x is stored as
+ *     n16   = fp16(||x||_2)                          (round to nearest even)
+ *     u     = Rot(x) / ||x||,  Rot(x) = H (s * x) / sqrt(128)
+ *     idx_i = nearest entry of a symmetric b-bit codebook to u_i (ties: lower)
+ *   with s a seeded +-1 sign vector and H the Sylvester Hadamard matrix.
+ *   Attention over such a cache equals attention over the fully dequantized
+ *   vectors Rot^-1(n16 * c[idx]); because Rot is orthogonal the library scores
+ *   with Rot(q) against n16*c[idx], accumulates P.V in the rotated basis, and
+ *   inverse-rotates only the [B, Hq, Tq, 128] output (the rotated-basis identity
+ *   rotate(SDPA(q,k,v)) == SDPA(q,k,rotate(v)) of the mlxcel pull request).
+ *
+ * Conventions for every call:
+ *   - Return 0 on success, a negative TQ_ERR_* code on failure.  Argument errors
+ *     are detected on the host before any launch; nothing is launched then.
+ *   - Calls are asynchronous on the given stream (a cudaStream_t passed as
+ *     void*, NULL = legacy default stream) and never synchronize, except
+ *     tq_get_status and tq_get_kernel_time.
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never frees them.  The library owns only the context (workspace, status
+ *     word, cached tables), created lazily when *ctx == NULL and released by
+ *     tq_free.  A context is bound to the device that was current when it was
+ *     created.
+ *   - Conditions only the GPU can see (a sequence whose append passes the
+ *     capacity, a norm that overflows fp16, a sequence shorter than the query
+ *     block, a pipeline wait that timed out) never trap: the kernels OR a bit
+ *     into the context's device status word, read by tq_get_status.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* error codes */
+#define TQ_OK                0
+#define TQ_ERR_INVALID_ARG  (-1)
+#define TQ_ERR_UNSUPPORTED  (-2)
+#define TQ_ERR_CAPACITY     (-3)
+#define TQ_ERR_CUDA         (-4)
+#define TQ_ERR_NOMEM        (-5)
+
+/* modes: (K format, V format).  Turbo4Asym = fp16 K + 4-bit rotated V
+ * (mlxcel pull request #369, Problem); turbo3 / turbo4 = K and V both 3- or
+ * 4-bit rotated ("4-mag LUT" turbo3 of the smem-dequant experiment). */
+#define TQ_TURBO4_ASYM  0
+#define TQ_TURBO3       1
+#define TQ_TURBO4       2
+
+/* device status bits (tq_get_status) */
+#define TQ_STATUS_CAPACITY        1u  /* an append would pass `capacity`; that sequence was skipped */
+#define TQ_STATUS_NORM_OVERFLOW   2u  /* a vector norm overflowed fp16; stored as +inf */
+#define TQ_STATUS_SHORT_CONTEXT   4u  /* a query row saw no token (length < Tq); its output is 0 */
+#define TQ_STATUS_PIPELINE_STALL  8u  /* a bounded in-kernel wait gave up; results are invalid */
+
+typedef struct tq_ctx tq_ctx;
+
+/*
+ * The packed cache (caller-owned device memory).
+ *
+ *   k_data  TQ_TURBO4_ASYM: fp16 [batch, num_kv_heads, capacity, 128], unrotated.
+ *           otherwise: uint8 [batch, num_kv_heads, capacity, rb_k] packed codes,
+ *           rb_k = tq_record_bytes(bits_k) (48 for 3-bit, 64 for 4-bit).
+ *   k_norm  fp16 [batch, num_kv_heads, capacity] (NULL for TQ_TURBO4_ASYM).
+ *   v_data  uint8 [batch, num_kv_heads, capacity, rb_v] packed codes.
+ *   v_norm  fp16 [batch, num_kv_heads, capacity].
+ *   lengths int32 [batch]: visible tokens per sequence; tq_encode_append
+ *           advances it on the device.
+ *   Code layout of one record (dimension d, code kappa = sign<<(b-1) | rank,
+ *   sign = 1 for the negative half of the codebook, rank 0 = smallest |c|):
+ *     4-bit: kappa(d) in byte d/2, low nibble for even d.
+ *     3-bit: four 12-byte quarters; quarter q = dims 32q..32q+31 as three
+ *            little-endian 32-bit words w0..w2 at bytes 12q+4k; bits 4j..4j+2
+ *            of wk = kappa(32q+8k+j), bit 4j+3 of wk = bit k of kappa(32q+24+j).
+ *   Every pointer must be 16-byte aligned and capacity a multiple of 16.
+ *
+ *   codebook_k / codebook_v: HOST pointers to 2^bits fp32 values, strictly
+ *   ascending and exactly symmetric (c[j] == -c[2^bits-1-j]); codebook_k is
+ *   ignored for TQ_TURBO4_ASYM.  tq_lloyd_max_codebook gives the standard one.
+ *   rot_seed: seed of the sign vector (s_i = -1 iff bit 63 of the i-th
+ *   splitmix64 output is set).  v_rescale: scalar applied to V (its effect on
+ *   the output is a plain scale).
+ */
+typedef struct {
+    int32_t mode;
+    int32_t batch;
+    int32_t num_kv_heads;
+    int32_t head_dim;        /* must be 128 */
+    int32_t capacity;        /* tokens per (batch, kv head) row; multiple of 16 */
+    void *k_data;
+    void *k_norm;
+    void *v_data;
+    void *v_norm;
+    int32_t *lengths;
+    const float *codebook_k;
+    int32_t codebook_k_size;
+    const float *codebook_v;
+    int32_t codebook_v_size;
+    uint64_t rot_seed;
+    float v_rescale;
+} tq_cache;
+
+/*
+ * Append t_new tokens per sequence (the cache update of the decode step,
+ * mlxcel pull request #369, Change: "uses v_rescale and mutates cache state
+ * identically ... (only self.update)").
+ *   k_new, v_new: fp16 [batch, num_kv_heads, t_new, 128] device pointers.
+ *   Token j of sequence b is written at position lengths[b] + j; afterwards
+ *   lengths[b] += t_new.  A sequence with lengths[b] + t_new > capacity is left
+ *   untouched and TQ_STATUS_CAPACITY is raised.  t_new == 0 is a no-op.
+ */
+int tq_encode_append(tq_ctx **ctx, const tq_cache *cache, const void *k_new,
+                     const void *v_new, int32_t t_new, void *stream);
+
+/*
+ * Decode attention over the visible cache (scores, online softmax, rotated-
+ * basis P.V, split-K combine, inverse rotation of the output).
+ *   q:   fp16 [batch, num_q_heads, tq, 128] device pointer.
+ *   out: fp16 [batch, num_q_heads, tq, 128] device pointer.
+ *   num_q_heads must be a multiple of num_kv_heads; q head h reads kv head
+ *   h / (num_q_heads / num_kv_heads).  Query j (0 <= j < tq) of sequence b
+ *   attends to tokens [0, lengths[b] - tq + j] (causal within the block).
+ *   max_len_hint: an upper bound of every lengths[b] (sizes the split-K grid);
+ *   it must not exceed capacity; tokens past it are not read.
+ *   scale: softmax scale, 0 selects 1/sqrt(128).
+ *   The call uses context workspace; it grows (cudaMalloc) when a larger
+ *   problem arrives, so warm up before capturing a CUDA graph.
+ */
+int tq_decode_attention(tq_ctx **ctx, const tq_cache *cache, const void *q,
+                        int32_t num_q_heads, int32_t tq, int32_t max_len_hint,
+                        float scale, void *out, void *stream);
+
+/* Release a context (device memory included).  tq_free(NULL) is a no-op. */
+void tq_free(tq_ctx *ctx);
+
+/* Synchronize the device, return the device status bits in *status and clear
+ * them.  Returns TQ_ERR_CUDA if the device reported an error. */
+int tq_get_status(tq_ctx *ctx, uint32_t *status);
+
+/* Host-only: the Lloyd-Max codebook of N(0, 1/128) with 2^bits levels
+ * (bits in 1..4), iterated in double precision to a fixed point and rounded to
+ * fp32, ascending, into out[0 .. 2^bits-1]. */
+int tq_lloyd_max_codebook(int32_t bits, float *out);
+
+/* Host-only: bytes of one packed record: 48 (bits 3), 64 (bits 4), 256 (16 = fp16). */
+int tq_record_bytes(int32_t bits);
+
+/* Host-only: the split-K plan tq_decode_attention would use: tokens per split
+ * and number of splits (per sequence and row group). */
+int tq_plan_splits(int32_t mode, int32_t batch, int32_t num_kv_heads,
+                   int32_t rows_per_kv_head, int32_t max_len_hint,
+                   int32_t *split_tokens, int32_t *num_splits);
+
+/* Benchmark hook: when enabled, tq_decode_attention records CUDA events around
+ * its main (split-K) kernel; tq_get_kernel_time synchronizes on the last event
+ * and returns the summed milliseconds and the number of timed launches since
+ * the last read (and resets both). */
+int tq_set_kernel_timing(tq_ctx *ctx, int32_t enable);
+int tq_get_kernel_time(tq_ctx *ctx, float *ms_total, int32_t *launches);
+
+/* Human-readable text of an error code. */
+const char *tq_error_string(int32_t code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */

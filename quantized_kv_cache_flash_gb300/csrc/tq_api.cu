@@ -1,0 +1,518 @@
+// Host side of the C ABI declared in include/tq.h: argument checks, codebook
+// tables, sign vector, split planning, workspace, launches.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "tq.h"
+#include "tq_internal.h"
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kSMs = 152;  // GB300 (only used to size the split grid)
+
+struct EventPair {
+    cudaEvent_t a = nullptr, b = nullptr;
+};
+
+struct CodebookTables {
+    bool valid = false;
+    int bits = 0;
+    float cb[16] = {};
+    uint32_t tab[4] = {};  // prmt byte tables
+    float gt[7] = {}, ge[7] = {};
+};
+
+}  // namespace
+
+struct tq_ctx {
+    int device = -1;
+    uint32_t* d_words = nullptr;  // [0] status, [1] encode ticket counter
+    float* d_work = nullptr;
+    size_t work_bytes = 0;
+    CodebookTables ktab, vtab;
+    bool signs_valid = false;
+    uint64_t seed = 0;
+    uint32_t signs[4] = {};
+    // tensor map of the fp16 K rows (rebuilt when the buffer or shape changes)
+    CUtensorMap kmap;
+    const void* kmap_ptr = nullptr;
+    uint64_t kmap_rows = 0;
+    bool timing = false;
+    std::vector<EventPair> events;
+    size_t events_used = 0;
+};
+
+namespace {
+
+int cuda_err(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int mode_bits(int mode, int* kb, int* vb) {
+    switch (mode) {
+        case TQ_TURBO4_ASYM: *kb = 16; *vb = 4; return TQ_OK;
+        case TQ_TURBO3: *kb = 3; *vb = 3; return TQ_OK;
+        case TQ_TURBO4: *kb = 4; *vb = 4; return TQ_OK;
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+}
+
+// splitmix64 (Steele, Lea, Flood 2014; the finaliser of Vigna's splitmix64.c)
+uint64_t splitmix64_next(uint64_t& state) {
+    state += 0x9E3779B97F4A7C15ull;
+    uint64_t z = state;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+void make_signs(uint64_t seed, uint32_t out[4]) {
+    uint64_t st = seed;
+    out[0] = out[1] = out[2] = out[3] = 0;
+    for (int d = 0; d < kD; ++d) {
+        const uint64_t v = splitmix64_next(st);
+        if (v >> 63) out[d >> 5] |= 1u << (d & 31);
+    }
+}
+
+uint16_t half_bits(float f) {
+    __half h = __float2half_rn(f);
+    uint16_t b;
+    std::memcpy(&b, &h, 2);
+    return b;
+}
+
+// A codebook must have 2^bits finite entries, strictly ascending, exactly
+// symmetric (the sign-magnitude codes rely on c[j] == -c[n-1-j]).
+int check_codebook(const float* cb, int n, int bits) {
+    if (cb == nullptr || n != (1 << bits)) return TQ_ERR_INVALID_ARG;
+    for (int j = 0; j < n; ++j)
+        if (!std::isfinite(cb[j])) return TQ_ERR_INVALID_ARG;
+    for (int j = 0; j + 1 < n; ++j)
+        if (!(cb[j] < cb[j + 1])) return TQ_ERR_INVALID_ARG;
+    for (int j = 0; j < n; ++j)
+        if (cb[j] != -cb[n - 1 - j]) return TQ_ERR_INVALID_ARG;
+    return TQ_OK;
+}
+
+// Build the prmt tables and exact decision thresholds of a checked codebook.
+int build_tables(const float* cb, int n, int bits, CodebookTables* t) {
+    if (t->valid && t->bits == bits && std::memcmp(t->cb, cb, n * sizeof(float)) == 0)
+        return TQ_OK;
+    const int h = n / 2;
+    // magnitudes by rank: m[r] = cb[h + r]
+    uint8_t lo[8] = {}, hi[8] = {};
+    if (bits == 3) {
+        // indexed by the 3-bit code kappa = sign<<2 | rank (sign 1 = negative)
+        for (int k = 0; k < 8; ++k) {
+            const int r = k & 3;
+            const float v = (k & 4) ? -cb[h + r] : cb[h + r];
+            const uint16_t hb = half_bits(v);
+            lo[k] = hb & 0xFF;
+            hi[k] = hb >> 8;
+        }
+    } else if (bits == 4) {
+        // indexed by rank; the sign is applied in the kernel
+        for (int r = 0; r < 8; ++r) {
+            const uint16_t hb = half_bits(cb[h + r]);
+            lo[r] = hb & 0xFF;
+            hi[r] = hb >> 8;
+        }
+    } else {
+        return TQ_ERR_UNSUPPORTED;
+    }
+    auto word = [](const uint8_t* b) {
+        return uint32_t(b[0]) | (uint32_t(b[1]) << 8) | (uint32_t(b[2]) << 16) | (uint32_t(b[3]) << 24);
+    };
+    t->tab[0] = word(lo);
+    t->tab[1] = word(lo + 4);
+    t->tab[2] = word(hi);
+    t->tab[3] = word(hi + 4);
+    // thresholds between positive neighbours: tau_k = (m[k] + m[k+1]) / 2 exactly
+    for (int k = 0; k < 7; ++k) t->gt[k] = t->ge[k] = INFINITY;
+    for (int k = 0; k + 1 < h; ++k) {
+        const double tau = 0.5 * (double(cb[h + k]) + double(cb[h + k + 1]));
+        const float f = float(tau);
+        const float up = std::nextafter(f, INFINITY);
+        if (double(f) > tau) { t->ge[k] = f; t->gt[k] = f; }
+        else if (double(f) == tau) { t->ge[k] = f; t->gt[k] = up; }
+        else { t->ge[k] = up; t->gt[k] = up; }
+    }
+    std::memcpy(t->cb, cb, n * sizeof(float));
+    t->bits = bits;
+    t->valid = true;
+    return TQ_OK;
+}
+
+int get_ctx(tq_ctx** pctx, tq_ctx** out) {
+    if (pctx == nullptr) return TQ_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+    if (*pctx == nullptr) {
+        tq_ctx* c = new (std::nothrow) tq_ctx();
+        if (c == nullptr) return TQ_ERR_NOMEM;
+        c->device = dev;
+        if (cudaMalloc(&c->d_words, 64) != cudaSuccess) {
+            delete c;
+            return TQ_ERR_NOMEM;
+        }
+        if (cudaMemset(c->d_words, 0, 64) != cudaSuccess) {
+            cudaFree(c->d_words);
+            delete c;
+            return TQ_ERR_CUDA;
+        }
+        *pctx = c;
+    } else if ((*pctx)->device != dev) {
+        return TQ_ERR_INVALID_ARG;
+    }
+    *out = *pctx;
+    return TQ_OK;
+}
+
+int check_cache(const tq_cache* c, int* kb, int* vb) {
+    if (c == nullptr) return TQ_ERR_INVALID_ARG;
+    int r = mode_bits(c->mode, kb, vb);
+    if (r != TQ_OK) return r;
+    if (c->head_dim != kD) return TQ_ERR_UNSUPPORTED;
+    if (c->batch <= 0 || c->num_kv_heads <= 0 || c->capacity <= 0 || (c->capacity % 16) != 0)
+        return TQ_ERR_INVALID_ARG;
+    if (c->k_data == nullptr || c->v_data == nullptr || c->v_norm == nullptr || c->lengths == nullptr)
+        return TQ_ERR_INVALID_ARG;
+    if (*kb != 16 && c->k_norm == nullptr) return TQ_ERR_INVALID_ARG;
+    if (!aligned16(c->k_data) || !aligned16(c->v_data) || !aligned16(c->v_norm) ||
+        (c->k_norm && !aligned16(c->k_norm)))
+        return TQ_ERR_INVALID_ARG;
+    const long long rows = 1ll * c->batch * c->num_kv_heads * c->capacity;
+    if (rows >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;
+    if (*kb != 16 && (r = check_codebook(c->codebook_k, c->codebook_k_size, *kb)) != TQ_OK) return r;
+    if ((r = check_codebook(c->codebook_v, c->codebook_v_size, *vb)) != TQ_OK) return r;
+    return TQ_OK;
+}
+
+int prepare_tables(tq_ctx* ctx, const tq_cache* c, int kb, int vb) {
+    if (kb != 16) {
+        int r = build_tables(c->codebook_k, c->codebook_k_size, kb, &ctx->ktab);
+        if (r != TQ_OK) return r;
+    }
+    int r = build_tables(c->codebook_v, c->codebook_v_size, vb, &ctx->vtab);
+    if (r != TQ_OK) return r;
+    if (!ctx->signs_valid || ctx->seed != c->rot_seed) {
+        make_signs(c->rot_seed, ctx->signs);
+        ctx->seed = c->rot_seed;
+        ctx->signs_valid = true;
+    }
+    return TQ_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// fp16 K rows [B*Hkv*cap, 128] as a 2-D tensor, boxes of 32 rows x 64 halves
+// (128 bytes, 128-byte swizzle).
+int prepare_kmap(tq_ctx* ctx, const tq_cache* c) {
+    const uint64_t rows = uint64_t(c->batch) * c->num_kv_heads * c->capacity;
+    if (ctx->kmap_ptr == c->k_data && ctx->kmap_rows == rows) return TQ_OK;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_tiled();
+    if (enc == nullptr) return TQ_ERR_CUDA;
+    cuuint64_t dims[2] = {kD, rows};
+    cuuint64_t strides[1] = {kD * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&ctx->kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c->k_data, dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return TQ_ERR_CUDA;
+    ctx->kmap_ptr = c->k_data;
+    ctx->kmap_rows = rows;
+    return TQ_OK;
+}
+
+void plan(int kb, int vb, int batch, int hkv, int row_groups, int max_len, int* split_tokens,
+          int* nsplit) {
+    const long long units = 1ll * batch * hkv * row_groups;
+    const int cps = tq::decode_ctas_per_sm(kb, vb);
+    // aim for ~2 waves of CTAs over the context, splits a multiple of 32 tokens
+    const long long target_ctas = 2ll * kSMs * cps;
+    long long per_unit = (target_ctas + units - 1) / units;
+    if (per_unit < 1) per_unit = 1;
+    long long st = (max_len + per_unit - 1) / per_unit;
+    st = ((st + 31) / 32) * 32;
+    st = std::max<long long>(st, 256);
+    st = std::min<long long>(st, 1ll << 20);
+    *split_tokens = int(st);
+    *nsplit = int((max_len + st - 1) / st);
+    if (*nsplit < 1) *nsplit = 1;
+}
+
+int ensure_work(tq_ctx* ctx, size_t bytes) {
+    if (ctx->work_bytes >= bytes) return TQ_OK;
+    if (ctx->d_work) cudaFree(ctx->d_work);
+    ctx->d_work = nullptr;
+    ctx->work_bytes = 0;
+    if (cudaMalloc(&ctx->d_work, bytes) != cudaSuccess) return TQ_ERR_NOMEM;
+    ctx->work_bytes = bytes;
+    return TQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tq_error_string(int32_t code) {
+    switch (code) {
+        case TQ_OK: return "ok";
+        case TQ_ERR_INVALID_ARG: return "invalid argument";
+        case TQ_ERR_UNSUPPORTED: return "unsupported shape or mode";
+        case TQ_ERR_CAPACITY: return "capacity exceeded";
+        case TQ_ERR_CUDA: return "CUDA error";
+        case TQ_ERR_NOMEM: return "out of device memory";
+        default: return "unknown error";
+    }
+}
+
+int tq_record_bytes(int32_t bits) {
+    if (bits == 3) return 48;
+    if (bits == 4) return 64;
+    if (bits == 16) return 256;
+    return TQ_ERR_UNSUPPORTED;
+}
+
+int tq_lloyd_max_codebook(int32_t bits, float* out) {
+    if (out == nullptr) return TQ_ERR_INVALID_ARG;
+    if (bits < 1 || bits > 4) return TQ_ERR_UNSUPPORTED;
+    const int n = 1 << bits;
+    const double sigma = 1.0 / std::sqrt(double(kD));
+    const double inv_sqrt2pi = 0.3989422804014327;
+    double c[16], nc[16];
+    for (int j = 0; j < n; ++j) c[j] = sigma * (-2.0 + 4.0 * j / (n - 1));
+    // Lloyd iteration: cell boundaries at midpoints, each level at its cell's
+    // conditional mean sigma * (phi(a) - phi(b)) / (Phi(b) - Phi(a)) in
+    // standardised units.
+    for (int it = 0; it < 200000; ++it) {
+        double delta = 0.0;
+        for (int j = 0; j < n; ++j) {
+            const double a = (j == 0) ? -INFINITY : 0.5 * (c[j - 1] + c[j]) / sigma;
+            const double b = (j == n - 1) ? INFINITY : 0.5 * (c[j] + c[j + 1]) / sigma;
+            const double pa = std::isinf(a) ? 0.0 : inv_sqrt2pi * std::exp(-0.5 * a * a);
+            const double pb = std::isinf(b) ? 0.0 : inv_sqrt2pi * std::exp(-0.5 * b * b);
+            const double Pa = 0.5 * std::erfc(-a / std::sqrt(2.0));
+            const double Pb = 0.5 * std::erfc(-b / std::sqrt(2.0));
+            nc[j] = sigma * (pa - pb) / (Pb - Pa);
+        }
+        for (int j = 0; j < n; ++j) {
+            delta = std::max(delta, std::fabs(nc[j] - c[j]));
+            c[j] = nc[j];
+        }
+        if (delta < 1e-15) break;
+    }
+    for (int j = 0; j < n; ++j) out[j] = float(c[j]);
+    return TQ_OK;
+}
+
+int tq_plan_splits(int32_t mode, int32_t batch, int32_t num_kv_heads, int32_t rows_per_kv_head,
+                   int32_t max_len_hint, int32_t* split_tokens, int32_t* num_splits) {
+    int kb, vb;
+    if (mode_bits(mode, &kb, &vb) != TQ_OK) return TQ_ERR_UNSUPPORTED;
+    if (batch <= 0 || num_kv_heads <= 0 || rows_per_kv_head <= 0 || max_len_hint <= 0 ||
+        split_tokens == nullptr || num_splits == nullptr)
+        return TQ_ERR_INVALID_ARG;
+    const int rg = (rows_per_kv_head + 15) / 16;
+    plan(kb, vb, batch, num_kv_heads, rg, max_len_hint, split_tokens, num_splits);
+    return TQ_OK;
+}
+
+int tq_encode_append(tq_ctx** pctx, const tq_cache* c, const void* k_new, const void* v_new,
+                     int32_t t_new, void* stream) {
+    int kb, vb;
+    int r = check_cache(c, &kb, &vb);
+    if (r != TQ_OK) return r;
+    if (t_new < 0) return TQ_ERR_INVALID_ARG;
+    if (t_new == 0) return TQ_OK;
+    if (k_new == nullptr || v_new == nullptr || !aligned16(k_new) || !aligned16(v_new))
+        return TQ_ERR_INVALID_ARG;
+    if (t_new > c->capacity) return TQ_ERR_CAPACITY;
+    tq_ctx* ctx;
+    if ((r = get_ctx(pctx, &ctx)) != TQ_OK) return r;
+    if ((r = prepare_tables(ctx, c, kb, vb)) != TQ_OK) return r;
+    tq::EncodeParams p{};
+    p.k_new = static_cast<const __half*>(k_new);
+    p.v_new = static_cast<const __half*>(v_new);
+    p.k_codes = static_cast<uint8_t*>(c->k_data);
+    p.k_norm = static_cast<__half*>(c->k_norm);
+    p.v_codes = static_cast<uint8_t*>(c->v_data);
+    p.v_norm = static_cast<__half*>(c->v_norm);
+    p.lengths = c->lengths;
+    p.status = ctx->d_words;
+    p.counter = ctx->d_words + 1;
+    p.batch = c->batch;
+    p.hkv = c->num_kv_heads;
+    p.t_new = t_new;
+    p.cap = c->capacity;
+    std::memcpy(p.signs, ctx->signs, sizeof(p.signs));
+    if (kb != 16) {
+        std::memcpy(p.k_gt, ctx->ktab.gt, sizeof(p.k_gt));
+        std::memcpy(p.k_ge, ctx->ktab.ge, sizeof(p.k_ge));
+    }
+    std::memcpy(p.v_gt, ctx->vtab.gt, sizeof(p.v_gt));
+    std::memcpy(p.v_ge, ctx->vtab.ge, sizeof(p.v_ge));
+    return cuda_err(static_cast<cudaError_t>(
+        tq::launch_encode(kb, vb, p, static_cast<cudaStream_t>(stream))));
+}
+
+int tq_decode_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_heads,
+                        int32_t tq_rows, int32_t max_len_hint, float scale, void* out, void* stream) {
+    int kb, vb;
+    int r = check_cache(c, &kb, &vb);
+    if (r != TQ_OK) return r;
+    if (q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+    if (tq_rows <= 0 || max_len_hint <= 0 || max_len_hint > c->capacity) return TQ_ERR_INVALID_ARG;
+    if (tq_rows > max_len_hint) return TQ_ERR_INVALID_ARG;
+    if (!(scale >= 0.f) || !std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
+    if (!std::isfinite(c->v_rescale)) return TQ_ERR_INVALID_ARG;
+    const int group = num_q_heads / c->num_kv_heads;
+    const int rows = group * tq_rows;
+    if (rows > 256) return TQ_ERR_UNSUPPORTED;
+    tq_ctx* ctx;
+    if ((r = get_ctx(pctx, &ctx)) != TQ_OK) return r;
+    if ((r = prepare_tables(ctx, c, kb, vb)) != TQ_OK) return r;
+    if (kb == 16 && (r = prepare_kmap(ctx, c)) != TQ_OK) return r;
+
+    const int row_groups = (rows + 15) / 16;
+    int split_tokens, nsplit;
+    plan(kb, vb, c->batch, c->num_kv_heads, row_groups, max_len_hint, &split_tokens, &nsplit);
+    const size_t slots = size_t(c->batch) * c->num_kv_heads * row_groups * nsplit * 16;
+    if ((r = ensure_work(ctx, slots * (kD + 2) * sizeof(float))) != TQ_OK) return r;
+
+    const float sc = (scale == 0.f) ? 1.0f / std::sqrt(float(kD)) : scale;
+    tq::DecodeParams p{};
+    p.k_codes = static_cast<const uint8_t*>(c->k_data);
+    p.k_norm = static_cast<const __half*>(c->k_norm);
+    p.v_codes = static_cast<const uint8_t*>(c->v_data);
+    p.v_norm = static_cast<const __half*>(c->v_norm);
+    p.lengths = c->lengths;
+    p.q = static_cast<const __half*>(q);
+    p.part_o = ctx->d_work;
+    p.part_ml = ctx->d_work + slots * kD;
+    p.status = ctx->d_words;
+    p.batch = c->batch;
+    p.hkv = c->num_kv_heads;
+    p.hq = num_q_heads;
+    p.group = group;
+    p.tq = tq_rows;
+    p.rows = rows;
+    p.row_groups = row_groups;
+    p.cap = c->capacity;
+    p.max_len = max_len_hint;
+    p.split_tokens = split_tokens;
+    p.nsplit = nsplit;
+    p.scale_log2e = sc * 1.4426950408889634f;
+    if (kb != 16) std::memcpy(p.ktab, ctx->ktab.tab, sizeof(p.ktab));
+    std::memcpy(p.vtab, ctx->vtab.tab, sizeof(p.vtab));
+    std::memcpy(p.signs, ctx->signs, sizeof(p.signs));
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (ctx->timing) {
+        if (ctx->events_used == ctx->events.size()) {
+            EventPair ep;
+            if (cudaEventCreate(&ep.a) != cudaSuccess || cudaEventCreate(&ep.b) != cudaSuccess)
+                return TQ_ERR_CUDA;
+            ctx->events.push_back(ep);
+        }
+        e0 = ctx->events[ctx->events_used].a;
+        e1 = ctx->events[ctx->events_used].b;
+        ctx->events_used++;
+    }
+    CUtensorMap dummy;
+    std::memset(&dummy, 0, sizeof(dummy));
+    r = tq::launch_decode(kb, vb, p, kb == 16 ? &ctx->kmap : &dummy, s, e0, e1);
+    if (r != 0) return TQ_ERR_CUDA;
+
+    tq::CombineParams cp{};
+    cp.part_o = p.part_o;
+    cp.part_ml = p.part_ml;
+    cp.lengths = c->lengths;
+    cp.out = static_cast<__half*>(out);
+    cp.status = ctx->d_words;
+    cp.batch = c->batch;
+    cp.hkv = c->num_kv_heads;
+    cp.hq = num_q_heads;
+    cp.group = group;
+    cp.tq = tq_rows;
+    cp.row_groups = row_groups;
+    cp.max_len = max_len_hint;
+    cp.split_tokens = split_tokens;
+    cp.nsplit = nsplit;
+    cp.v_rescale = c->v_rescale;
+    std::memcpy(cp.signs, ctx->signs, sizeof(cp.signs));
+    return cuda_err(static_cast<cudaError_t>(tq::launch_combine(cp, s)));
+}
+
+void tq_free(tq_ctx* ctx) {
+    if (ctx == nullptr) return;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(ctx->device);
+    for (auto& e : ctx->events) {
+        if (e.a) cudaEventDestroy(e.a);
+        if (e.b) cudaEventDestroy(e.b);
+    }
+    if (ctx->d_work) cudaFree(ctx->d_work);
+    if (ctx->d_words) cudaFree(ctx->d_words);
+    cudaSetDevice(prev);
+    delete ctx;
+}
+
+int tq_get_status(tq_ctx* ctx, uint32_t* status) {
+    if (status == nullptr) return TQ_ERR_INVALID_ARG;
+    *status = 0;
+    if (ctx == nullptr) return TQ_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, ctx->d_words, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaMemset(ctx->d_words, 0, 4) != cudaSuccess) return TQ_ERR_CUDA;
+    *status = v;
+    return TQ_OK;
+}
+
+int tq_set_kernel_timing(tq_ctx* ctx, int32_t enable) {
+    if (ctx == nullptr) return TQ_ERR_INVALID_ARG;
+    ctx->timing = enable != 0;
+    return TQ_OK;
+}
+
+int tq_get_kernel_time(tq_ctx* ctx, float* ms_total, int32_t* launches) {
+    if (ctx == nullptr || ms_total == nullptr || launches == nullptr) return TQ_ERR_INVALID_ARG;
+    float total = 0.f;
+    for (size_t i = 0; i < ctx->events_used; ++i) {
+        if (cudaEventSynchronize(ctx->events[i].b) != cudaSuccess) return TQ_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, ctx->events[i].a, ctx->events[i].b) != cudaSuccess)
+            return TQ_ERR_CUDA;
+        total += ms;
+    }
+    *ms_total = total;
+    *launches = int32_t(ctx->events_used);
+    ctx->events_used = 0;
+    return TQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// Host <-> device parameter blocks and launcher entry points (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tq {
+
+// Decode (split-K) kernel parameters.  One CTA = one (split, batch*kv-head,
+// row group); a row group is up to 16 query rows (GQA heads x Tq) of one KV
+// head, the M dimension of the warp-level MMA.
+struct DecodeParams {
+    const uint8_t* k_codes;   // packed K codes (unused for fp16 K)
+    const __half* k_norm;     // fp16 K norms (unused for fp16 K)
+    const uint8_t* v_codes;   // packed V codes
+    const __half* v_norm;     // fp16 V norms
+    const int32_t* lengths;   // [B]
+    const __half* q;          // [B, Hq, Tq, 128]
+    float* part_o;            // [units, row_groups, nsplit, 16, 128]
+    float* part_ml;           // [units, row_groups, nsplit, 16, 2]  (running max in log2 units, sum)
+    uint32_t* status;
+    int32_t batch, hkv, hq, group, tq, rows, row_groups, cap, max_len;
+    int32_t split_tokens, nsplit;
+    float scale_log2e;        // softmax scale * log2(e)
+    uint32_t ktab[4];         // prmt byte tables of the K codebook (lo0, lo1, hi0, hi1)
+    uint32_t vtab[4];
+    uint32_t signs[4];        // bit d set <=> s_d = -1
+};
+
+struct CombineParams {
+    const float* part_o;
+    const float* part_ml;
+    const int32_t* lengths;
+    __half* out;              // [B, Hq, Tq, 128]
+    uint32_t* status;
+    int32_t batch, hkv, hq, group, tq, row_groups, max_len, split_tokens, nsplit;
+    float v_rescale;
+    uint32_t signs[4];
+};
+
+struct EncodeParams {
+    const __half* k_new;      // [B, Hkv, T, 128]
+    const __half* v_new;
+    uint8_t* k_codes;         // packed codes or fp16 K rows (fp16 K mode)
+    __half* k_norm;
+    uint8_t* v_codes;
+    __half* v_norm;
+    int32_t* lengths;
+    uint32_t* status;
+    uint32_t* counter;        // zero between calls; the last CTA resets it
+    int32_t batch, hkv, t_new, cap;
+    uint32_t signs[4];
+    // decision thresholds on |u| over the positive half of the codebook:
+    // a > tau_k  <=>  a >= gt[k];   a >= tau_k  <=>  a >= ge[k]   (fp32, exact)
+    float k_gt[7], k_ge[7], v_gt[7], v_ge[7];
+};
+
+// Launchers (return a cudaError_t value).
+int launch_decode(int kbits, int vbits, const DecodeParams& p, const CUtensorMap* kmap,
+                  cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end);
+int launch_combine(const CombineParams& p, cudaStream_t stream);
+int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stream);
+
+// Shape of the decode kernel's per-warp stage (for the host planner).
+int decode_ctas_per_sm(int kbits, int vbits);
+
+}  // namespace tq

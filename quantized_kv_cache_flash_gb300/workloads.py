@@ -153,3 +153,25 @@ def kv_unit(w: Workload, b: int, h: int, stop: int):
     """(K, V) fp16 [stop, 128] each for tokens [0, stop) of unit (b, h)."""
     return keys(w, b, h, 0, stop), values(w, b, h, 0, stop)
 
+
+
+_S_RANDCODE, _S_RANDNORM = 7, 8
+
+
+def random_codes(key: int, rows: int, record_bytes: int) -> np.ndarray:
+    """Uniform random bytes [rows, record_bytes]: a packed cache whose every
+    code is equally likely (any byte pattern is a valid record)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([key, _S_RANDCODE])))
+    return rng.integers(0, 256, size=(rows, record_bytes), dtype=np.uint8)
+
+
+def random_norms(key: int, rows: int, lo: float = 6.0, hi: float = 16.0) -> np.ndarray:
+    """fp16 norms ~ U[lo, hi] (the norm of a 128-dim N(0,1) vector is ~11.3)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([key, _S_RANDNORM])))
+    return rng.uniform(lo, hi, size=rows).astype(np.float16)
+
+
+def random_fp16(key: int, shape, scale: float = 1.0) -> np.ndarray:
+    """N(0, scale^2) rounded to fp16."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([key, 9])))
+    return (rng.standard_normal(shape, dtype=np.float32) * np.float32(scale)).astype(np.float16)

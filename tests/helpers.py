@@ -1,0 +1,131 @@
+"""Shared test helpers: GPU-side cache setup through the C ABI, the format
+decoder used to read GPU output, and the parity bounds."""
+import math
+
+import numpy as np
+
+from oracle import tq_oracle as o
+from quantized_kv_cache_flash_gb300 import workloads as wl
+
+# attention parity bounds (relative to the RMS of the oracle output)
+MAX_ABS_REL = 1e-2
+RMS_REL = 2e-3
+# encode: elements whose fp64 u is this close to a decision midpoint may differ
+BOUNDARY = 1e-5
+BOUNDARY_FRACTION = 1e-4
+
+MODE_BITS = {"turbo4_asym": (16, 4), "turbo3": (3, 3), "turbo4": (4, 4)}
+
+
+def attention_errors(got, want):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    rms = math.sqrt(float(np.mean(want * want)))
+    err = got - want
+    return rms, float(np.max(np.abs(err))), math.sqrt(float(np.mean(err * err)))
+
+
+def assert_attention_close(got, want, what=""):
+    rms, mx, rmse = attention_errors(got, want)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert rms > 0, f"{what}: degenerate reference"
+    assert mx <= MAX_ABS_REL * rms, f"{what}: max-abs {mx:.3e} > {MAX_ABS_REL} x rms {rms:.3e}"
+    assert rmse <= RMS_REL * rms, f"{what}: rms err {rmse:.3e} > {RMS_REL} x rms {rms:.3e}"
+    return rms, mx, rmse
+
+
+def decode_records(packed: np.ndarray, bits: int) -> np.ndarray:
+    """Read ascending codebook indices back from packed records (GPU output).
+
+    Written separately from the oracle's unpacker: sign-magnitude code kappa
+    -> index h + rank (sign 0) or h - 1 - rank (sign 1).
+    """
+    p = np.ascontiguousarray(packed, np.uint8).reshape(-1, packed.shape[-1])
+    n = p.shape[0]
+    if bits == 4:
+        kappa = np.empty((n, 128), np.int64)
+        kappa[:, 0::2] = p & 0x0F
+        kappa[:, 1::2] = p >> 4
+    else:
+        w = p.view("<u4").astype(np.int64).reshape(n, 4, 3)     # [vec, quarter, word]
+        j = np.arange(8)
+        nib = (w[:, :, :, None] >> (4 * j)) & 0xF               # [vec, q, k, j]
+        low = nib & 7                                           # dims 8k + j
+        spare = (nib >> 3) & 1                                  # bit k of dim 24 + j
+        kappa = np.empty((n, 4, 32), np.int64)
+        kappa[:, :, :24] = low.reshape(n, 4, 24)
+        kappa[:, :, 24:] = spare[:, :, 0] | (spare[:, :, 1] << 1) | (spare[:, :, 2] << 2)
+        kappa = kappa.reshape(n, 128)
+    h = 1 << (bits - 1)
+    sign = kappa >> (bits - 1)
+    rank = kappa & (h - 1)
+    idx = np.where(sign == 0, h + rank, h - 1 - rank)
+    return idx.astype(np.uint8).reshape(*packed.shape[:-1], 128)
+
+
+def torch_device():
+    import torch
+    return torch.device("cuda", 0)
+
+
+def upload(x, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+
+def gpu_cache_from_records(mode, B, Hkv, cap, lengths, kdata, knorm, vdata, vnorm, device,
+                           v_rescale=1.0, rot_seed=42):
+    """A library Cache whose buffers hold the given records (numpy, [B,Hkv,cap,...])."""
+    import torch
+    import quantized_kv_cache_flash_gb300 as tqf
+    c = tqf.Cache(tqf.MODES[mode], B, Hkv, cap, device, rot_seed=rot_seed, v_rescale=v_rescale)
+    c.k_data.copy_(upload(kdata, device))
+    if c.k_norm is not None:
+        c.k_norm.copy_(upload(knorm, device))
+    c.v_data.copy_(upload(vdata, device))
+    c.v_norm.copy_(upload(vnorm, device))
+    c.lengths.copy_(torch.from_numpy(np.asarray(lengths, np.int32)))
+    return c
+
+
+def random_cache(mode, B, Hkv, cap, key):
+    """Random packed records straight from the input generator (numpy)."""
+    kb, vb = MODE_BITS[mode]
+    rows = B * Hkv * cap
+    if kb == 16:
+        kdata = wl.random_fp16(key, (B, Hkv, cap, 128))
+        knorm = None
+    else:
+        kdata = wl.random_codes(key, rows, 16 * kb).reshape(B, Hkv, cap, 16 * kb)
+        knorm = wl.random_norms(key, rows).reshape(B, Hkv, cap)
+    vdata = wl.random_codes(key + 1, rows, 16 * vb).reshape(B, Hkv, cap, 16 * vb)
+    vnorm = wl.random_norms(key + 1, rows).reshape(B, Hkv, cap)
+    return kdata, knorm, vdata, vnorm
+
+
+def oracle_unit_from_records(mode, kdata, knorm, vdata, vnorm, b, h, L):
+    """Oracle view of unit (b, h) of a record cache (the oracle unpacks the bytes)."""
+    kb, vb = MODE_BITS[mode]
+    unit = {"v_idx": o.unpack_codes(vdata[b, h, :L], vb), "v_norm": vnorm[b, h, :L]}
+    if kb == 16:
+        unit["k"] = kdata[b, h, :L]
+    else:
+        unit["k_idx"] = o.unpack_codes(kdata[b, h, :L], kb)
+        unit["k_norm"] = knorm[b, h, :L]
+    return unit
+
+
+def oracle_decode(mode, q, units, lengths, Hkv, tq, scale, v_rescale, rot_seed=42):
+    """Oracle output [B, Hq, Tq, 128] (fp64) from per-unit dicts units[(b, h)]."""
+    kb, vb = MODE_BITS[mode]
+    cbk = o.codebook(kb) if kb != 16 else None
+    cbv = o.codebook(vb)
+    s = o.sign_vector(rot_seed)
+    B, Hq = q.shape[0], q.shape[1]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, tq, 128))
+    for (b, h), unit in units.items():
+        out[b, h * G:(h + 1) * G] = o.decode_unit(mode, q[b, h * G:(h + 1) * G], unit,
+                                                  int(lengths[b]), tq, G, cbk, cbv, s, scale,
+                                                  v_rescale)
+    return out

@@ -1,0 +1,255 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bounds (from the benchmark definition): packed indices bit-exact except
+elements whose fp64 u lies within 1e-5 of a decision midpoint (fewer than
+1e-4 of the elements); norms bit-exact; attention max-abs error <= 1e-2 x RMS
+and RMS error <= 2e-3 x RMS of the oracle output, over the whole tensor.
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import quantized_kv_cache_flash_gb300 as tqf
+from quantized_kv_cache_flash_gb300 import workloads as wl
+from oracle import tq_oracle as o
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+DEV = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    global DEV
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_kv_cache_flash_gb300 import build
+    build.build()
+    DEV = torch.device("cuda", 0)
+    yield
+
+
+def _run_decode(cache, q_np, tq_rows, max_len, scale=0.0, ctx=None):
+    ctx = ctx or tqf.Context()
+    q = H.upload(q_np, DEV)
+    out = torch.empty_like(q)
+    tqf.tq_decode_attention(ctx, cache, q, out, max_len, scale)
+    torch.cuda.synchronize()
+    status = tqf.tq_get_status(ctx)
+    return out.float().cpu().numpy(), status, ctx
+
+
+# ---------------------------------------------------------------------------
+# decode on the same packed cache (random records from the input generator)
+# ---------------------------------------------------------------------------
+DECODE_CASES = [
+    # mode, B, Hq, Hkv, lengths, Tq, cap, scale, v_rescale
+    ("turbo3", 1, 4, 1, [1], 1, 16, 0.0, 1.0),                  # context 1
+    ("turbo3", 2, 8, 2, [37, 300], 1, 320, 0.0, 1.0),           # ragged, tails
+    ("turbo4", 3, 12, 4, [100, 513, 1000], 2, 1024, 0.0, 1.0),  # Tq 2, G 3
+    ("turbo4_asym", 1, 4, 2, [256], 1, 256, 0.0, 1.0),          # tiny Turbo4Asym shape
+    ("turbo4_asym", 2, 28, 4, [2049, 700], 1, 2064, 0.0, 0.5),  # v_rescale
+    ("turbo3", 1, 32, 2, [777], 4, 784, 0.0, 1.0),              # 64 rows: 4 row groups
+    ("turbo4", 2, 8, 8, [5000, 1], 1, 5008, 0.0, 1.0),          # many splits + a 1-token seq
+    ("turbo3", 1, 4, 1, [40], 4, 48, 0.05, 1.0),                # causal block, custom scale
+    ("turbo4", 1, 16, 2, [16], 8, 16, 0.0, 1.0),                # Tq 8 x G 8 = 64 rows, L = Tq*2
+    ("turbo3", 2, 28, 4, [8192, 8191], 1, 8192, 0.0, 1.0),      # Qwen2.5-7B shape, min=max-1
+]
+
+
+@pytest.mark.parametrize("case", DECODE_CASES, ids=lambda c: f"{c[0]}-B{c[1]}-Hq{c[2]}-L{max(c[4])}-Tq{c[5]}")
+def test_decode_same_cache(case):
+    mode, B, Hq, Hkv, lengths, Tq, cap, scale, vr = case
+    key = 7000 + sum(lengths) + 31 * Hq + Tq
+    kd, kn, vd, vn = H.random_cache(mode, B, Hkv, cap, key)
+    q = wl.random_fp16(key + 5, (B, Hq, Tq, 128))
+    cache = H.gpu_cache_from_records(mode, B, Hkv, cap, lengths, kd, kn, vd, vn, DEV, v_rescale=vr)
+    got, status, _ = _run_decode(cache, q, Tq, max(lengths), scale)
+    assert status == 0
+    units = {(b, h): H.oracle_unit_from_records(mode, kd, kn, vd, vn, b, h, lengths[b])
+             for b in range(B) for h in range(Hkv)}
+    sc = scale if scale else 1 / math.sqrt(128)
+    want = H.oracle_decode(mode, q, units, lengths, Hkv, Tq, sc, vr)
+    H.assert_attention_close(got, want, str(case))
+
+
+def test_decode_short_context_rows_are_zero_and_flagged():
+    # lengths 2 with a 4-query block: rows j = 0, 1 see no token
+    mode, B, Hq, Hkv, cap = "turbo3", 1, 2, 1, 16
+    kd, kn, vd, vn = H.random_cache(mode, B, Hkv, cap, 99)
+    q = wl.random_fp16(100, (B, Hq, 4, 128))
+    cache = H.gpu_cache_from_records(mode, B, Hkv, cap, [2], kd, kn, vd, vn, DEV)
+    got, status, _ = _run_decode(cache, q, 4, 16)
+    assert status & tqf.TQ_STATUS_SHORT_CONTEXT
+    assert np.all(got[:, :, :2] == 0)
+    units = {(0, 0): H.oracle_unit_from_records(mode, kd, kn, vd, vn, 0, 0, 2)}
+    want = H.oracle_decode(mode, q, units, [2], Hkv, 4, 1 / math.sqrt(128), 1.0)
+    H.assert_attention_close(got[:, :, 2:], want[:, :, 2:])
+
+
+def test_decode_lengths_beyond_hint_are_clamped():
+    # tokens past max_len_hint are not read: equals the oracle on the first 64
+    mode = "turbo4"
+    kd, kn, vd, vn = H.random_cache(mode, 1, 1, 128, 55)
+    q = wl.random_fp16(56, (1, 2, 1, 128))
+    cache = H.gpu_cache_from_records(mode, 1, 1, 128, [100], kd, kn, vd, vn, DEV)
+    got, _, _ = _run_decode(cache, q, 1, 64)
+    units = {(0, 0): H.oracle_unit_from_records(mode, kd, kn, vd, vn, 0, 0, 64)}
+    # causal position is the true length (100) but only 64 tokens are visible
+    want = H.oracle_decode(mode, q, units, [64], 1, 1, 1 / math.sqrt(128), 1.0)
+    H.assert_attention_close(got, want)
+
+
+# ---------------------------------------------------------------------------
+# encode / append: bit-exact codes and norms
+# ---------------------------------------------------------------------------
+def _crafted_vectors():
+    v = [np.zeros(128, np.float16)]
+    x = np.zeros(128, np.float16); x[:3] = [2048, 64, 1]; v.append(x)         # norm tie -> even
+    x = np.zeros(128, np.float16); x[:4] = [2050, 64, 2, 1]; v.append(x)      # norm tie -> up
+    x = np.zeros(128, np.float16); x[0] = 1.0; v.append(x)                    # basis vector
+    x = np.zeros(128, np.float16); x[5] = -3.0; x[77] = 3.0; v.append(x)      # exact zeros in u
+    v.append(np.full(128, 5000, np.float16))                                  # norm 56568
+    v.append(np.full(128, 6e-8, np.float16))                                  # subnormals
+    v.append(np.full(128, -65504, np.float16))                                # overflow (inf norm)
+    v.append(np.linspace(-8, 8, 128).astype(np.float16))
+    return np.stack(v)
+
+
+@pytest.mark.parametrize("mode", ["turbo3", "turbo4", "turbo4_asym"])
+def test_encode_append_bit_exact(mode):
+    kb, vb = H.MODE_BITS[mode]
+    B, Hkv, T, cap = 2, 3, 300, 320
+    rng = np.random.default_rng(3)
+    k = wl.random_fp16(11, (B, Hkv, T, 128))
+    v = wl.random_fp16(12, (B, Hkv, T, 128), scale=3.0)
+    crafted = _crafted_vectors()
+    k[0, 0, :len(crafted)] = crafted
+    v[1, 2, :len(crafted)] = crafted
+    ctx = tqf.Context()
+    cache = tqf.Cache(tqf.MODES[mode], B, Hkv, cap, DEV)
+    cache.lengths.copy_(torch.tensor([5, 0], dtype=torch.int32))
+    tqf.tq_encode_append(ctx, cache, H.upload(k, DEV), H.upload(v, DEV))
+    torch.cuda.synchronize()
+    status = tqf.tq_get_status(ctx)
+    assert status == tqf.TQ_STATUS_NORM_OVERFLOW          # the -65504 vectors
+    assert cache.lengths.cpu().tolist() == [5 + T, T]
+    s = o.sign_vector(42)
+    total = near = bad = 0
+    for which, bits, x, data, norm in (("k", kb, k, cache.k_data, cache.k_norm),
+                                       ("v", vb, v, cache.v_data, cache.v_norm)):
+        for b, L0 in ((0, 5), (1, 0)):
+            got_rec = data[b, :, L0:L0 + T].cpu().numpy()
+            if bits == 16:
+                assert np.array_equal(got_rec.view(np.float16), x[b])
+                continue
+            idx, n16, u, ov = o.encode(x[b], o.codebook(bits), s)
+            got_n = norm[b, :, L0:L0 + T].cpu().numpy()
+            assert np.array_equal(got_n.view(np.uint16), n16.view(np.uint16)), (which, b)
+            got_idx = H.decode_records(got_rec, bits)
+            dist = o.boundary_distance(u, o.codebook(bits))
+            finite = ~ov[..., None] & np.ones_like(got_idx, bool)
+            diff = (got_idx != idx) & finite
+            total += int(finite.sum())
+            near += int((diff & (dist < H.BOUNDARY)).sum())
+            bad += int((diff & (dist >= H.BOUNDARY)).sum())
+            # records with no element near a midpoint must match the oracle's bytes
+            clean = ~np.any(dist < H.BOUNDARY, axis=-1) & ~ov
+            want_rec = o.pack_codes(idx, bits)
+            assert np.array_equal(got_rec[clean], want_rec[clean]), (which, b)
+    assert bad == 0
+    assert near <= max(1, H.BOUNDARY_FRACTION * total), (near, total)
+
+
+def test_encode_capacity_overflow_is_flagged_and_skipped():
+    ctx = tqf.Context()
+    cache = tqf.Cache(tqf.TQ_TURBO3, 2, 1, 16, DEV)
+    cache.lengths.copy_(torch.tensor([10, 2], dtype=torch.int32))
+    k = H.upload(wl.random_fp16(1, (2, 1, 8, 128)), DEV)
+    tqf.tq_encode_append(ctx, cache, k, k)
+    torch.cuda.synchronize()
+    assert tqf.tq_get_status(ctx) == tqf.TQ_STATUS_CAPACITY
+    assert cache.lengths.cpu().tolist() == [10, 10]
+    assert not cache.k_data[0].any().item()              # sequence 0 untouched
+
+
+# ---------------------------------------------------------------------------
+# end to end: each side encodes on its own, then decodes
+# ---------------------------------------------------------------------------
+def _e2e(mode, B, Hq, Hkv, L, Tq, cap, outliers_key):
+    w = wl.Workload(0, "test", mode, B, Hq, Hkv, L, tq=Tq)
+    k = np.stack([np.stack([wl.random_fp16(outliers_key + 10 * b + h, (L, 128))
+                            for h in range(Hkv)]) for b in range(B)])
+    k[..., [3, 50, 77, 120]] = (k[..., [3, 50, 77, 120]].astype(np.float32) * 8).astype(np.float16)
+    v = np.stack([np.stack([wl.random_fp16(outliers_key + 1000 + 10 * b + h, (L, 128))
+                            for h in range(Hkv)]) for b in range(B)])
+    q = wl.random_fp16(outliers_key + 77, (B, Hq, Tq, 128))
+    ctx = tqf.Context()
+    cache = tqf.Cache(tqf.MODES[mode], B, Hkv, cap, DEV)
+    tqf.tq_encode_append(ctx, cache, H.upload(k, DEV), H.upload(v, DEV))
+    got, status, _ = _run_decode(cache, q, Tq, L, ctx=ctx)
+    assert status == 0
+    kb, vb = H.MODE_BITS[mode]
+    s = o.sign_vector(42)
+    units = {}
+    for b in range(B):
+        for h in range(Hkv):
+            vi, vn, _, _ = o.encode(v[b, h], o.codebook(vb), s)
+            u = {"v_idx": vi, "v_norm": vn}
+            if kb == 16:
+                u["k"] = k[b, h]
+            else:
+                ki, kn, _, _ = o.encode(k[b, h], o.codebook(kb), s)
+                u["k_idx"], u["k_norm"] = ki, kn
+            units[(b, h)] = u
+    want = H.oracle_decode(mode, q, units, [L] * B, Hkv, Tq, 1 / math.sqrt(128), 1.0)
+    return H.assert_attention_close(got, want, f"e2e {mode}")
+
+
+@pytest.mark.parametrize("mode,B,Hq,Hkv,L,Tq,cap", [
+    ("turbo4_asym", 1, 4, 2, 256, 1, 256),
+    ("turbo3", 1, 28, 4, 1000, 1, 1024),
+    ("turbo4", 2, 32, 8, 700, 1, 704),
+    ("turbo3", 1, 32, 8, 600, 4, 608),
+])
+def test_end_to_end_own_encodings(mode, B, Hq, Hkv, L, Tq, cap):
+    _e2e(mode, B, Hq, Hkv, L, Tq, cap, 400 + L)
+
+
+def test_multistep_append_decode_lockstep():
+    """16 append+decode steps on the tiny Turbo4Asym shape (GQA 4/2), as in the
+    mlxcel parity test: the lengths stay in lockstep and every step is within
+    the bounds."""
+    w = wl.by_number(1)
+    B, Hq, Hkv, cap = w.batch, w.num_q_heads, w.num_kv_heads, 272
+    L0 = 240
+    s = o.sign_vector(w.rot_seed)
+    cbv = o.codebook(4)
+    ctx = tqf.Context()
+    cache = tqf.Cache(tqf.TQ_TURBO4_ASYM, B, Hkv, cap, DEV)
+    oc = {"mode": "turbo4_asym", "capacity": cap, "lengths": np.zeros(B, np.int32),
+          "k": np.zeros((B, Hkv, cap, 128), np.float16),
+          "v_data": np.zeros((B, Hkv, cap, 64), np.uint8),
+          "v_norm": np.zeros((B, Hkv, cap), np.float16)}
+    kall = np.stack([wl.keys(w, 0, h, 0, L0 + 16) for h in range(Hkv)])[None]
+    vall = np.stack([wl.values(w, 0, h, 0, L0 + 16) for h in range(Hkv)])[None]
+    tqf.tq_encode_append(ctx, cache, H.upload(kall[:, :, :L0], DEV), H.upload(vall[:, :, :L0], DEV))
+    o.encode_append(oc, kall[:, :, :L0], vall[:, :, :L0], None, cbv, s)
+    for step in range(16):
+        kn = np.ascontiguousarray(kall[:, :, L0 + step:L0 + step + 1])
+        vn = np.ascontiguousarray(vall[:, :, L0 + step:L0 + step + 1])
+        tqf.tq_encode_append(ctx, cache, H.upload(kn, DEV), H.upload(vn, DEV))
+        o.encode_append(oc, kn, vn, None, cbv, s)
+        L = int(oc["lengths"][0])
+        assert cache.lengths.cpu().tolist() == oc["lengths"].tolist()
+        q = wl.random_fp16(5000 + step, (B, Hq, 1, 128))
+        got, status, _ = _run_decode(cache, q, 1, L, ctx=ctx)
+        assert status == 0
+        units = {(0, h): {"k": oc["k"][0, h, :L], "v_idx": o.unpack_codes(oc["v_data"][0, h, :L], 4),
+                          "v_norm": oc["v_norm"][0, h, :L]} for h in range(Hkv)}
+        want = H.oracle_decode("turbo4_asym", q, units, [L], Hkv, 1, 1 / math.sqrt(128), 1.0)
+        H.assert_attention_close(got, want, f"step {step}")
