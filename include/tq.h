@@ -144,6 +144,33 @@ int tq_decode_attention(tq_ctx **ctx, const tq_cache *cache, const void *q,
                         int32_t num_q_heads, int32_t tq, int32_t max_len_hint,
                         float scale, void *out, void *stream);
 
+/*
+ * No-allocation decode (this entry point has no counterpart on the pages; it
+ * exists for callers that cannot allocate device memory on the decode path,
+ * e.g. a server that owns all device memory through its own pools, or a
+ * process under a hard memory budget, and that therefore cannot let
+ * tq_decode_attention create a context and grow its workspace).
+ *
+ * Same computation and arguments as tq_decode_attention, without a context:
+ * the split-K scratch lives in a fixed TQ_NOALLOC_SCRATCH_BYTES array that the
+ * library's CUDA module reserves on every GPU where it is loaded, until the
+ * process exits.  The call allocates nothing (no cudaMalloc/cudaFree).
+ *   status: device pointer to a caller-owned uint32 into which the kernels OR
+ *           TQ_STATUS_* bits (the caller clears it), or NULL to drop them.
+ *   Returns TQ_ERR_CAPACITY when the problem needs more scratch than the
+ *   array holds (batch * num_kv_heads * ceil(rows/16) split slots of 8320
+ *   bytes each must fit; the split count is reduced to fit when possible).
+ * The first call on a device, with that device current, looks up the array's
+ * address (cudaGetSymbolAddress, once per device); make that first call before
+ * any stream capture.  All calls share the one array and it keeps the last
+ * call's contents: calls that overlap on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller.
+ */
+#define TQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int tq_decode_attention_noalloc(const tq_cache *cache, const void *q, int32_t num_q_heads,
+                                int32_t tq, int32_t max_len_hint, float scale, void *out,
+                                uint32_t *status, void *stream);
+
 /* Release a context (device memory included).  tq_free(NULL) is a no-op. */
 void tq_free(tq_ctx *ctx);
 

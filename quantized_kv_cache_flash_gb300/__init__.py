@@ -41,6 +41,9 @@ _SIGS = {
     "tq_decode_attention": (_c.c_int, [_c.POINTER(_c.c_void_p), _c.c_void_p, _c.c_void_p,
                                        _c.c_int32, _c.c_int32, _c.c_int32, _c.c_float,
                                        _c.c_void_p, _c.c_void_p]),
+    "tq_decode_attention_noalloc": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32,
+                                               _c.c_int32, _c.c_float, _c.c_void_p, _c.c_void_p,
+                                               _c.c_void_p]),
     "tq_free": (None, [_c.c_void_p]),
     "tq_get_status": (_c.c_int, [_c.c_void_p, _c.POINTER(_c.c_uint32)]),
     "tq_lloyd_max_codebook": (_c.c_int, [_c.c_int32, _c.POINTER(_c.c_float)]),
@@ -221,6 +224,23 @@ def tq_decode_attention(ctx: Context, cache: Cache, q, out, max_len_hint: int,
                                      _ptr(q), int(q.shape[1]), int(q.shape[2]),
                                      int(max_len_hint), float(scale), _ptr(out),
                                      _stream(stream)), "tq_decode_attention")
+
+
+def tq_decode_attention_noalloc(cache: Cache, q, out, max_len_hint: int, scale: float = 0.0,
+                                status=None, stream=None) -> None:
+    """Decode without a context and without any device allocation: the split-K
+    scratch is the library's fixed device array (shared by all calls; serialise
+    calls that could overlap on the GPU).  `status` is an optional int32/uint32
+    device tensor of one element that the kernels OR status bits into."""
+    import torch
+    if q.dtype != torch.float16 or not q.is_contiguous() or q.dim() != 4:
+        raise ValueError("q must be contiguous fp16 [B, Hq, Tq, 128]")
+    if out.dtype != torch.float16 or not out.is_contiguous() or out.shape != q.shape:
+        raise ValueError("out must be contiguous fp16 shaped like q")
+    _check(lib().tq_decode_attention_noalloc(ctypes.byref(cache.struct), _ptr(q), int(q.shape[1]),
+                                             int(q.shape[2]), int(max_len_hint), float(scale),
+                                             _ptr(out), _ptr(status), _stream(stream)),
+           "tq_decode_attention_noalloc")
 
 
 def tq_free(ctx: Context) -> None:
