@@ -275,6 +275,7 @@ def gpu_arm(args, rank, world, device_index):
     tqf.tq_set_kernel_timing(ctx, True)
     tqf.tq_get_kernel_time(ctx)   # reset
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")   # ncu --nvtx --nvtx-include timed/ selects these launches
     if not flush:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -296,6 +297,7 @@ def gpu_arm(args, rank, world, device_index):
             evs.append((a, b))
         torch.cuda.synchronize()
         ms = sum(a.elapsed_time(b) for a, b in evs)
+    torch.cuda.nvtx.range_pop()
     clk = clocks.stop()
     kern_ms, kern_n = tqf.tq_get_kernel_time(ctx)
     tqf.tq_set_kernel_timing(ctx, False)

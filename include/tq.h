@@ -82,7 +82,9 @@ typedef struct tq_ctx tq_ctx;
  *           advances it on the device.
  *   Code layout of one record (dimension d, code kappa = sign<<(b-1) | rank,
  *   sign = 1 for the negative half of the codebook, rank 0 = smallest |c|):
- *     4-bit: kappa(d) in byte d/2, low nibble for even d.
+ *     4-bit: sixteen little-endian 32-bit words, word k = dims 8k..8k+7; bits
+ *            4j..4j+2 = rank of dim 8k+j; bit 8j+7 = sign of dim 8k+j and bit
+ *            8j+3 = sign of dim 8k+4+j (j = 0..3).
  *     3-bit: four 12-byte quarters; quarter q = dims 32q..32q+31 as three
  *            little-endian 32-bit words w0..w2 at bytes 12q+4k; bits 4j..4j+2
  *            of wk = kappa(32q+8k+j), bit 4j+3 of wk = bit k of kappa(32q+24+j).

@@ -22,7 +22,7 @@ What it computes (plain, slow, obviously correct; float64 unless stated):
 * Encode: n16 = fp16 round-to-nearest-even of the exact L2 norm of the fp16
   input; u = Rot(x) / n (unrounded fp64 n), rounded to fp32; idx = the nearest
   codebook entry to that fp32 u in exact arithmetic, ties to the lower index.
-* Packing: sign-magnitude codes in the nibble / 3-bit layout spelled out in
+* Packing: sign-magnitude codes in the 4-bit / 3-bit layouts spelled out in
   ``pack_codes``.  Format choice; the pages give no byte layout (the 56-byte
   turbo3 block of smem-dequant-experiment.md, Hypothesis 1, is not broken down).
 * Dequant: rotated basis n16 * c[idx]; original basis Rot^-1 of that.
@@ -266,7 +266,10 @@ def record_bytes(bits: int) -> int:
 def pack_codes(idx: np.ndarray, bits: int) -> np.ndarray:
     """Pack [..., 128] ascending indices into [..., 16*bits] bytes.
 
-    4-bit: code of dimension d sits in byte d // 2, low nibble for even d.
+    4-bit: eight 32-bit little-endian words, word k = dimensions 8k .. 8k+7.
+    Bits 4j .. 4j+2 hold the magnitude rank of dimension 8k+j (j = 0..7); the
+    sign bits sit in the nibbles' top bits: bit 8j+7 = sign of dim 8k+j and
+    bit 8j+3 = sign of dim 8k+4+j (j = 0..3).
     3-bit: four 12-byte quarters; quarter q holds dimensions 32q .. 32q+31 as
     three little-endian 32-bit words w0, w1, w2 (bytes 12q + 4k).  In word k,
     bits 4j .. 4j+2 hold the code of dimension 32q + 8k + j (j = 0..7) and bit
@@ -277,8 +280,17 @@ def pack_codes(idx: np.ndarray, bits: int) -> np.ndarray:
     kap = kap.reshape(-1, D)
     n = kap.shape[0]
     if bits == 4:
-        out = (kap[:, 0::2] | (kap[:, 1::2] << 4)).astype(np.uint8)
-        return out.reshape(*shp, 64)
+        rank, sign = kap & 7, kap >> 3
+        words = np.zeros((n, 16), np.uint32)
+        for k in range(16):
+            w = np.zeros(n, np.uint32)
+            for j in range(8):
+                w |= rank[:, 8 * k + j] << (4 * j)
+            for j in range(4):
+                w |= sign[:, 8 * k + j] << (8 * j + 7)
+                w |= sign[:, 8 * k + 4 + j] << (8 * j + 3)
+            words[:, k] = w
+        return words.astype("<u4").view(np.uint8).reshape(*shp, 64)
     if bits != 3:
         raise ValueError("bits must be 3 or 4")
     words = np.zeros((n, 12), np.uint32)
@@ -300,8 +312,14 @@ def unpack_codes(packed: np.ndarray, bits: int) -> np.ndarray:
     n = p.shape[0]
     kap = np.zeros((n, D), np.uint32)
     if bits == 4:
-        kap[:, 0::2] = p & 15
-        kap[:, 1::2] = p >> 4
+        words = p.view("<u4").astype(np.uint32)
+        for k in range(16):
+            w = words[:, k]
+            for j in range(8):
+                kap[:, 8 * k + j] = (w >> (4 * j)) & 7
+            for j in range(4):
+                kap[:, 8 * k + j] |= ((w >> (8 * j + 7)) & 1) << 3
+                kap[:, 8 * k + 4 + j] |= ((w >> (8 * j + 3)) & 1) << 3
     elif bits == 3:
         words = p.view("<u4").astype(np.uint32)
         for q in range(4):

@@ -244,10 +244,10 @@ int prepare_kmap(tq_ctx* ctx, const tq_cache* c) {
     return TQ_OK;
 }
 
-void plan(int kb, int vb, int batch, int hkv, int row_groups, int max_len, int* split_tokens,
-          int* nsplit) {
+void plan(int kb, int vb, int group_rows, int batch, int hkv, int row_groups, int max_len,
+          int* split_tokens, int* nsplit) {
     const long long units = 1ll * batch * hkv * row_groups;
-    const int cps = tq::decode_ctas_per_sm(kb, vb);
+    const int cps = tq::decode_ctas_per_sm(kb, vb, group_rows);
     // aim for ~2 waves of CTAs over the context, splits a multiple of 32 tokens
     const long long target_ctas = 2ll * kSMs * cps;
     long long per_unit = (target_ctas + units - 1) / units;
@@ -333,8 +333,9 @@ int tq_plan_splits(int32_t mode, int32_t batch, int32_t num_kv_heads, int32_t ro
     if (batch <= 0 || num_kv_heads <= 0 || rows_per_kv_head <= 0 || max_len_hint <= 0 ||
         split_tokens == nullptr || num_splits == nullptr)
         return TQ_ERR_INVALID_ARG;
-    const int rg = (rows_per_kv_head + 15) / 16;
-    plan(kb, vb, batch, num_kv_heads, rg, max_len_hint, split_tokens, num_splits);
+    const int gr = tq::group_rows_for(rows_per_kv_head);
+    const int rg = (rows_per_kv_head + gr - 1) / gr;
+    plan(kb, vb, gr, batch, num_kv_heads, rg, max_len_hint, split_tokens, num_splits);
     return TQ_OK;
 }
 
@@ -395,9 +396,11 @@ int tq_decode_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t
     if ((r = prepare_tables(ctx, c, kb, vb)) != TQ_OK) return r;
     if (kb == 16 && (r = prepare_kmap(ctx, c)) != TQ_OK) return r;
 
-    const int row_groups = (rows + 15) / 16;
+    const int group_rows = tq::group_rows_for(rows);
+    const int row_groups = (rows + group_rows - 1) / group_rows;
     int split_tokens, nsplit;
-    plan(kb, vb, c->batch, c->num_kv_heads, row_groups, max_len_hint, &split_tokens, &nsplit);
+    plan(kb, vb, group_rows, c->batch, c->num_kv_heads, row_groups, max_len_hint, &split_tokens,
+         &nsplit);
     const size_t slots = size_t(c->batch) * c->num_kv_heads * row_groups * nsplit * 16;
     if ((r = ensure_work(ctx, slots * (kD + 2) * sizeof(float))) != TQ_OK) return r;
 
@@ -419,6 +422,7 @@ int tq_decode_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t
     p.tq = tq_rows;
     p.rows = rows;
     p.row_groups = row_groups;
+    p.group_rows = group_rows;
     p.cap = c->capacity;
     p.max_len = max_len_hint;
     p.split_tokens = split_tokens;
@@ -458,6 +462,7 @@ int tq_decode_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t
     cp.group = group;
     cp.tq = tq_rows;
     cp.row_groups = row_groups;
+    cp.group_rows = group_rows;
     cp.max_len = max_len_hint;
     cp.split_tokens = split_tokens;
     cp.nsplit = nsplit;

@@ -25,11 +25,13 @@
 
 namespace tq {
 
-template <int KB, int VB>
+template <int KB, int VB, int NT>
 struct DecCfg {
     static constexpr int kWarps = 4;
-    static constexpr int kChunk = 32;                       // tokens per warp stage
-    static constexpr int kStages = (KB == 0) ? 3 : 4;
+    static constexpr int kChunk = 32;                       // tokens per warp stage (2 MMA tiles)
+    static constexpr int kStages = (KB == 0 || NT == 1) ? 2 : 3;
+    static constexpr int kRows = 8 * NT;                    // query rows per row group
+    static constexpr int kMinCtas = (NT == 1) ? 4 : 3;      // resident CTAs per SM targeted
     static constexpr int kRbK = (KB == 0) ? 256 : KB * 16;  // bytes per K record
     static constexpr int kRbV = VB * 16;
     static constexpr int kKBytes = kChunk * kRbK;
@@ -42,26 +44,55 @@ struct DecCfg {
     static constexpr int kStageAlign = (KB == 0) ? 1024 : 128;
     static constexpr int kStage = (kStageRaw + kStageAlign - 1) / kStageAlign * kStageAlign;
     static constexpr int kPipeBytes = kWarps * kStages * kStage;
-    static constexpr int kQOff = kPipeBytes;                 // fp32 [16][128] query rows
-    static constexpr int kBarOff = kQOff + 16 * kD * 4;
+    static constexpr int kQOff = kPipeBytes;                 // fp32 [kRows][128] query rows
+    static constexpr int kBarOff = kQOff + kRows * kD * 4;
     static constexpr int kSmem = kBarOff + kWarps * kStages * 8;
     static constexpr int kSmemAlloc = kSmem + 1024;          // base alignment slack
-    // epilogue scratch (reuses the pipeline): per warp O[16][kOStride] + (m, l)[16]
-    static constexpr int kOStride = kD + 8;
-    static_assert(kWarps * 16 * kOStride * 4 + kWarps * 16 * 8 <= kPipeBytes, "scratch");
+    // epilogue scratch (reuses the pipeline): per warp O[kRows][kOStride] + (m, l)[kRows]
+    static constexpr int kOStride = kD + 4;
+    static_assert(kWarps * kRows * kOStride * 4 + kWarps * kRows * 8 <= kPipeBytes, "scratch");
 };
 
-template <int KB, int VB>
-__global__ void __launch_bounds__(128)
+template <int KB, int COL>
+__device__ __forceinline__ void dequant_quarter_q(const uint8_t* rec, const Tables& t,
+                                                  uint32_t (&q)[8][4]) {
+    if constexpr (KB == 3) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(rec);
+        dequant3_quarter_q<COL>(w[0], w[1], w[2], t, q);
+    } else {
+        dequant4_quarter_q<COL>(*reinterpret_cast<const uint4*>(rec), t, q);
+    }
+}
+
+template <int KB>
+__device__ __forceinline__ void dequant_quarter(const uint8_t* rec, const Tables& t,
+                                                uint32_t (&h)[16]) {
+    if constexpr (KB == 3) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(rec);
+        dequant3_quarter(w[0], w[1], w[2], t, h);
+    } else {
+        dequant4_quarter(*reinterpret_cast<const uint4*>(rec), t, h);
+    }
+}
+
+// One CTA: 4 warps on one (split, batch*kv-head, row group).  Per 16-token
+// tile a warp runs
+//   S^T[16 tok x 8 rows]  = C_k[16 x 128] . Rot(q)^T      (8 k-steps per row tile)
+//   O^T[128 x 8 rows]    += C_v^T[128 x 16 tok] . (P n_v)^T (8 dim tiles)
+// with the tokens (M = 16) dequantised in registers: a thread owns tokens g and
+// g+8 of the tile and decodes its quarter t (32 dims) of both records.
+template <int KB, int VB, int NT>
+__global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
     tq_decode_kernel(const __grid_constant__ DecodeParams p,
                      const __grid_constant__ CUtensorMap kmap) {
-    using C = DecCfg<KB, VB>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    using C = DecCfg<KB, VB, NT>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned base, derived from smem_raw by an integer offset so the
+    // compiler keeps every access in the shared window (LDS, not generic loads)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, tig = lane & 3;
+    const int g = lane >> 2, t = lane & 3;
     const int split = blockIdx.x, unit = blockIdx.y, rg = blockIdx.z;
     const int b = unit / p.hkv, h = unit - b * p.hkv;
     const int L = p.lengths[b];
@@ -108,8 +139,8 @@ __global__ void __launch_bounds__(128)
 
     // ---- query rows of this row group -> shared (rotated for quantized K) ----
     float* sQ = reinterpret_cast<float*>(smem + C::kQOff);
-    const int rbase = rg * 16;
-    for (int r = warp; r < 16; r += C::kWarps) {
+    const int rbase = rg * C::kRows;
+    for (int r = warp; r < C::kRows; r += C::kWarps) {
         const int rr = rbase + r;
         float v[4] = {0.f, 0.f, 0.f, 0.f};
         if (rr < p.rows) {
@@ -134,31 +165,41 @@ __global__ void __launch_bounds__(128)
     }
     __syncthreads();
 
-    // A fragments of the score MMA.  Quantized K: a thread's B operand is its
-    // token's quarter `tig` (dims 32*tig .. +31) in order, so logical k-index
-    // 16*kc + 2*tig + e maps to dim 32*tig + 4*kc + e (and +8 -> +2).
-    uint32_t qa[8][4];
+    // B fragments of the score MMA (k = head dims, n = query rows).  Quantized
+    // K: a thread's A operand is its tokens' quarter `t` in order, so logical
+    // k-index 16*kc + 2*t + e maps to dim 32*t + 4*kc + e (and +8 -> +2).
+    uint32_t qb[NT][8][2];
 #pragma unroll
-    for (int kc = 0; kc < 8; ++kc) {
-        int d0, d1;
-        if constexpr (KB != 0) { d0 = 32 * tig + 4 * kc; d1 = d0 + 2; }
-        else { d0 = 16 * kc + 2 * tig; d1 = d0 + 8; }
-        qa[kc][0] = pack_half2(sQ[g * kD + d0], sQ[g * kD + d0 + 1]);
-        qa[kc][1] = pack_half2(sQ[(g + 8) * kD + d0], sQ[(g + 8) * kD + d0 + 1]);
-        qa[kc][2] = pack_half2(sQ[g * kD + d1], sQ[g * kD + d1 + 1]);
-        qa[kc][3] = pack_half2(sQ[(g + 8) * kD + d1], sQ[(g + 8) * kD + d1 + 1]);
+    for (int n = 0; n < NT; ++n) {
+        const float* qr = sQ + (8 * n + g) * kD;
+#pragma unroll
+        for (int kc = 0; kc < 8; ++kc) {
+            int d0, d1;
+            if constexpr (KB != 0) { d0 = 32 * t + 4 * kc; d1 = d0 + 2; }
+            else { d0 = 16 * kc + 2 * t; d1 = d0 + 8; }
+            qb[n][kc][0] = pack_half2(qr[d0], qr[d0 + 1]);
+            qb[n][kc][1] = pack_half2(qr[d1], qr[d1 + 1]);
+        }
     }
 
     const Tables kt{p.ktab[0], p.ktab[1], p.ktab[2], p.ktab[3]};
     const Tables vt{p.vtab[0], p.vtab[1], p.vtab[2], p.vtab[3]};
-    // last visible token (inclusive) of the two rows this thread owns
-    const int lim0 = L - p.tq + ((rbase + g) % p.tq);
-    const int lim1 = L - p.tq + ((rbase + g + 8) % p.tq);
-
-    float O[16][4];
+    // last visible token (inclusive) of the rows 8n + 2t + e this thread owns
+    int lim[NT][2];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) lim[n][e] = L - p.tq + ((rbase + 8 * n + 2 * t + e) % p.tq);
+    const int all_visible_below = L - p.tq + 1;  // tokens below this are seen by every row
+
+    float O[NT][8][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) O[n][i][0] = O[n][i][1] = O[n][i][2] = O[n][i][3] = 0.f;
+    float m[NT][2], l[NT][2];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) m[n][0] = m[n][1] = -INFINITY, l[n][0] = l[n][1] = 0.f;
     bool stalled = false;
     int it = 0;
 
@@ -171,137 +212,163 @@ __global__ void __launch_bounds__(128)
         if (__any_sync(0xffffffffu, !ok)) { stalled = true; break; }
         const uint8_t* st = wpipe + stage * C::kStage;
         const int tok0 = t_begin + c * C::kChunk;
+        const int nvalid = min(C::kChunk, t_end - tok0);
+        const bool two = nvalid > 16;
+        const bool full = (nvalid == C::kChunk) && (tok0 + C::kChunk <= all_visible_below);
 
-#pragma unroll 1
-        for (int so = 0; so < C::kChunk; so += 16) {
-            if (tok0 + so >= t_end) break;
-            // ---------------- scores S = Rot(q) . C_k^T ----------------
-            float S[2][4];
+        // ---------------- scores S^T = C_k . Rot(q)^T ----------------
+        float x[2][NT][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
-                if constexpr (KB == 0) {
+        for (int tile = 0; tile < 2; ++tile) {
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int row = so + nt * 8 + (lane & 7);
-                        const int db = 4 * jj + (lane >> 3);  // 16-byte chunk 0..15 of the row
-                        const uint32_t addr = smem_u32(st) + (db >> 3) * 4096 + row * 128 +
-                                              ((((db & 7) ^ (row & 7))) << 4);
-                        uint32_t r0, r1, r2, r3;
-                        ldsm_x4(addr, r0, r1, r2, r3);
-                        mma_f16(S[nt], qa[2 * jj][0], qa[2 * jj][1], qa[2 * jj][2], qa[2 * jj][3], r0, r1);
-                        mma_f16(S[nt], qa[2 * jj + 1][0], qa[2 * jj + 1][1], qa[2 * jj + 1][2],
-                                qa[2 * jj + 1][3], r2, r3);
-                    }
-                } else {
-                    uint32_t hk[16];
-                    const uint8_t* rec = st + (so + nt * 8 + g) * C::kRbK + tig * (C::kRbK / 4);
-                    if constexpr (KB == 3) {
-                        const uint32_t* w = reinterpret_cast<const uint32_t*>(rec);
-                        dequant3_quarter(w[0], w[1], w[2], kt, hk);
-                    } else {
-                        dequant4_quarter(*reinterpret_cast<const uint4*>(rec), kt, hk);
-                    }
-#pragma unroll
-                    for (int kc = 0; kc < 8; ++kc)
-                        mma_f16(S[nt], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], hk[2 * kc],
-                                hk[2 * kc + 1]);
-                }
-            }
-
-            // ---------------- online softmax (log2 domain) ----------------
-            // this thread's tokens: so + {2tig, 2tig+1, 8+2tig, 9+2tig}
-            const int ta = so + 2 * tig, tb = so + 8 + 2 * tig;
-            float ks[4];
+            for (int n = 0; n < NT; ++n) x[tile][n][0] = x[tile][n][1] = x[tile][n][2] = x[tile][n][3] = 0.f;
+            if (tile == 1 && !two) break;
             if constexpr (KB == 0) {
-                ks[0] = ks[1] = ks[2] = ks[3] = p.scale_log2e;
+                const int mi = lane >> 3;
+                const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+                for (int kc = 0; kc < 8; ++kc) {
+                    const int db = 2 * kc + (mi >> 1);  // 16-byte chunk 0..15 of the row
+                    const uint32_t addr = smem_u32(st) + (db >> 3) * 4096 + row * 128 +
+                                          (((db & 7) ^ (row & 7)) << 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(addr, a0, a1, a2, a3);
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) mma_f16(x[tile][n], a0, a1, a2, a3, qb[n][kc][0], qb[n][kc][1]);
+                }
             } else {
-                const float2 na = __half22float2(*reinterpret_cast<const __half2*>(st + C::kKnOff + 2 * ta));
-                const float2 nb = __half22float2(*reinterpret_cast<const __half2*>(st + C::kKnOff + 2 * tb));
-                ks[0] = na.x * p.scale_log2e; ks[1] = na.y * p.scale_log2e;
-                ks[2] = nb.x * p.scale_log2e; ks[3] = nb.y * p.scale_log2e;
-            }
-            const float2 va = __half22float2(*reinterpret_cast<const __half2*>(st + C::kVnOff + 2 * ta));
-            const float2 vb = __half22float2(*reinterpret_cast<const __half2*>(st + C::kVnOff + 2 * tb));
-            const float nv[4] = {va.x, va.y, vb.x, vb.y};
-            const int tg[4] = {tok0 + ta, tok0 + ta + 1, tok0 + tb, tok0 + tb + 1};
-            float x0[4] = {S[0][0], S[0][1], S[1][0], S[1][1]};
-            float x1[4] = {S[0][2], S[0][3], S[1][2], S[1][3]};
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+                // A quad of k-step kc: (token g, dims 2kc), (token g+8, 2kc),
+                // (token g, 2kc+1), (token g+8, 2kc+1) in quarter-pair units
+                uint32_t aq[8][4];
+                dequant_quarter_q<KB, 0>(st + (tile * 16 + g) * C::kRbK + t * (C::kRbK / 4), kt, aq);
+                dequant_quarter_q<KB, 1>(st + (tile * 16 + g + 8) * C::kRbK + t * (C::kRbK / 4), kt, aq);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool valid = tg[i] < t_end;
-                x0[i] = (valid && tg[i] <= lim0) ? x0[i] * ks[i] : -INFINITY;
-                x1[i] = (valid && tg[i] <= lim1) ? x1[i] * ks[i] : -INFINITY;
-                mx0 = fmaxf(mx0, x0[i]);
-                mx1 = fmaxf(mx1, x1[i]);
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-            const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-            const float al0 = fast_exp2(m0 - base0), al1 = fast_exp2(m1 - base1);
-            m0 = mn0;
-            m1 = mn1;
-            float p0[4], p1[4], s0 = 0.f, s1 = 0.f;
+                for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                p0[i] = fast_exp2(x0[i] - base0);
-                p1[i] = fast_exp2(x1[i] - base1);
-                s0 += p0[i];
-                s1 += p1[i];
+                    for (int n = 0; n < NT; ++n)
+                        mma_f16(x[tile][n], aq[kc][0], aq[kc][1], aq[kc][2], aq[kc][3],
+                                qb[n][kc][0], qb[n][kc][1]);
             }
-            l0 = l0 * al0 + s0;
-            l1 = l1 * al1 + s1;
-            if (al0 != 1.f || al1 != 1.f) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    O[i][0] *= al0; O[i][1] *= al0;
-                    O[i][2] *= al1; O[i][3] *= al1;
-                }
-            }
-            float w0[4], w1[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool valid = tg[i] < t_end;
-                w0[i] = valid ? p0[i] * nv[i] : 0.f;
-                w1[i] = valid ? p1[i] * nv[i] : 0.f;
-            }
-            const uint32_t a0 = pack_half2(w0[0], w0[1]);
-            const uint32_t a1 = pack_half2(w1[0], w1[1]);
-            const uint32_t a2 = pack_half2(w0[2], w0[3]);
-            const uint32_t a3 = pack_half2(w1[2], w1[3]);
+        }
 
-            // ---------------- O += (P n_v) . C_v (rotated basis) ----------------
-            uint32_t bv0[16], bv1[16];
+        // ---------------- online softmax (log2 domain) ----------------
+        // thread's tokens: tile*16 + g (c0, c1) and tile*16 + g + 8 (c2, c3);
+        // rows 8n + 2t (c0, c2) and 8n + 2t + 1 (c1, c3)
+        float nv[2][2];
+#pragma unroll
+        for (int tile = 0; tile < 2; ++tile) {
+            const int ta = tile * 16 + g, tb = ta + 8;
+            float ka = p.scale_log2e, kb2 = p.scale_log2e;
+            if constexpr (KB != 0) {
+                ka *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * ta));
+                kb2 *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * tb));
+            }
+            nv[tile][0] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * ta));
+            nv[tile][1] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * tb));
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                x[tile][n][0] *= ka; x[tile][n][1] *= ka;
+                x[tile][n][2] *= kb2; x[tile][n][3] *= kb2;
+            }
+            if (!full) {
+                const int ga = tok0 + ta, gb = tok0 + tb;
+                const bool va = ga < t_end && (tile == 0 || two);
+                const bool vb = gb < t_end && (tile == 0 || two);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    x[tile][n][0] = (va && ga <= lim[n][0]) ? x[tile][n][0] : -INFINITY;
+                    x[tile][n][1] = (va && ga <= lim[n][1]) ? x[tile][n][1] : -INFINITY;
+                    x[tile][n][2] = (vb && gb <= lim[n][0]) ? x[tile][n][2] : -INFINITY;
+                    x[tile][n][3] = (vb && gb <= lim[n][1]) ? x[tile][n][3] : -INFINITY;
+                }
+                if (!va) nv[tile][0] = 0.f;
+                if (!vb) nv[tile][1] = 0.f;
+            }
+        }
+        // The exp2 base of a row stays at its running max until a score exceeds
+        // it by more than kSlack (log2 units); only then (warp-uniform slow
+        // path) is the true max taken and O, l rescaled.  So p <= 2^kSlack.
+        constexpr float kSlack = 4.f;
+        bool grow = false;
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float lim_x = m[n][e] + kSlack;
+                grow |= x[0][n][e] > lim_x || x[0][n][e + 2] > lim_x ||
+                        x[1][n][e] > lim_x || x[1][n][e + 2] > lim_x;
+            }
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float mx = fmaxf(fmaxf(x[0][n][e], x[0][n][e + 2]), fmaxf(x[1][n][e], x[1][n][e + 2]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float mn = fmaxf(m[n][e], mx);
+                    const float al = (m[n][e] == -INFINITY) ? 0.f : fast_exp2(m[n][e] - mn);
+                    m[n][e] = mn;
+                    l[n][e] *= al;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        O[n][i][e] *= al;
+                        O[n][i][e + 2] *= al;
+                    }
+                }
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float base = (m[n][e] == -INFINITY) ? 0.f : m[n][e];
+                float s = 0.f;
+#pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+                    x[tile][n][e] = fast_exp2(x[tile][n][e] - base);
+                    x[tile][n][e + 2] = fast_exp2(x[tile][n][e + 2] - base);
+                    s += x[tile][n][e] + x[tile][n][e + 2];
+                }
+                l[n][e] += s;
+            }
+
+        // ---------------- O^T += C_v^T . (P n_v)^T (rotated basis) ----------------
+#pragma unroll
+        for (int tile = 0; tile < 2; ++tile) {
+            if (tile == 1 && !two) break;
+            uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                pb0[n] = movtrans(pack_half2(x[tile][n][0] * nv[tile][0], x[tile][n][1] * nv[tile][0]));
+                pb1[n] = movtrans(pack_half2(x[tile][n][2] * nv[tile][1], x[tile][n][3] * nv[tile][1]));
+            }
+            // A quad of dim tile mt: transposed pairs 2mt, 2mt+1 of token block 0
+            // (tokens 0-7 of the tile) then of block 1 (tokens 8-15)
+            uint32_t vq[8][4];
             {
-                const uint8_t* rec = st + C::kVOff + (so + g) * C::kRbV + tig * (C::kRbV / 4);
-                if constexpr (VB == 3) {
-                    const uint32_t* w = reinterpret_cast<const uint32_t*>(rec);
-                    dequant3_quarter(w[0], w[1], w[2], vt, bv0);
-                } else {
-                    dequant4_quarter(*reinterpret_cast<const uint4*>(rec), vt, bv0);
+                uint32_t hv[16];
+                dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g) * C::kRbV + t * (C::kRbV / 4), vt, hv);
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    vq[mt][0] = movtrans(hv[2 * mt]);
+                    vq[mt][1] = movtrans(hv[2 * mt + 1]);
                 }
             }
             {
-                const uint8_t* rec = st + C::kVOff + (so + 8 + g) * C::kRbV + tig * (C::kRbV / 4);
-                if constexpr (VB == 3) {
-                    const uint32_t* w = reinterpret_cast<const uint32_t*>(rec);
-                    dequant3_quarter(w[0], w[1], w[2], vt, bv1);
-                } else {
-                    dequant4_quarter(*reinterpret_cast<const uint4*>(rec), vt, bv1);
+                uint32_t hv[16];
+                dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g + 8) * C::kRbV + t * (C::kRbV / 4), vt, hv);
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    vq[mt][2] = movtrans(hv[2 * mt]);
+                    vq[mt][3] = movtrans(hv[2 * mt + 1]);
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                bv0[i] = movtrans(bv0[i]);
-                bv1[i] = movtrans(bv1[i]);
-            }
+            for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-            for (int i = 0; i < 16; ++i) mma_f16(O[i], a0, a1, a2, a3, bv0[i], bv1[i]);
+                for (int n = 0; n < NT; ++n)
+                    mma_f16(O[n][mt], vq[mt][0], vq[mt][1], vq[mt][2], vq[mt][3], pb0[n], pb1[n]);
         }
 
         __syncwarp();
@@ -326,51 +393,63 @@ __global__ void __launch_bounds__(128)
     }
 
     // ---- combine the 4 warps of the CTA, write this split's partial ----
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    __syncthreads();  // every warp is done with its pipeline stages
-    float* sO = reinterpret_cast<float*>(smem) + warp * 16 * C::kOStride;
-    float* sML = reinterpret_cast<float*>(smem) + C::kWarps * 16 * C::kOStride;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int d = 32 * tig + 2 * i;
-        *reinterpret_cast<float2*>(sO + g * C::kOStride + d) = make_float2(O[i][0], O[i][1]);
-        *reinterpret_cast<float2*>(sO + (g + 8) * C::kOStride + d) = make_float2(O[i][2], O[i][3]);
-    }
-    if (tig == 0) {
-        sML[(warp * 16 + g) * 2 + 0] = m0;
-        sML[(warp * 16 + g) * 2 + 1] = l0;
-        sML[(warp * 16 + g + 8) * 2 + 0] = m1;
-        sML[(warp * 16 + g + 8) * 2 + 1] = l1;
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            l[n][e] += __shfl_xor_sync(0xffffffffu, l[n][e], 4);
+            l[n][e] += __shfl_xor_sync(0xffffffffu, l[n][e], 8);
+            l[n][e] += __shfl_xor_sync(0xffffffffu, l[n][e], 16);
+        }
+    __syncthreads();  // every warp is done with its pipeline stages
+    float* sO = reinterpret_cast<float*>(smem) + warp * C::kRows * C::kOStride;
+    float* sML = reinterpret_cast<float*>(smem) + C::kWarps * C::kRows * C::kOStride;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        const int r0 = 8 * n + 2 * t;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int dlo = 32 * (g >> 1) + 4 * mt + (g & 1);
+            sO[r0 * C::kOStride + dlo] = O[n][mt][0];
+            sO[(r0 + 1) * C::kOStride + dlo] = O[n][mt][1];
+            sO[r0 * C::kOStride + dlo + 2] = O[n][mt][2];
+            sO[(r0 + 1) * C::kOStride + dlo + 2] = O[n][mt][3];
+        }
+        if (g == 0) {
+            sML[(warp * C::kRows + r0) * 2 + 0] = m[n][0];
+            sML[(warp * C::kRows + r0) * 2 + 1] = l[n][0];
+            sML[(warp * C::kRows + r0 + 1) * 2 + 0] = m[n][1];
+            sML[(warp * C::kRows + r0 + 1) * 2 + 1] = l[n][1];
+        }
     }
     __syncthreads();
     {
-        const int r = threadIdx.x >> 3;
-        const int d0 = (threadIdx.x & 7) * 16;
+        constexpr int kPerRow = 128 / C::kRows;      // threads per row
+        constexpr int kDims = kD / kPerRow;          // dims per thread
+        const int r = threadIdx.x / kPerRow;
+        const int d0 = (threadIdx.x % kPerRow) * kDims;
         if (rbase + r < p.rows) {
             float mw[C::kWarps], M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < C::kWarps; ++w) {
-                mw[w] = sML[(w * 16 + r) * 2];
+                mw[w] = sML[(w * C::kRows + r) * 2];
                 M = fmaxf(M, mw[w]);
             }
             float sc[C::kWarps], lsum = 0.f;
 #pragma unroll
             for (int w = 0; w < C::kWarps; ++w) {
                 sc[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
-                lsum += sc[w] * sML[(w * 16 + r) * 2 + 1];
+                lsum += sc[w] * sML[(w * C::kRows + r) * 2 + 1];
             }
             const size_t pidx =
                 ((static_cast<size_t>(unit) * p.row_groups + rg) * p.nsplit + split) * 16 + r;
             float* po = p.part_o + pidx * kD + d0;
 #pragma unroll
-            for (int d = 0; d < 16; d += 4) {
+            for (int d = 0; d < kDims; d += 4) {
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int w = 0; w < C::kWarps; ++w) {
-                    const float* src = reinterpret_cast<float*>(smem) + (w * 16 + r) * C::kOStride + d0 + d;
+                    const float* src = reinterpret_cast<float*>(smem) + (w * C::kRows + r) * C::kOStride + d0 + d;
                     acc.x += sc[w] * src[0];
                     acc.y += sc[w] * src[1];
                     acc.z += sc[w] * src[2];
@@ -378,7 +457,7 @@ __global__ void __launch_bounds__(128)
                 }
                 *reinterpret_cast<float4*>(po + d) = acc;
             }
-            if ((threadIdx.x & 7) == 0) {
+            if ((threadIdx.x % kPerRow) == 0) {
                 p.part_ml[pidx * 2 + 0] = M;
                 p.part_ml[pidx * 2 + 1] = lsum;
             }
@@ -399,7 +478,7 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
     const int b = row / (p.tq * p.hq);
     const int kv = hq / p.group, hl = hq - kv * p.group;
     const int r = hl * p.tq + j;
-    const int rg = r >> 4, rl = r & 15;
+    const int rg = r / p.group_rows, rl = r - rg * p.group_rows;
     const int unit = b * p.hkv + kv;
     const int L = min(p.lengths[b], p.max_len);
     const int ns = min(p.nsplit, (L + p.split_tokens - 1) / p.split_tokens);
@@ -432,30 +511,38 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
     *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(row) * kD + lane * 4) = o;
 }
 
-template <int KB, int VB>
+template <int KB, int VB, int NT>
 static int launch_decode_t(const DecodeParams& p, const CUtensorMap* kmap, cudaStream_t stream,
                            cudaEvent_t ev0, cudaEvent_t ev1) {
-    using C = DecCfg<KB, VB>;
+    using C = DecCfg<KB, VB, NT>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tq_decode_kernel<KB, VB>,
+        cudaError_t e = cudaFuncSetAttribute(tq_decode_kernel<KB, VB, NT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid(p.nsplit, p.batch * p.hkv, p.row_groups);
     if (ev0) cudaEventRecord(ev0, stream);
-    tq_decode_kernel<KB, VB><<<grid, C::kWarps * 32, C::kSmemAlloc, stream>>>(p, *kmap);
+    tq_decode_kernel<KB, VB, NT><<<grid, C::kWarps * 32, C::kSmemAlloc, stream>>>(p, *kmap);
     cudaError_t e = cudaGetLastError();
     if (ev1) cudaEventRecord(ev1, stream);
     return e;
 }
 
+template <int NT>
+static int launch_decode_nt(int kbits, int vbits, const DecodeParams& p, const CUtensorMap* kmap,
+                            cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
+    if (kbits == 16 && vbits == 4) return launch_decode_t<0, 4, NT>(p, kmap, stream, ev0, ev1);
+    if (kbits == 3 && vbits == 3) return launch_decode_t<3, 3, NT>(p, kmap, stream, ev0, ev1);
+    if (kbits == 4 && vbits == 4) return launch_decode_t<4, 4, NT>(p, kmap, stream, ev0, ev1);
+    return cudaErrorInvalidValue;
+}
+
 int launch_decode(int kbits, int vbits, const DecodeParams& p, const CUtensorMap* kmap,
                   cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
-    if (kbits == 16 && vbits == 4) return launch_decode_t<0, 4>(p, kmap, stream, ev0, ev1);
-    if (kbits == 3 && vbits == 3) return launch_decode_t<3, 3>(p, kmap, stream, ev0, ev1);
-    if (kbits == 4 && vbits == 4) return launch_decode_t<4, 4>(p, kmap, stream, ev0, ev1);
+    if (p.group_rows == 8) return launch_decode_nt<1>(kbits, vbits, p, kmap, stream, ev0, ev1);
+    if (p.group_rows == 16) return launch_decode_nt<2>(kbits, vbits, p, kmap, stream, ev0, ev1);
     return cudaErrorInvalidValue;
 }
 
@@ -465,14 +552,21 @@ int launch_combine(const CombineParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-int decode_ctas_per_sm(int kbits, int vbits) {
+template <int KB, int VB>
+static int smem_of(int nt) {
+    return nt == 1 ? DecCfg<KB, VB, 1>::kSmemAlloc : DecCfg<KB, VB, 2>::kSmemAlloc;
+}
+
+int decode_ctas_per_sm(int kbits, int vbits, int group_rows) {
+    const int nt = group_rows <= 8 ? 1 : 2;
     int smem = 0;
-    if (kbits == 16) smem = DecCfg<0, 4>::kSmemAlloc;
-    else if (kbits == 3) smem = DecCfg<3, 3>::kSmemAlloc;
-    else smem = DecCfg<4, 4>::kSmemAlloc;
+    if (kbits == 16) smem = smem_of<0, 4>(nt);
+    else if (kbits == 3) smem = smem_of<3, 3>(nt);
+    else smem = smem_of<4, 4>(nt);
     int by_smem = (228 * 1024) / (smem + 1024);  // 1 KB per CTA is reserved
-    if (by_smem < 1) by_smem = 1;
-    return by_smem < 3 ? by_smem : 3;
+    const int by_regs = nt == 1 ? 4 : 3;         // the kernels' launch bounds
+    int c = by_smem < by_regs ? by_smem : by_regs;
+    return c < 1 ? 1 : c;
 }
 
 }  // namespace tq

@@ -192,42 +192,74 @@ __device__ __forceinline__ void lut4(uint32_t sel, const Tables& t, uint32_t& h0
 // dim 24+j, gathered into nibbles by three masked shifts.
 __device__ __forceinline__ void dequant3_quarter(uint32_t w0, uint32_t w1, uint32_t w2,
                                                  const Tables& t, uint32_t (&h)[16]) {
+    // right shifts as multiply-high (FMA pipe) to leave the ALU pipe to prmt
     const uint32_t m0 = w0 & 0x77777777u;
     const uint32_t m1 = w1 & 0x77777777u;
     const uint32_t m2 = w2 & 0x77777777u;
-    const uint32_t sp = ((w0 >> 3) & 0x11111111u) | ((w1 >> 2) & 0x22222222u) |
-                        ((w2 >> 1) & 0x44444444u);
+    const uint32_t sp = (__umulhi(w0, 1u << 29) & 0x11111111u) |
+                        (__umulhi(w1, 1u << 30) & 0x22222222u) |
+                        (__umulhi(w2, 1u << 31) & 0x44444444u);
     lut4(m0, t, h[0], h[1]);
-    lut4(m0 >> 16, t, h[2], h[3]);
+    lut4(__umulhi(m0, 1u << 16), t, h[2], h[3]);
     lut4(m1, t, h[4], h[5]);
-    lut4(m1 >> 16, t, h[6], h[7]);
+    lut4(__umulhi(m1, 1u << 16), t, h[6], h[7]);
     lut4(m2, t, h[8], h[9]);
-    lut4(m2 >> 16, t, h[10], h[11]);
+    lut4(__umulhi(m2, 1u << 16), t, h[10], h[11]);
     lut4(sp, t, h[12], h[13]);
-    lut4(sp >> 16, t, h[14], h[15]);
+    lut4(__umulhi(sp, 1u << 16), t, h[14], h[15]);
 }
 
-// 4-bit: eight dims of one word w (nibble j = code of dim j, bit 3 = sign).
-// The tables hold the 8 magnitudes (indexed by rank); the sign bit of each
-// code is turned into a byte mask with prmt's sign-replicate mode and OR-ed
-// into the high byte.
+// 4-bit: eight dims of one word w.  Bits 4j..4j+2 = magnitude rank of dim j;
+// the tables hold the 8 magnitudes (indexed by rank).  The sign of dim j < 4
+// sits in bit 8j+7 and that of dim 4+j in bit 8j+3, i.e. exactly where the
+// fp16 sign bit of the gathered high byte goes (directly for dims 0..3, after
+// a shift by 4 for dims 4..7), so one logic op applies four signs.
 __device__ __forceinline__ void dequant4_word(uint32_t w, const Tables& t, uint32_t& h0,
                                               uint32_t& h1, uint32_t& h2, uint32_t& h3) {
     const uint32_t rk = w & 0x77777777u;
-    const uint32_t w4 = w << 4;
     {
         const uint32_t L = prmt(t.lo0, t.lo1, rk);
-        const uint32_t H = prmt(t.hi0, t.hi1, rk) | (prmt(w4, w, 0xD9C8) & 0x80808080u);
+        const uint32_t H = prmt(t.hi0, t.hi1, rk) | (w & 0x80808080u);
         h0 = prmt(L, H, 0x5140);
         h1 = prmt(L, H, 0x7362);
     }
     {
-        const uint32_t r2 = rk >> 16;
+        const uint32_t r2 = __umulhi(rk, 1u << 16);  // rk >> 16, on the FMA pipe
+        const uint32_t w4 = w << 4;
         const uint32_t L = prmt(t.lo0, t.lo1, r2);
-        const uint32_t H = prmt(t.hi0, t.hi1, r2) | (prmt(w4, w, 0xFBEA) & 0x80808080u);
+        const uint32_t H = prmt(t.hi0, t.hi1, r2) | (w4 & 0x80808080u);
         h2 = prmt(L, H, 0x5140);
         h3 = prmt(L, H, 0x7362);
     }
+}
+
+// Quarter dequantisers that write pair i straight into slot q[i/2][COL + 2*(i%2)]
+// of an 8 x 4 array of MMA operand quads (no register copies to form quads).
+template <int COL>
+__device__ __forceinline__ void dequant3_quarter_q(uint32_t w0, uint32_t w1, uint32_t w2,
+                                                   const Tables& t, uint32_t (&q)[8][4]) {
+    const uint32_t m0 = w0 & 0x77777777u;
+    const uint32_t m1 = w1 & 0x77777777u;
+    const uint32_t m2 = w2 & 0x77777777u;
+    const uint32_t sp = (__umulhi(w0, 1u << 29) & 0x11111111u) |
+                        (__umulhi(w1, 1u << 30) & 0x22222222u) |
+                        (__umulhi(w2, 1u << 31) & 0x44444444u);
+    lut4(m0, t, q[0][COL], q[0][COL + 2]);
+    lut4(__umulhi(m0, 1u << 16), t, q[1][COL], q[1][COL + 2]);
+    lut4(m1, t, q[2][COL], q[2][COL + 2]);
+    lut4(__umulhi(m1, 1u << 16), t, q[3][COL], q[3][COL + 2]);
+    lut4(m2, t, q[4][COL], q[4][COL + 2]);
+    lut4(__umulhi(m2, 1u << 16), t, q[5][COL], q[5][COL + 2]);
+    lut4(sp, t, q[6][COL], q[6][COL + 2]);
+    lut4(__umulhi(sp, 1u << 16), t, q[7][COL], q[7][COL + 2]);
+}
+
+template <int COL>
+__device__ __forceinline__ void dequant4_quarter_q(uint4 w, const Tables& t, uint32_t (&q)[8][4]) {
+    dequant4_word(w.x, t, q[0][COL], q[0][COL + 2], q[1][COL], q[1][COL + 2]);
+    dequant4_word(w.y, t, q[2][COL], q[2][COL + 2], q[3][COL], q[3][COL + 2]);
+    dequant4_word(w.z, t, q[4][COL], q[4][COL + 2], q[5][COL], q[5][COL + 2]);
+    dequant4_word(w.w, t, q[6][COL], q[6][COL + 2], q[7][COL], q[7][COL + 2]);
 }
 
 __device__ __forceinline__ void dequant4_quarter(uint4 w, const Tables& t,

@@ -151,10 +151,17 @@ __device__ __forceinline__ void encode_vector(const __half* src, uint8_t* dst, _
     for (int i = 0; i < 4; ++i) code[i] = quantize_code<BITS>(x[i] * inv, gt, ge);
 
     if constexpr (BITS == 4) {
-        // code of dim d -> nibble d of the record
-        const uint32_t nib = code[0] | (code[1] << 4) | (code[2] << 8) | (code[3] << 12);
-        const uint32_t up = __shfl_down_sync(0xffffffffu, nib, 1);
-        if ((lane & 1) == 0) reinterpret_cast<uint32_t*>(dst)[lane >> 1] = nib | (up << 16);
+        // word k = dims 8k..8k+7 (lanes 2k, 2k+1): rank of dim 8k+j in bits
+        // 4j..4j+2; sign of dim 8k+j (j < 4) in bit 8j+7, of dim 8k+4+j in bit 8j+3
+        const bool upper = (lane & 1) != 0;
+        uint32_t part = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            part |= (code[i] & 7u) << (4 * i + (upper ? 16 : 0));
+            part |= (code[i] >> 3) << (8 * i + (upper ? 3 : 7));
+        }
+        const uint32_t other = __shfl_down_sync(0xffffffffu, part, 1);
+        if (!upper) reinterpret_cast<uint32_t*>(dst)[lane >> 1] = part | other;
     } else {
         // quarter q = lanes 8q..8q+7; lanes 8q+2k, 8q+2k+1 carry dims 32q+8k..+7
         // (word k's nibbles); lanes 8q+6, 8q+7 carry dims 32q+24..31, whose

@@ -9,8 +9,9 @@
 namespace tq {
 
 // Decode (split-K) kernel parameters.  One CTA = one (split, batch*kv-head,
-// row group); a row group is up to 16 query rows (GQA heads x Tq) of one KV
-// head, the M dimension of the warp-level MMA.
+// row group); a row group is up to group_rows (8 or 16) query rows (GQA heads
+// x Tq) of one KV head: the N dimension of the warp-level MMAs, whose M
+// dimension is 16 tokens.
 struct DecodeParams {
     const uint8_t* k_codes;   // packed K codes (unused for fp16 K)
     const __half* k_norm;     // fp16 K norms (unused for fp16 K)
@@ -21,7 +22,7 @@ struct DecodeParams {
     float* part_o;            // [units, row_groups, nsplit, 16, 128]
     float* part_ml;           // [units, row_groups, nsplit, 16, 2]  (running max in log2 units, sum)
     uint32_t* status;
-    int32_t batch, hkv, hq, group, tq, rows, row_groups, cap, max_len;
+    int32_t batch, hkv, hq, group, tq, rows, row_groups, group_rows, cap, max_len;
     int32_t split_tokens, nsplit;
     float scale_log2e;        // softmax scale * log2(e)
     uint32_t ktab[4];         // prmt byte tables of the K codebook (lo0, lo1, hi0, hi1)
@@ -35,7 +36,7 @@ struct CombineParams {
     const int32_t* lengths;
     __half* out;              // [B, Hq, Tq, 128]
     uint32_t* status;
-    int32_t batch, hkv, hq, group, tq, row_groups, max_len, split_tokens, nsplit;
+    int32_t batch, hkv, hq, group, tq, row_groups, group_rows, max_len, split_tokens, nsplit;
     float v_rescale;
     uint32_t signs[4];
 };
@@ -58,12 +59,16 @@ struct EncodeParams {
 };
 
 // Launchers (return a cudaError_t value).
+// group_rows (p.group_rows) selects the 8- or 16-row variant.
 int launch_decode(int kbits, int vbits, const DecodeParams& p, const CUtensorMap* kmap,
                   cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end);
 int launch_combine(const CombineParams& p, cudaStream_t stream);
 int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stream);
 
-// Shape of the decode kernel's per-warp stage (for the host planner).
-int decode_ctas_per_sm(int kbits, int vbits);
+// Resident CTAs per SM of a decode variant (for the host split planner).
+int decode_ctas_per_sm(int kbits, int vbits, int group_rows);
+
+// Query rows per row group for `rows` query rows of one KV head.
+inline int group_rows_for(int rows) { return rows <= 8 ? 8 : 16; }
 
 }  // namespace tq

@@ -150,7 +150,8 @@ extern "C" int tq_decode_attention_noalloc(const tq_cache* c, const void* q, int
     const int group = num_q_heads / c->num_kv_heads;
     const int rows = group * tq_rows;
     if (rows > 256) return TQ_ERR_UNSUPPORTED;
-    const int row_groups = (rows + 15) / 16;
+    const int group_rows = tq::group_rows_for(rows);
+    const int row_groups = (rows + group_rows - 1) / group_rows;
 
     // split plan, limited to what the fixed scratch holds
     int split_tokens = 0, nsplit = 0;
@@ -196,6 +197,7 @@ extern "C" int tq_decode_attention_noalloc(const tq_cache* c, const void* q, int
     p.tq = tq_rows;
     p.rows = rows;
     p.row_groups = row_groups;
+    p.group_rows = group_rows;
     p.cap = c->capacity;
     p.max_len = max_len_hint;
     p.split_tokens = split_tokens;
@@ -239,6 +241,7 @@ extern "C" int tq_decode_attention_noalloc(const tq_cache* c, const void* q, int
     cp.group = group;
     cp.tq = tq_rows;
     cp.row_groups = row_groups;
+    cp.group_rows = group_rows;
     cp.max_len = max_len_hint;
     cp.split_tokens = split_tokens;
     cp.nsplit = nsplit;

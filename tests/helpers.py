@@ -43,9 +43,12 @@ def decode_records(packed: np.ndarray, bits: int) -> np.ndarray:
     p = np.ascontiguousarray(packed, np.uint8).reshape(-1, packed.shape[-1])
     n = p.shape[0]
     if bits == 4:
-        kappa = np.empty((n, 128), np.int64)
-        kappa[:, 0::2] = p & 0x0F
-        kappa[:, 1::2] = p >> 4
+        w = p.view("<u4").astype(np.int64).reshape(n, 16)       # [vec, word]
+        j = np.arange(8)
+        rank = (w[:, :, None] >> (4 * j)) & 7                   # dims 8k + j
+        s_lo = (w[:, :, None] >> (8 * j[:4] + 7)) & 1           # sign of dims 8k + 0..3
+        s_hi = (w[:, :, None] >> (8 * j[:4] + 3)) & 1           # sign of dims 8k + 4..7
+        kappa = (rank | (np.concatenate([s_lo, s_hi], axis=2) << 3)).reshape(n, 128)
     else:
         w = p.view("<u4").astype(np.int64).reshape(n, 4, 3)     # [vec, quarter, word]
         j = np.arange(8)

@@ -276,12 +276,15 @@ def test_pack_hand_computed_bytes():
     want = bytearray(48)
     want[0] = 0x80; want[4] = 0x80; want[17] = 0x07
     assert bytes(p) == bytes(want)
-    # 4-bit: dim 5 = index 15 (code 7) -> byte 2 high nibble; dim 6 = index 0 (code 15)
-    # -> byte 3 low nibble; background index 8 (code 0)
+    # 4-bit, background index 8 (+m0: sign 0, rank 0).  dim 5 = index 15 (+m7):
+    # rank 7 in bits 20-22 -> byte 2 = 0x70.  dim 6 = index 0 (-m7): rank 7 in
+    # bits 24-26 -> byte 3 = 0x07, sign at bit 8*2+3 = 19 -> byte 2 |= 0x08.
+    # dim 1 = index 7 (-m0): rank 0, sign at bit 8*1+7 = 15 -> byte 1 = 0x80.
+    # dim 8 (word 1) = index 9 (+m1): rank 1 in bits 32-34 -> byte 4 = 0x01.
     idx = np.full((1, 128), 8, np.uint8)
-    idx[0, 5] = 15; idx[0, 6] = 0
+    idx[0, 5] = 15; idx[0, 6] = 0; idx[0, 1] = 7; idx[0, 8] = 9
     p = o.pack_codes(idx, 4)[0]
-    want = bytearray(64); want[2] = 0x70; want[3] = 0x0F
+    want = bytearray(64); want[1] = 0x80; want[2] = 0x78; want[3] = 0x07; want[4] = 0x01
     assert bytes(p) == bytes(want)
 
 
