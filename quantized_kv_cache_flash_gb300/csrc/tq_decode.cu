@@ -20,6 +20,8 @@
 // V operand comes from the same dequant followed by an 8x8 transpose.
 #include <float.h>
 
+#include <type_traits>
+
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
@@ -91,7 +93,10 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
     // compiler keeps every access in the shared window (LDS, not generic loads)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // warp index through a shuffle so the compiler treats it (and the chunk,
+    // stage and copy addresses derived from it) as warp-uniform
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
+    const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int split = blockIdx.x, unit = blockIdx.y, rg = blockIdx.z;
     const int b = unit / p.hkv, h = unit - b * p.hkv;
@@ -201,193 +206,197 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
 #pragma unroll
     for (int n = 0; n < NT; ++n) m[n][0] = m[n][1] = -INFINITY, l[n][0] = l[n][1] = 0.f;
     bool stalled = false;
-    int it = 0;
 
-    for (;; ++it) {
-        const int c = warp + C::kWarps * it;
-        if (c >= nchunks) break;
-        const int stage = it % C::kStages;
-        const uint32_t parity = (it / C::kStages) & 1;
-        const bool ok = mbar_wait_bounded(bar0 + 8 * stage, parity);
+    // One 32-token chunk of this warp.  FULL: all 32 tokens valid and visible
+    // to every row (no masking); otherwise the tail / causal path.
+    auto process = [&](const uint8_t* st, const int tok0, auto full_tag) {
+        constexpr bool FULL = decltype(full_tag)::value;
+        const int nvalid = FULL ? C::kChunk : min(C::kChunk, t_end - tok0);
+        const bool two = FULL || nvalid > 16;
+            // ---------------- scores S^T = C_k . Rot(q)^T ----------------
+            float x[2][NT][4];
+    #pragma unroll
+            for (int tile = 0; tile < 2; ++tile) {
+    #pragma unroll
+                for (int n = 0; n < NT; ++n) x[tile][n][0] = x[tile][n][1] = x[tile][n][2] = x[tile][n][3] = 0.f;
+                if (!FULL && tile == 1 && !two) break;
+                if constexpr (KB == 0) {
+                    const int mi = lane >> 3;
+                    const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
+    #pragma unroll
+                    for (int kc = 0; kc < 8; ++kc) {
+                        const int db = 2 * kc + (mi >> 1);  // 16-byte chunk 0..15 of the row
+                        const uint32_t addr = smem_u32(st) + (db >> 3) * 4096 + row * 128 +
+                                              (((db & 7) ^ (row & 7)) << 4);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(addr, a0, a1, a2, a3);
+    #pragma unroll
+                        for (int n = 0; n < NT; ++n) mma_f16(x[tile][n], a0, a1, a2, a3, qb[n][kc][0], qb[n][kc][1]);
+                    }
+                } else {
+                    // A quad of k-step kc: (token g, dims 2kc), (token g+8, 2kc),
+                    // (token g, 2kc+1), (token g+8, 2kc+1) in quarter-pair units
+                    uint32_t aq[8][4];
+                    dequant_quarter_q<KB, 0>(st + (tile * 16 + g) * C::kRbK + t * (C::kRbK / 4), kt, aq);
+                    dequant_quarter_q<KB, 1>(st + (tile * 16 + g + 8) * C::kRbK + t * (C::kRbK / 4), kt, aq);
+    #pragma unroll
+                    for (int kc = 0; kc < 8; ++kc)
+    #pragma unroll
+                        for (int n = 0; n < NT; ++n)
+                            mma_f16(x[tile][n], aq[kc][0], aq[kc][1], aq[kc][2], aq[kc][3],
+                                    qb[n][kc][0], qb[n][kc][1]);
+                }
+            }
+
+            // ---------------- online softmax (log2 domain) ----------------
+            // thread's tokens: tile*16 + g (c0, c1) and tile*16 + g + 8 (c2, c3);
+            // rows 8n + 2t (c0, c2) and 8n + 2t + 1 (c1, c3)
+            float nv[2][2];
+    #pragma unroll
+            for (int tile = 0; tile < 2; ++tile) {
+                const int ta = tile * 16 + g, tb = ta + 8;
+                float ka = p.scale_log2e, kb2 = p.scale_log2e;
+                if constexpr (KB != 0) {
+                    ka *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * ta));
+                    kb2 *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * tb));
+                }
+                nv[tile][0] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * ta));
+                nv[tile][1] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * tb));
+    #pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    x[tile][n][0] *= ka; x[tile][n][1] *= ka;
+                    x[tile][n][2] *= kb2; x[tile][n][3] *= kb2;
+                }
+                if constexpr (!FULL) {
+                    const int ga = tok0 + ta, gb = tok0 + tb;
+                    const bool va = ga < t_end && (tile == 0 || two);
+                    const bool vb = gb < t_end && (tile == 0 || two);
+    #pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        x[tile][n][0] = (va && ga <= lim[n][0]) ? x[tile][n][0] : -INFINITY;
+                        x[tile][n][1] = (va && ga <= lim[n][1]) ? x[tile][n][1] : -INFINITY;
+                        x[tile][n][2] = (vb && gb <= lim[n][0]) ? x[tile][n][2] : -INFINITY;
+                        x[tile][n][3] = (vb && gb <= lim[n][1]) ? x[tile][n][3] : -INFINITY;
+                    }
+                    if (!va) nv[tile][0] = 0.f;
+                    if (!vb) nv[tile][1] = 0.f;
+                }
+            }
+            // The exp2 base of a row stays at its running max until a score exceeds
+            // it by more than kSlack (log2 units); only then (warp-uniform slow
+            // path) is the true max taken and O, l rescaled.  So p <= 2^kSlack.
+            constexpr float kSlack = 4.f;
+            bool grow = false;
+    #pragma unroll
+            for (int n = 0; n < NT; ++n)
+    #pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float lim_x = m[n][e] + kSlack;
+                    grow |= x[0][n][e] > lim_x || x[0][n][e + 2] > lim_x ||
+                            x[1][n][e] > lim_x || x[1][n][e + 2] > lim_x;
+                }
+            if (__any_sync(0xffffffffu, grow)) {
+    #pragma unroll
+                for (int n = 0; n < NT; ++n)
+    #pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        float mx = fmaxf(fmaxf(x[0][n][e], x[0][n][e + 2]), fmaxf(x[1][n][e], x[1][n][e + 2]));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float mn = fmaxf(m[n][e], mx);
+                        const float al = (m[n][e] == -INFINITY) ? 0.f : fast_exp2(m[n][e] - mn);
+                        m[n][e] = mn;
+                        l[n][e] *= al;
+    #pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            O[n][i][e] *= al;
+                            O[n][i][e + 2] *= al;
+                        }
+                    }
+            }
+    #pragma unroll
+            for (int n = 0; n < NT; ++n)
+    #pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float base = (m[n][e] == -INFINITY) ? 0.f : m[n][e];
+                    float s = 0.f;
+    #pragma unroll
+                    for (int tile = 0; tile < 2; ++tile) {
+                        x[tile][n][e] = fast_exp2(x[tile][n][e] - base);
+                        x[tile][n][e + 2] = fast_exp2(x[tile][n][e + 2] - base);
+                        s += x[tile][n][e] + x[tile][n][e + 2];
+                    }
+                    l[n][e] += s;
+                }
+
+            // ---------------- O^T += C_v^T . (P n_v)^T (rotated basis) ----------------
+    #pragma unroll
+            for (int tile = 0; tile < 2; ++tile) {
+                if (!FULL && tile == 1 && !two) break;
+                uint32_t pb0[NT], pb1[NT];
+    #pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    pb0[n] = movtrans(pack_half2(x[tile][n][0] * nv[tile][0], x[tile][n][1] * nv[tile][0]));
+                    pb1[n] = movtrans(pack_half2(x[tile][n][2] * nv[tile][1], x[tile][n][3] * nv[tile][1]));
+                }
+                // A quad of dim tile mt: transposed pairs 2mt, 2mt+1 of token block 0
+                // (tokens 0-7 of the tile) then of block 1 (tokens 8-15)
+                uint32_t vq[8][4];
+                {
+                    uint32_t hv[16];
+                    dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g) * C::kRbV + t * (C::kRbV / 4), vt, hv);
+    #pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        vq[mt][0] = movtrans(hv[2 * mt]);
+                        vq[mt][1] = movtrans(hv[2 * mt + 1]);
+                    }
+                }
+                {
+                    uint32_t hv[16];
+                    dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g + 8) * C::kRbV + t * (C::kRbV / 4), vt, hv);
+    #pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        vq[mt][2] = movtrans(hv[2 * mt]);
+                        vq[mt][3] = movtrans(hv[2 * mt + 1]);
+                    }
+                }
+    #pragma unroll
+                for (int mt = 0; mt < 8; ++mt)
+    #pragma unroll
+                    for (int n = 0; n < NT; ++n)
+                        mma_f16(O[n][mt], vq[mt][0], vq[mt][1], vq[mt][2], vq[mt][3], pb0[n], pb1[n]);
+            }
+
+    };
+
+    int stage = 0;
+    uint32_t phase = 0;
+    int c = warp;
+    for (; c < nchunks; c += C::kWarps) {
+        const bool ok = mbar_wait_bounded(bar0 + 8 * stage, phase);
         if (__any_sync(0xffffffffu, !ok)) { stalled = true; break; }
         const uint8_t* st = wpipe + stage * C::kStage;
         const int tok0 = t_begin + c * C::kChunk;
-        const int nvalid = min(C::kChunk, t_end - tok0);
-        const bool two = nvalid > 16;
-        const bool full = (nvalid == C::kChunk) && (tok0 + C::kChunk <= all_visible_below);
-
-        // ---------------- scores S^T = C_k . Rot(q)^T ----------------
-        float x[2][NT][4];
-#pragma unroll
-        for (int tile = 0; tile < 2; ++tile) {
-#pragma unroll
-            for (int n = 0; n < NT; ++n) x[tile][n][0] = x[tile][n][1] = x[tile][n][2] = x[tile][n][3] = 0.f;
-            if (tile == 1 && !two) break;
-            if constexpr (KB == 0) {
-                const int mi = lane >> 3;
-                const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-                for (int kc = 0; kc < 8; ++kc) {
-                    const int db = 2 * kc + (mi >> 1);  // 16-byte chunk 0..15 of the row
-                    const uint32_t addr = smem_u32(st) + (db >> 3) * 4096 + row * 128 +
-                                          (((db & 7) ^ (row & 7)) << 4);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(addr, a0, a1, a2, a3);
-#pragma unroll
-                    for (int n = 0; n < NT; ++n) mma_f16(x[tile][n], a0, a1, a2, a3, qb[n][kc][0], qb[n][kc][1]);
-                }
-            } else {
-                // A quad of k-step kc: (token g, dims 2kc), (token g+8, 2kc),
-                // (token g, 2kc+1), (token g+8, 2kc+1) in quarter-pair units
-                uint32_t aq[8][4];
-                dequant_quarter_q<KB, 0>(st + (tile * 16 + g) * C::kRbK + t * (C::kRbK / 4), kt, aq);
-                dequant_quarter_q<KB, 1>(st + (tile * 16 + g + 8) * C::kRbK + t * (C::kRbK / 4), kt, aq);
-#pragma unroll
-                for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-                    for (int n = 0; n < NT; ++n)
-                        mma_f16(x[tile][n], aq[kc][0], aq[kc][1], aq[kc][2], aq[kc][3],
-                                qb[n][kc][0], qb[n][kc][1]);
-            }
-        }
-
-        // ---------------- online softmax (log2 domain) ----------------
-        // thread's tokens: tile*16 + g (c0, c1) and tile*16 + g + 8 (c2, c3);
-        // rows 8n + 2t (c0, c2) and 8n + 2t + 1 (c1, c3)
-        float nv[2][2];
-#pragma unroll
-        for (int tile = 0; tile < 2; ++tile) {
-            const int ta = tile * 16 + g, tb = ta + 8;
-            float ka = p.scale_log2e, kb2 = p.scale_log2e;
-            if constexpr (KB != 0) {
-                ka *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * ta));
-                kb2 *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * tb));
-            }
-            nv[tile][0] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * ta));
-            nv[tile][1] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * tb));
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                x[tile][n][0] *= ka; x[tile][n][1] *= ka;
-                x[tile][n][2] *= kb2; x[tile][n][3] *= kb2;
-            }
-            if (!full) {
-                const int ga = tok0 + ta, gb = tok0 + tb;
-                const bool va = ga < t_end && (tile == 0 || two);
-                const bool vb = gb < t_end && (tile == 0 || two);
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    x[tile][n][0] = (va && ga <= lim[n][0]) ? x[tile][n][0] : -INFINITY;
-                    x[tile][n][1] = (va && ga <= lim[n][1]) ? x[tile][n][1] : -INFINITY;
-                    x[tile][n][2] = (vb && gb <= lim[n][0]) ? x[tile][n][2] : -INFINITY;
-                    x[tile][n][3] = (vb && gb <= lim[n][1]) ? x[tile][n][3] : -INFINITY;
-                }
-                if (!va) nv[tile][0] = 0.f;
-                if (!vb) nv[tile][1] = 0.f;
-            }
-        }
-        // The exp2 base of a row stays at its running max until a score exceeds
-        // it by more than kSlack (log2 units); only then (warp-uniform slow
-        // path) is the true max taken and O, l rescaled.  So p <= 2^kSlack.
-        constexpr float kSlack = 4.f;
-        bool grow = false;
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float lim_x = m[n][e] + kSlack;
-                grow |= x[0][n][e] > lim_x || x[0][n][e + 2] > lim_x ||
-                        x[1][n][e] > lim_x || x[1][n][e + 2] > lim_x;
-            }
-        if (__any_sync(0xffffffffu, grow)) {
-#pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float mx = fmaxf(fmaxf(x[0][n][e], x[0][n][e + 2]), fmaxf(x[1][n][e], x[1][n][e + 2]));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    const float mn = fmaxf(m[n][e], mx);
-                    const float al = (m[n][e] == -INFINITY) ? 0.f : fast_exp2(m[n][e] - mn);
-                    m[n][e] = mn;
-                    l[n][e] *= al;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        O[n][i][e] *= al;
-                        O[n][i][e + 2] *= al;
-                    }
-                }
-        }
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float base = (m[n][e] == -INFINITY) ? 0.f : m[n][e];
-                float s = 0.f;
-#pragma unroll
-                for (int tile = 0; tile < 2; ++tile) {
-                    x[tile][n][e] = fast_exp2(x[tile][n][e] - base);
-                    x[tile][n][e + 2] = fast_exp2(x[tile][n][e + 2] - base);
-                    s += x[tile][n][e] + x[tile][n][e + 2];
-                }
-                l[n][e] += s;
-            }
-
-        // ---------------- O^T += C_v^T . (P n_v)^T (rotated basis) ----------------
-#pragma unroll
-        for (int tile = 0; tile < 2; ++tile) {
-            if (tile == 1 && !two) break;
-            uint32_t pb0[NT], pb1[NT];
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                pb0[n] = movtrans(pack_half2(x[tile][n][0] * nv[tile][0], x[tile][n][1] * nv[tile][0]));
-                pb1[n] = movtrans(pack_half2(x[tile][n][2] * nv[tile][1], x[tile][n][3] * nv[tile][1]));
-            }
-            // A quad of dim tile mt: transposed pairs 2mt, 2mt+1 of token block 0
-            // (tokens 0-7 of the tile) then of block 1 (tokens 8-15)
-            uint32_t vq[8][4];
-            {
-                uint32_t hv[16];
-                dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g) * C::kRbV + t * (C::kRbV / 4), vt, hv);
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    vq[mt][0] = movtrans(hv[2 * mt]);
-                    vq[mt][1] = movtrans(hv[2 * mt + 1]);
-                }
-            }
-            {
-                uint32_t hv[16];
-                dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g + 8) * C::kRbV + t * (C::kRbV / 4), vt, hv);
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    vq[mt][2] = movtrans(hv[2 * mt]);
-                    vq[mt][3] = movtrans(hv[2 * mt + 1]);
-                }
-            }
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-                for (int n = 0; n < NT; ++n)
-                    mma_f16(O[n][mt], vq[mt][0], vq[mt][1], vq[mt][2], vq[mt][3], pb0[n], pb1[n]);
-        }
-
+        if (tok0 + C::kChunk <= t_end && tok0 + C::kChunk <= all_visible_below)
+            process(st, tok0, std::true_type{});
+        else
+            process(st, tok0, std::false_type{});
         __syncwarp();
-        if (lane == 0) {
-            const int cn = c + C::kWarps * C::kStages;
-            if (cn < nchunks) {
-                fence_proxy_async();
-                issue(cn, stage);
-            }
+        const int cn = c + C::kWarps * C::kStages;
+        if (cn < nchunks && lane == 0) {
+            fence_proxy_async();
+            issue(cn, stage);
         }
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
     }
 
     if (stalled) {
         // Drain this warp's copies still in flight (bounded), flag, and stop.
         for (int k = 0; k < C::kStages; ++k) {
-            const int c = warp + C::kWarps * (it + k);
-            if (c >= nchunks) break;
-            const int stage = (it + k) % C::kStages;
-            (void)mbar_wait_bounded(bar0 + 8 * stage, ((it + k) / C::kStages) & 1);
+            if (c + C::kWarps * k >= nchunks) break;
+            (void)mbar_wait_bounded(bar0 + 8 * stage, phase);
+            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (lane == 0) atomicOr(p.status, kStatusPipelineStall);
     }

@@ -1,12 +1,12 @@
 // Encode/append: fp16 K/V vectors -> (fp16 norm, packed b-bit codes) written
 // at each sequence's current length, then lengths[b] += t_new.
 //
-// Per vector (one warp, lane l holds dims 4l .. 4l+3):
-//   n16  = fp16 round-to-nearest-even of the exact L2 norm.  The sum of
-//          squares is formed exactly as a 128-bit integer (every fp16 value is
-//          an integer multiple of 2^-24), an fp32 square root gives a
-//          candidate, and the candidate is corrected against the neighbouring
-//          rounding midpoints with exact integer comparisons.
+// Per vector (four lanes of a warp, lane q holds dims 32q .. 32q+31):
+//   n16  = fp16 round-to-nearest-even of the exact L2 norm: fp32 sum of the
+//          exact squares, certified against the rounding midpoints; if it is
+//          too close to call, the sum of squares is formed exactly as a
+//          128-bit integer (every fp16 value is an integer multiple of 2^-24)
+//          and the candidate corrected with exact integer comparisons.
 //   u    = Rot(x) / n = H (s * x) / (sqrt(128) n), in fp32.
 //   code = sign-magnitude index of the nearest codebook entry to u, decided
 //          with thresholds that make the fp32 comparison exact against the
@@ -100,41 +100,306 @@ __device__ __forceinline__ unsigned short norm_to_half(U128 S) {
     return hb;
 }
 
+// Exact fp16 norm of one vector whose 4 lanes each hold 32 dims; reloads the
+// lane's 32 fp16 values from src (out of line: it is the rare path of
+// norm_fp16 below).  gmask = the group's lanes.
+__device__ __noinline__ unsigned short norm_exact_group(const __half* src, int q, bool valid,
+                                                        unsigned gmask) {
+    U128 S;
+    S.lo = 0;
+    S.hi = 0;
+    if (valid) {
+        const __half* x = src + q * 32;
+        for (int i = 0; i < 32; ++i) S = add128(S, sq_u128(fp16_scaled_int(__half2float(x[i]))));
+    }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+        U128 o;
+        o.lo = __shfl_xor_sync(gmask, S.lo, m);
+        o.hi = __shfl_xor_sync(gmask, S.hi, m);
+        S = add128(S, o);
+    }
+    return norm_to_half(S);
+}
+
+__device__ __forceinline__ float half_bits_to_float(unsigned short b) {
+    return (b >= 0x7C00u) ? 65536.f : __half2float(__ushort_as_half(b));
+}
+
+// norm_fp16: fp16 round-to-nearest-even of the exact norm sqrt(sum x^2).  Fast path: the
+// fp32 sum of the (exact) squares is within 2^-17 (relative) of the exact sum,
+// so the candidate rounding of its square root is certain unless the sum lies
+// within 2^-16 of the square of a rounding midpoint (midpoints have 12
+// significant bits, so their squares are exact in fp32); then the exact
+// 128-bit integer path decides.
+// Candidate fp16 rounding of sqrt(S32) and whether it is certain (see norm_fp16).
+__device__ __forceinline__ unsigned short norm_candidate(float S32, bool& certain) {
+    certain = true;
+    if (S32 == 0.f) return 0;
+    const float n = sqrtf(S32);
+    unsigned short hb = __half_as_ushort(__float2half_rn(n));
+    if (hb > 0x7C00u) hb = 0x7C00u;
+    const float margin = S32 * (1.0f / 65536.0f);
+    const float hf = half_bits_to_float(hb);
+    if (hb < 0x7C00u) {
+        const float up = 0.5f * (hf + half_bits_to_float(hb + 1));
+        certain = certain && (S32 < up * up - margin);
+    }
+    if (hb > 0) {
+        const unsigned short db = (hb == 0x7C00u) ? 0x7BFFu : static_cast<unsigned short>(hb - 1);
+        const float dn = 0.5f * (half_bits_to_float(db) + ((hb == 0x7C00u) ? 65536.f : hf));
+        certain = certain && (S32 > dn * dn + margin);
+    }
+    return hb;
+}
+
+__device__ __forceinline__ unsigned short norm_fp16(const __half* src, int q, bool valid,
+                                                    float S32, unsigned gmask) {
+    bool ok;
+    const unsigned short hb = norm_candidate(S32, ok);
+    const bool all_ok = __all_sync(gmask, ok);   // the group decides together
+    return all_ok ? hb : norm_exact_group(src, q, valid, gmask);
+}
+
+// Sign-magnitude code of the centroid nearest to u: rank = #{tau_k < |u|} for
+// u > 0 and #{tau_k <= |u|} for u <= 0, with gt[k] / ge[k] the smallest fp32
+// values above / at-or-above the exact midpoint tau_k (ascending).  gt and ge
+// differ only when tau_k is itself an fp32 value, so the search runs on gt and
+// a negative u sitting exactly on such a tau_k moves one rank up.  Binary
+// search: BITS-1 comparisons.
 template <int BITS>
-__device__ __forceinline__ uint32_t quantize_code(float u, const float* gt, const float* ge) {
+__device__ __forceinline__ uint32_t quantize_code(float u, const float* gt, const float* ge,
+                                                  bool any_tie) {
     constexpr int H = 1 << (BITS - 1);
     const float a = fabsf(u);
     const bool neg = !(u > 0.f);
-    uint32_t rank = 0;
-#pragma unroll
-    for (int k = 0; k < H - 1; ++k) rank += (a >= (neg ? ge[k] : gt[k])) ? 1u : 0u;
+    uint32_t rank;
+    if constexpr (BITS == 3) {
+        const bool b1 = a >= gt[1];
+        const bool b0 = a >= (b1 ? gt[2] : gt[0]);
+        rank = (b1 ? 2u : 0u) | (b0 ? 1u : 0u);
+    } else {
+        const bool b2 = a >= gt[3];
+        const bool b1 = a >= (b2 ? gt[5] : gt[1]);
+        const float t0 = b2 ? (b1 ? gt[6] : gt[4]) : (b1 ? gt[2] : gt[0]);
+        const bool b0 = a >= t0;
+        rank = (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u);
+    }
+    if (any_tie && neg && rank < H - 1) {
+        // a in [ge[rank], gt[rank]) means a == tau_rank: the tie goes down (more negative)
+        if (a >= ge[rank] && a < gt[rank]) rank += 1;
+    }
     return (neg ? static_cast<uint32_t>(H) : 0u) | rank;
 }
 
-// Encode one fp16 vector with the warp; returns nothing, writes codes + norm.
+// Encode the vectors of one warp: 8 vectors, 4 lanes each; lane quarter q
+// holds dims 32q .. 32q+31.  `valid` marks lanes whose vector exists.
 template <int BITS>
-__device__ __forceinline__ void encode_vector(const __half* src, uint8_t* dst, __half* dst_norm,
-                                              const uint32_t (&signs)[4], const float* gt,
-                                              const float* ge, uint32_t* status, int lane) {
+__device__ __forceinline__ void encode_group(const __half* src, uint8_t* dst, __half* dst_norm,
+                                             const uint32_t (&signs)[4], const float* gt,
+                                             const float* ge, bool valid, uint32_t* status,
+                                             int q, unsigned gmask) {
+    float x[32];
+    if (valid) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + q * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 w = s4[i];
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
+                x[8 * i + 2 * k] = f.x;
+                x[8 * i + 2 * k + 1] = f.y;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = 0.f;
+    }
+
+    // norm: squares of fp16 values are exact in fp32
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ss = fmaf(x[i], x[i], ss);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    const float S32 = __shfl_sync(0xffffffffu, ss, 0, 4);   // one rounding order per group
+    const unsigned short nb = norm_fp16(src, q, valid, S32, gmask);
+    if (valid && q == 0) {
+        dst_norm[0] = __ushort_as_half(nb);
+        if (nb >= 0x7C00u) atomicOr(status, kStatusNormOverflow);
+    }
+
+    // rotate: H (s * x), 5 in-lane stages + 2 across the group's lanes
+    const uint32_t sg = signs[q];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = ((sg >> i) & 1u) ? -x[i] : x[i];
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (i & h) continue;
+            const float a = x[i], b = x[i + h];
+            x[i] = a + b;
+            x[i + h] = a - b;
+        }
+    }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+            x[i] = (q & m) ? (o - x[i]) : (x[i] + o);
+        }
+    }
+    const float n = sqrtf(S32);
+    const float inv = (n > 0.f) ? 1.0f / (n * 11.313708498984761f) : 0.f;
+
+    constexpr int H = 1 << (BITS - 1);
+    bool any_tie = false;
+#pragma unroll
+    for (int k = 0; k < H - 1; ++k) any_tie |= ge[k] != gt[k];
+    uint32_t code[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) code[i] = quantize_code<BITS>(x[i] * inv, gt, ge, any_tie);
+
+    if (!valid) return;
+    if constexpr (BITS == 4) {
+        // word k = dims 8k..8k+7: rank of dim 8k+j in bits 4j..4j+2; sign of dim
+        // 8k+j (j < 4) in bit 8j+7, of dim 8k+4+j in bit 8j+3
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v |= (code[8 * k + j] & 7u) << (4 * j);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v |= (code[8 * k + j] >> 3) << (8 * j + 7);
+                v |= (code[8 * k + 4 + j] >> 3) << (8 * j + 3);
+            }
+            w[k] = v;
+        }
+        *reinterpret_cast<uint4*>(dst + q * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+        // quarter q: word k (k < 3): bits 4j..4j+2 = code(8k+j), bit 4j+3 = bit k of code(24+j)
+        uint32_t* d = reinterpret_cast<uint32_t*>(dst + q * 12);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v |= (code[8 * k + j] & 7u) << (4 * j);
+                v |= ((code[24 + j] >> k) & 1u) << (4 * j + 3);
+            }
+            d[k] = v;
+        }
+    }
+}
+
+// Advance lengths[] after the last warp of the launch (every warp read
+// lengths[] before taking its ticket, so none sees an advanced length).
+__device__ __forceinline__ void finish_append(const EncodeParams& p, unsigned int total_warps,
+                                              int lane) {
+    __syncwarp();
+    unsigned int ticket = 0;
+    if (lane == 0) {
+        __threadfence();
+        ticket = atomicAdd(p.counter, 1u);
+    }
+    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+    if (ticket == total_warps - 1) {
+        __threadfence();
+        for (int bb = lane; bb < p.batch; bb += 32) {
+            const int Lb = *((volatile int32_t*)p.lengths + bb);
+            if (Lb >= 0 && Lb + p.t_new <= p.cap) p.lengths[bb] = Lb + p.t_new;
+        }
+        if (lane == 0) *((volatile uint32_t*)p.counter) = 0u;
+        __threadfence();
+    }
+}
+
+// grid: [K blocks | V blocks]; a CTA of 2 warps encodes 16 vectors of one
+// stream (K or V), 8 per warp, 4 lanes per vector.  KB = 0 copies fp16 K rows.
+constexpr int kEncWarps = 2;
+constexpr int kEncVecs = 8 * kEncWarps;
+
+template <int KB, int VB>
+__global__ void __launch_bounds__(32 * kEncWarps)
+    tq_encode_kernel(const __grid_constant__ EncodeParams p, int k_blocks) {
+    const int lane = threadIdx.x & 31;
+    const int q = lane & 3;
+    const unsigned gmask = 0xFu << (lane & ~3);
+    const bool is_v = static_cast<int>(blockIdx.x) >= k_blocks;
+    const long long blk = is_v ? blockIdx.x - k_blocks : blockIdx.x;
+    const long long v = blk * kEncVecs + (threadIdx.x >> 2);  // vector index in the stream
+    const long long nvec = static_cast<long long>(p.batch) * p.hkv * p.t_new;
+    bool valid = v < nvec;
+    const long long vv = valid ? v : 0;
+    const int t = static_cast<int>(vv % p.t_new);
+    const long long bh = vv / p.t_new;
+    const int b = static_cast<int>(bh / p.hkv);
+    const __half* src = (is_v ? p.v_new : p.k_new) + vv * kD;
+    const int L = p.lengths[b];
+    if (valid && (L < 0 || L + p.t_new > p.cap)) {
+        if (q == 0 && !is_v && t == 0 && (bh % p.hkv) == 0) atomicOr(p.status, kStatusCapacity);
+        valid = false;
+    }
+    const size_t pos = valid ? static_cast<size_t>(bh) * p.cap + L + t : 0;
+    if (!is_v) {
+        if constexpr (KB == 0) {
+            if (valid) {
+                const uint4* s4 = reinterpret_cast<const uint4*>(src + q * 32);
+                uint4* d4 = reinterpret_cast<uint4*>(p.k_codes + pos * 256 + q * 64);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) d4[i] = s4[i];
+            }
+        } else {
+            encode_group<KB>(src, p.k_codes + pos * (KB * 16), p.k_norm + pos, p.signs, p.k_gt,
+                             p.k_ge, valid, p.status, q, gmask);
+        }
+    } else {
+        encode_group<VB>(src, p.v_codes + pos * (VB * 16), p.v_norm + pos, p.signs, p.v_gt,
+                         p.v_ge, valid, p.status, q, gmask);
+    }
+
+    finish_append(p, gridDim.x * kEncWarps, lane);
+}
+
+// Small appends (a few tokens per sequence): one warp per vector, lane l holds
+// dims 4l .. 4l+3, so every vector gets its own warp and the dependent chain
+// per lane is short.  Same arithmetic and output as encode_group.
+template <int BITS>
+__device__ __forceinline__ void encode_vector_warp(const __half* src, uint8_t* dst,
+                                                   __half* dst_norm, const uint32_t (&signs)[4],
+                                                   const float* gt, const float* ge,
+                                                   uint32_t* status, int lane) {
     const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
     const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
     const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
     float x[4] = {f0.x, f0.y, f1.x, f1.y};
 
-    // exact sum of squares (units of 2^-48)
-    U128 S = sq_u128(fp16_scaled_int(x[0]));
+    float ss = fmaf(x[0], x[0], x[1] * x[1]) + fmaf(x[2], x[2], x[3] * x[3]);
 #pragma unroll
-    for (int i = 1; i < 4; ++i) S = add128(S, sq_u128(fp16_scaled_int(x[i])));
+    for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    const float S32 = __shfl_sync(0xffffffffu, ss, 0);
+    bool ok;
+    unsigned short nb = norm_candidate(S32, ok);
+    if (!__all_sync(0xffffffffu, ok)) {
+        // exact sum of squares (units of 2^-48) as a 128-bit integer
+        U128 S = sq_u128(fp16_scaled_int(x[0]));
 #pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-        U128 o;
-        o.lo = __shfl_xor_sync(0xffffffffu, S.lo, m);
-        o.hi = __shfl_xor_sync(0xffffffffu, S.hi, m);
-        S = add128(S, o);
+        for (int i = 1; i < 4; ++i) S = add128(S, sq_u128(fp16_scaled_int(x[i])));
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            U128 o;
+            o.lo = __shfl_xor_sync(0xffffffffu, S.lo, m);
+            o.hi = __shfl_xor_sync(0xffffffffu, S.hi, m);
+            S = add128(S, o);
+        }
+        nb = norm_to_half(S);
     }
-    const unsigned short nb = norm_to_half(S);
-    const float sf = static_cast<float>(S.hi) * 18446744073709551616.0f + static_cast<float>(S.lo);
-    const float n = sqrtf(sf) * (1.0f / 16777216.0f);   // unrounded norm (fp32)
     if (lane == 0) {
         dst_norm[0] = __ushort_as_half(nb);
         if (nb >= 0x7C00u) atomicOr(status, kStatusNormOverflow);
@@ -145,10 +410,15 @@ __device__ __forceinline__ void encode_vector(const __half* src, uint8_t* dst, _
 #pragma unroll
     for (int i = 0; i < 4; ++i) x[i] = ((sn >> i) & 1u) ? -x[i] : x[i];
     wht128_lane4(x, lane);
+    const float n = sqrtf(S32);
     const float inv = (n > 0.f) ? 1.0f / (n * 11.313708498984761f) : 0.f;
+    constexpr int H = 1 << (BITS - 1);
+    bool any_tie = false;
+#pragma unroll
+    for (int k = 0; k < H - 1; ++k) any_tie |= ge[k] != gt[k];
     uint32_t code[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) code[i] = quantize_code<BITS>(x[i] * inv, gt, ge);
+    for (int i = 0; i < 4; ++i) code[i] = quantize_code<BITS>(x[i] * inv, gt, ge, any_tie);
 
     if constexpr (BITS == 4) {
         // word k = dims 8k..8k+7 (lanes 2k, 2k+1): rank of dim 8k+j in bits
@@ -191,11 +461,11 @@ __device__ __forceinline__ void encode_vector(const __half* src, uint8_t* dst, _
     }
 }
 
-// grid: 8 warps per CTA, warp = (vector, K-or-V).  KB = 0 copies fp16 K rows.
+// grid: 4 warps per CTA, warp = (K-or-V, vector).  KB = 0 copies fp16 K rows.
 template <int KB, int VB>
-__global__ void __launch_bounds__(256) tq_encode_kernel(const __grid_constant__ EncodeParams p) {
+__global__ void __launch_bounds__(128) tq_encode_small_kernel(const __grid_constant__ EncodeParams p) {
     const int lane = threadIdx.x & 31;
-    const long long gw = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const long long gw = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     const long long nvec = static_cast<long long>(p.batch) * p.hkv * p.t_new;
     if (gw < 2 * nvec) {
         const int which = static_cast<int>(gw & 1);  // 0 = K, 1 = V
@@ -215,39 +485,34 @@ __global__ void __launch_bounds__(256) tq_encode_kernel(const __grid_constant__ 
                     reinterpret_cast<uint2*>(p.k_codes + pos * 256)[lane] =
                         reinterpret_cast<const uint2*>(src)[lane];
                 } else {
-                    encode_vector<KB>(src, p.k_codes + pos * (KB * 16), p.k_norm + pos, p.signs,
-                                      p.k_gt, p.k_ge, p.status, lane);
+                    encode_vector_warp<KB>(src, p.k_codes + pos * (KB * 16), p.k_norm + pos,
+                                           p.signs, p.k_gt, p.k_ge, p.status, lane);
                 }
             } else {
-                encode_vector<VB>(src, p.v_codes + pos * (VB * 16), p.v_norm + pos, p.signs, p.v_gt,
-                                  p.v_ge, p.status, lane);
+                encode_vector_warp<VB>(src, p.v_codes + pos * (VB * 16), p.v_norm + pos, p.signs,
+                                       p.v_gt, p.v_ge, p.status, lane);
             }
         }
     }
-    // The last CTA to finish advances the lengths.  Every CTA read lengths[]
-    // before its ticket, so no CTA can see an advanced length.
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned int ticket = atomicAdd(p.counter, 1u);
-        if (ticket == gridDim.x - 1) {
-            __threadfence();
-            for (int b = 0; b < p.batch; ++b) {
-                const int L = *((volatile int32_t*)p.lengths + b);
-                if (L >= 0 && L + p.t_new <= p.cap) p.lengths[b] = L + p.t_new;
-            }
-            *((volatile uint32_t*)p.counter) = 0u;
-            __threadfence();
-        }
-    }
+    finish_append(p, gridDim.x * 4, lane);
 }
 
 int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stream) {
-    const long long warps = 2ll * p.batch * p.hkv * p.t_new;
-    const unsigned int blocks = static_cast<unsigned int>((warps + 7) / 8);
-    if (kbits == 16 && vbits == 4) tq_encode_kernel<0, 4><<<blocks, 256, 0, stream>>>(p);
-    else if (kbits == 3 && vbits == 3) tq_encode_kernel<3, 3><<<blocks, 256, 0, stream>>>(p);
-    else if (kbits == 4 && vbits == 4) tq_encode_kernel<4, 4><<<blocks, 256, 0, stream>>>(p);
+    const long long nvec = 1ll * p.batch * p.hkv * p.t_new;
+    if (nvec <= 4096) {   // a warp per vector: short chains for small appends
+        const unsigned int sblocks = static_cast<unsigned int>((2 * nvec + 3) / 4);
+        if (kbits == 16 && vbits == 4) tq_encode_small_kernel<0, 4><<<sblocks, 128, 0, stream>>>(p);
+        else if (kbits == 3 && vbits == 3) tq_encode_small_kernel<3, 3><<<sblocks, 128, 0, stream>>>(p);
+        else if (kbits == 4 && vbits == 4) tq_encode_small_kernel<4, 4><<<sblocks, 128, 0, stream>>>(p);
+        else return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    }
+    const int kblocks = static_cast<int>((nvec + kEncVecs - 1) / kEncVecs);
+    const unsigned int blocks = static_cast<unsigned int>(2 * kblocks);
+    const int thr = 32 * kEncWarps;
+    if (kbits == 16 && vbits == 4) tq_encode_kernel<0, 4><<<blocks, thr, 0, stream>>>(p, kblocks);
+    else if (kbits == 3 && vbits == 3) tq_encode_kernel<3, 3><<<blocks, thr, 0, stream>>>(p, kblocks);
+    else if (kbits == 4 && vbits == 4) tq_encode_kernel<4, 4><<<blocks, thr, 0, stream>>>(p, kblocks);
     else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }

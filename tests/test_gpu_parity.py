@@ -120,10 +120,13 @@ def _crafted_vectors():
     return np.stack(v)
 
 
+# T = 300 runs the warp-per-vector kernel (small appends), T = 700 the
+# four-lanes-per-vector kernel (more than 4096 vectors per stream)
+@pytest.mark.parametrize("T", [300, 700])
 @pytest.mark.parametrize("mode", ["turbo3", "turbo4", "turbo4_asym"])
-def test_encode_append_bit_exact(mode):
+def test_encode_append_bit_exact(mode, T):
     kb, vb = H.MODE_BITS[mode]
-    B, Hkv, T, cap = 2, 3, 300, 320
+    B, Hkv, cap = 2, 3, 720
     rng = np.random.default_rng(3)
     k = wl.random_fp16(11, (B, Hkv, T, 128))
     v = wl.random_fp16(12, (B, Hkv, T, 128), scale=3.0)
