@@ -56,10 +56,15 @@ extern "C" {
 
 /* modes: (K format, V format).  Turbo4Asym = fp16 K + 4-bit rotated V
  * (mlxcel pull request #369, Problem); turbo3 / turbo4 = K and V both 3- or
- * 4-bit rotated ("4-mag LUT" turbo3 of the smem-dequant experiment). */
+ * 4-bit rotated ("4-mag LUT" turbo3 of the smem-dequant experiment);
+ * turbo3-asym = fp16 K + 3-bit rotated V (the memory-extremis mode of the
+ * mlxcel advisor commit); turbo4k-3v = 4-bit K + 3-bit V, the remaining
+ * pairing of the two codecs. */
 #define TQ_TURBO4_ASYM  0
 #define TQ_TURBO3       1
 #define TQ_TURBO4       2
+#define TQ_TURBO3_ASYM  3
+#define TQ_TURBO4K_3V   4
 
 /* device status bits (tq_get_status) */
 #define TQ_STATUS_CAPACITY        1u  /* an append would pass `capacity`; that sequence was skipped */

@@ -43,7 +43,8 @@ import numpy as np
 
 D = 128
 MASK64 = (1 << 64) - 1
-MODES = {"turbo4_asym": (None, 4), "turbo3": (3, 3), "turbo4": (4, 4)}
+MODES = {"turbo4_asym": (None, 4), "turbo3": (3, 3), "turbo4": (4, 4),
+         "turbo3_asym": (None, 3), "turbo4k_3v": (4, 3)}
 
 
 # --------------------------------------------------------------------------
@@ -380,7 +381,7 @@ def unit_kv_full(mode: str, unit: dict, cbk, cbv, s):
 
     unit keys: 'k' (fp16 [L,128], asym only) or 'k_idx','k_norm'; 'v_idx','v_norm'.
     """
-    if mode == "turbo4_asym":
+    if MODES[mode][0] is None:
         K = np.asarray(unit["k"], np.float64)
     else:
         K = dequant_full(unit["k_idx"], unit["k_norm"], cbk, s)
@@ -409,7 +410,7 @@ def decode_rotated_unit(mode: str, q_rows, unit: dict, L: int, tq: int, G: int,
     V stays rotated; only the output is inverse-rotated.
     """
     q = np.asarray(q_rows, np.float64).reshape(G * tq, D)
-    if mode == "turbo4_asym":
+    if MODES[mode][0] is None:
         qk, K = q, np.asarray(unit["k"], np.float64)
     else:
         qk, K = rotate(q, s), dequant_rotated(unit["k_idx"], unit["k_norm"], cbk)

@@ -25,8 +25,12 @@ TQ_ERR_NOMEM = -5
 TQ_TURBO4_ASYM = 0
 TQ_TURBO3 = 1
 TQ_TURBO4 = 2
-MODES = {"turbo4_asym": TQ_TURBO4_ASYM, "turbo3": TQ_TURBO3, "turbo4": TQ_TURBO4}
-MODE_BITS = {TQ_TURBO4_ASYM: (16, 4), TQ_TURBO3: (3, 3), TQ_TURBO4: (4, 4)}
+TQ_TURBO3_ASYM = 3
+TQ_TURBO4K_3V = 4
+MODES = {"turbo4_asym": TQ_TURBO4_ASYM, "turbo3": TQ_TURBO3, "turbo4": TQ_TURBO4,
+         "turbo3_asym": TQ_TURBO3_ASYM, "turbo4k_3v": TQ_TURBO4K_3V}
+MODE_BITS = {TQ_TURBO4_ASYM: (16, 4), TQ_TURBO3: (3, 3), TQ_TURBO4: (4, 4),
+             TQ_TURBO3_ASYM: (16, 3), TQ_TURBO4K_3V: (4, 3)}
 
 TQ_STATUS_CAPACITY = 1
 TQ_STATUS_NORM_OVERFLOW = 2

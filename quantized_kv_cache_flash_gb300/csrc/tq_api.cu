@@ -55,15 +55,6 @@ int cuda_err(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int mode_bits(int mode, int* kb, int* vb) {
-    switch (mode) {
-        case TQ_TURBO4_ASYM: *kb = 16; *vb = 4; return TQ_OK;
-        case TQ_TURBO3: *kb = 3; *vb = 3; return TQ_OK;
-        case TQ_TURBO4: *kb = 4; *vb = 4; return TQ_OK;
-        default: return TQ_ERR_UNSUPPORTED;
-    }
-}
-
 // splitmix64 (Steele, Lea, Flood 2014; the finaliser of Vigna's splitmix64.c)
 uint64_t splitmix64_next(uint64_t& state) {
     state += 0x9E3779B97F4A7C15ull;
@@ -178,7 +169,7 @@ int get_ctx(tq_ctx** pctx, tq_ctx** out) {
 
 int check_cache(const tq_cache* c, int* kb, int* vb) {
     if (c == nullptr) return TQ_ERR_INVALID_ARG;
-    int r = mode_bits(c->mode, kb, vb);
+    int r = tq::mode_bits(c->mode, kb, vb);
     if (r != TQ_OK) return r;
     if (c->head_dim != kD) return TQ_ERR_UNSUPPORTED;
     if (c->batch <= 0 || c->num_kv_heads <= 0 || c->capacity <= 0 || (c->capacity % 16) != 0)
@@ -329,7 +320,7 @@ int tq_lloyd_max_codebook(int32_t bits, float* out) {
 int tq_plan_splits(int32_t mode, int32_t batch, int32_t num_kv_heads, int32_t rows_per_kv_head,
                    int32_t max_len_hint, int32_t* split_tokens, int32_t* num_splits) {
     int kb, vb;
-    if (mode_bits(mode, &kb, &vb) != TQ_OK) return TQ_ERR_UNSUPPORTED;
+    if (tq::mode_bits(mode, &kb, &vb) != TQ_OK) return TQ_ERR_UNSUPPORTED;
     if (batch <= 0 || num_kv_heads <= 0 || rows_per_kv_head <= 0 || max_len_hint <= 0 ||
         split_tokens == nullptr || num_splits == nullptr)
         return TQ_ERR_INVALID_ARG;

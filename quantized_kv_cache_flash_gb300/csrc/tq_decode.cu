@@ -545,6 +545,8 @@ static int launch_decode_nt(int kbits, int vbits, const DecodeParams& p, const C
     if (kbits == 16 && vbits == 4) return launch_decode_t<0, 4, NT>(p, kmap, stream, ev0, ev1);
     if (kbits == 3 && vbits == 3) return launch_decode_t<3, 3, NT>(p, kmap, stream, ev0, ev1);
     if (kbits == 4 && vbits == 4) return launch_decode_t<4, 4, NT>(p, kmap, stream, ev0, ev1);
+    if (kbits == 16 && vbits == 3) return launch_decode_t<0, 3, NT>(p, kmap, stream, ev0, ev1);
+    if (kbits == 4 && vbits == 3) return launch_decode_t<4, 3, NT>(p, kmap, stream, ev0, ev1);
     return cudaErrorInvalidValue;
 }
 
@@ -569,9 +571,9 @@ static int smem_of(int nt) {
 int decode_ctas_per_sm(int kbits, int vbits, int group_rows) {
     const int nt = group_rows <= 8 ? 1 : 2;
     int smem = 0;
-    if (kbits == 16) smem = smem_of<0, 4>(nt);
+    if (kbits == 16) smem = vbits == 4 ? smem_of<0, 4>(nt) : smem_of<0, 3>(nt);
     else if (kbits == 3) smem = smem_of<3, 3>(nt);
-    else smem = smem_of<4, 4>(nt);
+    else smem = vbits == 4 ? smem_of<4, 4>(nt) : smem_of<4, 3>(nt);
     int by_smem = (228 * 1024) / (smem + 1024);  // 1 KB per CTA is reserved
     const int by_regs = nt == 1 ? 4 : 3;         // the kernels' launch bounds
     int c = by_smem < by_regs ? by_smem : by_regs;

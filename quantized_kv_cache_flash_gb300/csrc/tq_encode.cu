@@ -504,6 +504,8 @@ int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stre
         if (kbits == 16 && vbits == 4) tq_encode_small_kernel<0, 4><<<sblocks, 128, 0, stream>>>(p);
         else if (kbits == 3 && vbits == 3) tq_encode_small_kernel<3, 3><<<sblocks, 128, 0, stream>>>(p);
         else if (kbits == 4 && vbits == 4) tq_encode_small_kernel<4, 4><<<sblocks, 128, 0, stream>>>(p);
+        else if (kbits == 16 && vbits == 3) tq_encode_small_kernel<0, 3><<<sblocks, 128, 0, stream>>>(p);
+        else if (kbits == 4 && vbits == 3) tq_encode_small_kernel<4, 3><<<sblocks, 128, 0, stream>>>(p);
         else return cudaErrorInvalidValue;
         return cudaGetLastError();
     }
@@ -513,6 +515,8 @@ int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stre
     if (kbits == 16 && vbits == 4) tq_encode_kernel<0, 4><<<blocks, thr, 0, stream>>>(p, kblocks);
     else if (kbits == 3 && vbits == 3) tq_encode_kernel<3, 3><<<blocks, thr, 0, stream>>>(p, kblocks);
     else if (kbits == 4 && vbits == 4) tq_encode_kernel<4, 4><<<blocks, thr, 0, stream>>>(p, kblocks);
+    else if (kbits == 16 && vbits == 3) tq_encode_kernel<0, 3><<<blocks, thr, 0, stream>>>(p, kblocks);
+    else if (kbits == 4 && vbits == 3) tq_encode_kernel<4, 3><<<blocks, thr, 0, stream>>>(p, kblocks);
     else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "tq.h"
+
 namespace tq {
 
 // Decode (split-K) kernel parameters.  One CTA = one (split, batch*kv-head,
@@ -70,5 +72,17 @@ int decode_ctas_per_sm(int kbits, int vbits, int group_rows);
 
 // Query rows per row group for `rows` query rows of one KV head.
 inline int group_rows_for(int rows) { return rows <= 8 ? 8 : 16; }
+
+// (K bits, V bits) of a mode; 16 = fp16 K.
+inline int mode_bits(int mode, int* kb, int* vb) {
+    switch (mode) {
+        case TQ_TURBO4_ASYM: *kb = 16; *vb = 4; return TQ_OK;
+        case TQ_TURBO3: *kb = 3; *vb = 3; return TQ_OK;
+        case TQ_TURBO4: *kb = 4; *vb = 4; return TQ_OK;
+        case TQ_TURBO3_ASYM: *kb = 16; *vb = 3; return TQ_OK;
+        case TQ_TURBO4K_3V: *kb = 4; *vb = 3; return TQ_OK;
+        default: return TQ_ERR_UNSUPPORTED;
+    }
+}
 
 }  // namespace tq

@@ -56,15 +56,6 @@ int scratch_address(void** out) {
     return TQ_OK;
 }
 
-int bits_of(int mode, int* kb, int* vb) {
-    switch (mode) {
-        case TQ_TURBO4_ASYM: *kb = 16; *vb = 4; return TQ_OK;
-        case TQ_TURBO3: *kb = 3; *vb = 3; return TQ_OK;
-        case TQ_TURBO4: *kb = 4; *vb = 4; return TQ_OK;
-        default: return TQ_ERR_UNSUPPORTED;
-    }
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_codebook(const float* cb, int n, int bits) {
@@ -127,7 +118,7 @@ extern "C" int tq_decode_attention_noalloc(const tq_cache* c, const void* q, int
                                            void* out, uint32_t* status, void* stream) {
     int kb, vb;
     if (c == nullptr) return TQ_ERR_INVALID_ARG;
-    int r = bits_of(c->mode, &kb, &vb);
+    int r = tq::mode_bits(c->mode, &kb, &vb);
     if (r != TQ_OK) return r;
     if (c->head_dim != kD) return TQ_ERR_UNSUPPORTED;
     if (c->batch <= 0 || c->num_kv_heads <= 0 || c->capacity <= 0 || (c->capacity % 16) != 0)

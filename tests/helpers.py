@@ -14,7 +14,8 @@ RMS_REL = 2e-3
 BOUNDARY = 1e-5
 BOUNDARY_FRACTION = 1e-4
 
-MODE_BITS = {"turbo4_asym": (16, 4), "turbo3": (3, 3), "turbo4": (4, 4)}
+MODE_BITS = {"turbo4_asym": (16, 4), "turbo3": (3, 3), "turbo4": (4, 4),
+             "turbo3_asym": (16, 3), "turbo4k_3v": (4, 3)}
 
 
 def attention_errors(got, want):

@@ -58,6 +58,12 @@ DECODE_CASES = [
     ("turbo3", 1, 4, 1, [40], 4, 48, 0.05, 1.0),                # causal block, custom scale
     ("turbo4", 1, 16, 2, [16], 8, 16, 0.0, 1.0),                # Tq 8 x G 8 = 64 rows, L = Tq*2
     ("turbo3", 2, 28, 4, [8192, 8191], 1, 8192, 0.0, 1.0),      # Qwen2.5-7B shape, min=max-1
+    ("turbo3_asym", 1, 4, 2, [256], 1, 256, 0.0, 1.0),          # fp16 K + 3-bit V
+    ("turbo3_asym", 2, 28, 4, [3001, 77], 2, 3008, 0.0, 0.5),   # ragged, Tq 2, v_rescale
+    ("turbo3_asym", 1, 32, 2, [900], 4, 912, 0.0, 1.0),         # 64 rows
+    ("turbo4k_3v", 1, 4, 1, [1], 1, 16, 0.0, 1.0),              # 4-bit K + 3-bit V, context 1
+    ("turbo4k_3v", 3, 12, 4, [100, 513, 4000], 1, 4000, 0.0, 1.0),
+    ("turbo4k_3v", 1, 32, 2, [777], 4, 784, 0.05, 1.0),         # 64 rows, custom scale
 ]
 
 
@@ -123,7 +129,7 @@ def _crafted_vectors():
 # T = 300 runs the warp-per-vector kernel (small appends), T = 700 the
 # four-lanes-per-vector kernel (more than 4096 vectors per stream)
 @pytest.mark.parametrize("T", [300, 700])
-@pytest.mark.parametrize("mode", ["turbo3", "turbo4", "turbo4_asym"])
+@pytest.mark.parametrize("mode", ["turbo3", "turbo4", "turbo4_asym", "turbo3_asym", "turbo4k_3v"])
 def test_encode_append_bit_exact(mode, T):
     kb, vb = H.MODE_BITS[mode]
     B, Hkv, cap = 2, 3, 720
@@ -218,6 +224,8 @@ def _e2e(mode, B, Hq, Hkv, L, Tq, cap, outliers_key):
     ("turbo3", 1, 28, 4, 1000, 1, 1024),
     ("turbo4", 2, 32, 8, 700, 1, 704),
     ("turbo3", 1, 32, 8, 600, 4, 608),
+    ("turbo3_asym", 1, 28, 4, 900, 1, 912),
+    ("turbo4k_3v", 2, 32, 8, 500, 2, 512),
 ])
 def test_end_to_end_own_encodings(mode, B, Hq, Hkv, L, Tq, cap):
     _e2e(mode, B, Hq, Hkv, L, Tq, cap, 400 + L)

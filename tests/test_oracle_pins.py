@@ -342,7 +342,7 @@ def _random_unit(rng, mode, L, cbk, cbv):
     return unit
 
 
-@pytest.mark.parametrize("mode", ["turbo4_asym", "turbo3", "turbo4"])
+@pytest.mark.parametrize("mode", ["turbo4_asym", "turbo3", "turbo4", "turbo3_asym", "turbo4k_3v"])
 def test_rotated_basis_identity(mode):
     """rotate(SDPA(q,k,v)) == SDPA(q,k,rotate(v)): the shortcut equals full dequant."""
     rng = np.random.default_rng(11)
