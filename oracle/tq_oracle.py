@@ -371,6 +371,36 @@ def softmax_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float,
     return out
 
 
+def softmax_attention_sparse_v(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float,
+                               visible: np.ndarray, tau: float):
+    """Sparse-V attention for one KV head: the V skip of turboquant_plus
+    (smem-dequant-experiment.md, "What Would Actually Work" item 2: V dequant
+    is skipped for negligible weights) at the threshold the mlxcel ADR 0002
+    commit calls exact (tau = 1e-6).
+
+    The softmax weights p are the ordinary ones, normalised over every visible
+    token; a token whose weight is below tau adds nothing to the weighted sum
+    of V (the denominator keeps it).  Returns (out, bound) with
+    bound[r, i] = sum over the skipped tokens of p_t * |V[t, i]|: the most any
+    subset of the skipped tokens can add to out[r, i].
+    """
+    R = q.shape[0]
+    out = np.zeros((R, V.shape[1]))
+    bound = np.zeros((R, V.shape[1]))
+    scores = (np.asarray(q, np.float64) @ np.asarray(K, np.float64).T) * scale
+    for r in range(R):
+        n = int(visible[r])
+        if n <= 0:
+            continue
+        sr = scores[r, :n]
+        p = np.exp(sr - sr.max())
+        p /= p.sum()
+        skip = p < tau
+        out[r] = np.where(skip, 0.0, p) @ V[:n]
+        bound[r] = np.where(skip, p, 0.0) @ np.abs(V[:n])
+    return out, bound
+
+
 def visible_counts(L: int, tq: int) -> np.ndarray:
     """Query j of a Tq block at the end of an L-token context sees L - Tq + j + 1 tokens."""
     return np.array([L - tq + j + 1 for j in range(tq)])
@@ -400,6 +430,21 @@ def decode_unit(mode: str, q_rows: np.ndarray, unit: dict, L: int, tq: int, G: i
     q = np.asarray(q_rows, np.float64).reshape(G * tq, D)
     vis = np.tile(visible_counts(L, tq), G)
     return softmax_attention(q, K, V, scale, vis).reshape(G, tq, D)
+
+
+def decode_unit_sparse_v(mode: str, q_rows: np.ndarray, unit: dict, L: int, tq: int, G: int,
+                         cbk, cbv, s, scale: float, v_rescale: float, tau: float):
+    """Sparse-V decode for one (b, kv-head): (out, bound), both fp64 [G, Tq, 128].
+
+    Full dequant, then ``softmax_attention_sparse_v``, then v_rescale (|v_rescale|
+    for the bound).
+    """
+    K, V = unit_kv_full(mode, unit, cbk, cbv, s)
+    K, V = K[:L], V[:L] * v_rescale
+    q = np.asarray(q_rows, np.float64).reshape(G * tq, D)
+    vis = np.tile(visible_counts(L, tq), G)
+    out, bound = softmax_attention_sparse_v(q, K, V, scale, vis, tau)
+    return out.reshape(G, tq, D), bound.reshape(G, tq, D)
 
 
 def decode_rotated_unit(mode: str, q_rows, unit: dict, L: int, tq: int, G: int,

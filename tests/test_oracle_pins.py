@@ -443,3 +443,70 @@ def test_dequant_reconstructs_encoded_vector():
     c = cb.astype(np.float64)
     near = c[idx]
     assert np.all(np.abs(u - near) <= np.abs(u[..., None] - c).min(-1) + 1e-12)
+
+
+# --------------------------------------------------------------------------
+# sparse-V (V skipped for softmax weights below tau)
+# --------------------------------------------------------------------------
+def test_sparse_v_two_token_closed_form():
+    # scores 0 and -20 (scale 1): p1 = e^-20 / (1 + e^-20) ~ 2.06e-9
+    q = np.zeros((1, 4)); q[0, 0] = 1.0
+    K = np.zeros((2, 4)); K[1, 0] = -20.0
+    V = np.array([[1.0, 2.0, 0.0, -3.0], [1000.0, -1000.0, 5.0, 0.0]])
+    p1 = math.exp(-20.0) / (1.0 + math.exp(-20.0))
+    p0 = 1.0 / (1.0 + math.exp(-20.0))
+    out, bound = o.softmax_attention_sparse_v(q, K, V, 1.0, np.array([2]), 1e-6)
+    assert np.allclose(out[0], p0 * V[0], rtol=1e-15, atol=0)
+    assert np.allclose(bound[0], p1 * np.abs(V[1]), rtol=1e-15, atol=0)
+    # below the smaller weight nothing is skipped
+    out, bound = o.softmax_attention_sparse_v(q, K, V, 1.0, np.array([2]), 1e-10)
+    assert np.allclose(out[0], p0 * V[0] + p1 * V[1], rtol=1e-15, atol=0)
+    assert not bound.any()
+
+
+def test_sparse_v_degenerate_thresholds():
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((3, 16)) * 4; K = rng.standard_normal((40, 16))
+    V = rng.standard_normal((40, 16)); vis = np.array([40, 17, 1])
+    full = o.softmax_attention(q, K, V, 0.5, vis)
+    out, bound = o.softmax_attention_sparse_v(q, K, V, 0.5, vis, 0.0)
+    assert np.array_equal(out, full) and not bound.any()
+    # every weight is <= 1, so tau > 1 skips everything
+    out, bound = o.softmax_attention_sparse_v(q, K, V, 0.5, vis, 1.5)
+    assert not out.any()
+    assert np.allclose(bound, o.softmax_attention(q, K, np.abs(V), 0.5, vis), rtol=1e-14)
+
+
+def test_sparse_v_equals_naive_skip_loop_and_stays_within_bound():
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((4, 8)) * 6; K = rng.standard_normal((30, 8))
+    V = rng.standard_normal((30, 8)); tau = 1e-6
+    out, bound = o.softmax_attention_sparse_v(q, K, V, 1.0, np.full(4, 30), tau)
+    skipped = 0
+    for r in range(4):
+        sc = [sum(q[r, d] * K[t, d] for d in range(8)) for t in range(30)]
+        m = max(sc)
+        w = [math.exp(v - m) for v in sc]
+        z = sum(w)
+        want = np.zeros(8)
+        for t in range(30):
+            if w[t] / z >= tau:
+                want += (w[t] / z) * V[t]
+            else:
+                skipped += 1
+        assert np.max(np.abs(out[r] - want)) < 1e-12
+    assert skipped > 0      # sharp queries: the threshold is not vacuous here
+    full = o.softmax_attention(q, K, V, 1.0, np.full(4, 30))
+    assert np.all(np.abs(out - full) <= bound + 1e-15)
+
+
+def test_sparse_v_decode_unit_reduces_to_decode_unit_at_zero_tau():
+    rng = np.random.default_rng(23)
+    s = o.sign_vector(42); cb = o.codebook(3)
+    unit = _random_unit(rng, "turbo3", 33, cb, cb)
+    q = rng.standard_normal((2, 3, 128)).astype(np.float16)
+    want = o.decode_unit("turbo3", q, unit, 33, 3, 2, cb, cb, s, 0.1, -0.5)
+    got, bound = o.decode_unit_sparse_v("turbo3", q, unit, 33, 3, 2, cb, cb, s, 0.1, -0.5, 0.0)
+    assert np.array_equal(got, want) and not bound.any()
+    got, bound = o.decode_unit_sparse_v("turbo3", q, unit, 33, 3, 2, cb, cb, s, 0.1, -0.5, 2.0)
+    assert not got.any() and np.all(bound >= np.abs(want) - 1e-12)
