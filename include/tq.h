@@ -152,6 +152,28 @@ int tq_decode_attention(tq_ctx **ctx, const tq_cache *cache, const void *q,
                         float scale, void *out, void *stream);
 
 /*
+ * Sparse-V decode: tq_decode_attention, except that a token whose softmax
+ * weight is below tau adds nothing to the weighted sum of V (its weight still
+ * counts in the normaliser).  This is the V skip of turboquant_plus
+ * (smem-dequant-experiment.md, "What Would Actually Work" item 2: V dequant is
+ * skipped for negligible weights), which the mlxcel ADR 0002 commit ("Turbo KV
+ * split-dequant vs fused, sparse-V study") finds exact at tau = 1e-6 and
+ * places inside a fused kernel.
+ *   tau: finite, >= 0 (TQ_ERR_INVALID_ARG otherwise); 0 gives exactly the
+ *        plain decode.
+ * The kernel skips the V dequant and P.V of a 16-token tile when, for every
+ * query row of the tile's row group, each token's weight taken against the
+ * running maximum of its split is below tau.  That weight is never below the
+ * final normalised one, so a skipped token is always one the definition
+ * skips; a token the definition skips may still be kept.  Hence the result
+ * differs from the full decode by at most the sum, over the tokens with weight
+ * below tau, of weight * |v| per output element.
+ */
+int tq_decode_attention_sparse_v(tq_ctx **ctx, const tq_cache *cache, const void *q,
+                                 int32_t num_q_heads, int32_t tq, int32_t max_len_hint,
+                                 float scale, float tau, void *out, void *stream);
+
+/*
  * No-allocation decode (this entry point has no counterpart on the pages; it
  * exists for callers that cannot allocate device memory on the decode path,
  * e.g. a server that owns all device memory through its own pools, or a

@@ -368,8 +368,15 @@ int tq_encode_append(tq_ctx** pctx, const tq_cache* c, const void* k_new, const 
         tq::launch_encode(kb, vb, p, static_cast<cudaStream_t>(stream))));
 }
 
-int tq_decode_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_heads,
-                        int32_t tq_rows, int32_t max_len_hint, float scale, void* out, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Both decode entry points: tau = 0 is the plain decode, tau > 0 skips the V
+// work of 16-token tiles whose softmax weights are all below tau.
+int decode_impl(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_heads,
+                int32_t tq_rows, int32_t max_len_hint, float scale, float tau, void* out,
+                void* stream) {
     int kb, vb;
     int r = check_cache(c, &kb, &vb);
     if (r != TQ_OK) return r;
@@ -419,6 +426,7 @@ int tq_decode_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t
     p.split_tokens = split_tokens;
     p.nsplit = nsplit;
     p.scale_log2e = sc * 1.4426950408889634f;
+    p.sparse_tau = tau;
     if (kb != 16) std::memcpy(p.ktab, ctx->ktab.tab, sizeof(p.ktab));
     std::memcpy(p.vtab, ctx->vtab.tab, sizeof(p.vtab));
     std::memcpy(p.signs, ctx->signs, sizeof(p.signs));
@@ -460,6 +468,22 @@ int tq_decode_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t
     cp.v_rescale = c->v_rescale;
     std::memcpy(cp.signs, ctx->signs, sizeof(cp.signs));
     return cuda_err(static_cast<cudaError_t>(tq::launch_combine(cp, s)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int tq_decode_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_heads,
+                        int32_t tq_rows, int32_t max_len_hint, float scale, void* out, void* stream) {
+    return decode_impl(pctx, c, q, num_q_heads, tq_rows, max_len_hint, scale, 0.f, out, stream);
+}
+
+int tq_decode_attention_sparse_v(tq_ctx** pctx, const tq_cache* c, const void* q,
+                                 int32_t num_q_heads, int32_t tq_rows, int32_t max_len_hint,
+                                 float scale, float tau, void* out, void* stream) {
+    if (!(tau >= 0.f) || !std::isfinite(tau)) return TQ_ERR_INVALID_ARG;
+    return decode_impl(pctx, c, q, num_q_heads, tq_rows, max_len_hint, scale, tau, out, stream);
 }
 
 void tq_free(tq_ctx* ctx) {

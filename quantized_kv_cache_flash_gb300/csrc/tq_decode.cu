@@ -196,6 +196,13 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
 #pragma unroll
         for (int e = 0; e < 2; ++e) lim[n][e] = L - p.tq + ((rbase + 8 * n + 2 * t + e) % p.tq);
     const int all_visible_below = L - p.tq + 1;  // tokens below this are seen by every row
+    // rows of this thread that are real query rows (not padding of the group)
+    bool row_ok[NT][2];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) row_ok[n][e] = rbase + 8 * n + 2 * t + e < p.rows;
+    const bool sparse = p.sparse_tau > 0.f;
 
     float O[NT][8][4];
 #pragma unroll
@@ -330,10 +337,29 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
                     l[n][e] += s;
                 }
 
+            // Sparse V: a tile whose weights are all below tau for every real row
+            // skips its V dequant and P.V.  Here p = 2^(x - base) with base at
+            // most the running max, so p is never below the final normalised
+            // weight: only tokens the definition skips can be skipped.
+            bool keep[2] = {true, true};
+            if (sparse) {
+    #pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+                    float mx = 0.f;
+    #pragma unroll
+                    for (int n = 0; n < NT; ++n)
+    #pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            if (row_ok[n][e]) mx = fmaxf(mx, fmaxf(x[tile][n][e], x[tile][n][e + 2]));
+                    keep[tile] = __any_sync(0xffffffffu, mx >= p.sparse_tau);
+                }
+            }
+
             // ---------------- O^T += C_v^T . (P n_v)^T (rotated basis) ----------------
     #pragma unroll
             for (int tile = 0; tile < 2; ++tile) {
                 if (!FULL && tile == 1 && !two) break;
+                if (!keep[tile]) continue;
                 uint32_t pb0[NT], pb1[NT];
     #pragma unroll
                 for (int n = 0; n < NT; ++n) {

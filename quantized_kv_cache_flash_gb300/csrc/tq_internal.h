@@ -27,6 +27,7 @@ struct DecodeParams {
     int32_t batch, hkv, hq, group, tq, rows, row_groups, group_rows, cap, max_len;
     int32_t split_tokens, nsplit;
     float scale_log2e;        // softmax scale * log2(e)
+    float sparse_tau;         // sparse-V threshold on the softmax weight (0: off)
     uint32_t ktab[4];         // prmt byte tables of the K codebook (lo0, lo1, hi0, hi1)
     uint32_t vtab[4];
     uint32_t signs[4];        // bit d set <=> s_d = -1

@@ -133,3 +133,31 @@ def oracle_decode(mode, q, units, lengths, Hkv, tq, scale, v_rescale, rot_seed=4
                                                   int(lengths[b]), tq, G, cbk, cbv, s, scale,
                                                   v_rescale)
     return out
+
+
+def oracle_decode_sparse_v(mode, q, units, lengths, Hkv, tq, scale, v_rescale, tau, rot_seed=42):
+    """Oracle sparse-V output and bound, both fp64 [B, Hq, Tq, 128]."""
+    kb, vb = MODE_BITS[mode]
+    cbk = o.codebook(kb) if kb != 16 else None
+    cbv = o.codebook(vb)
+    s = o.sign_vector(rot_seed)
+    B, Hq = q.shape[0], q.shape[1]
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, tq, 128))
+    bound = np.zeros((B, Hq, tq, 128))
+    for (b, h), unit in units.items():
+        sl = slice(h * G, (h + 1) * G)
+        out[b, sl], bound[b, sl] = o.decode_unit_sparse_v(mode, q[b, sl], unit, int(lengths[b]), tq,
+                                                          G, cbk, cbv, s, scale, v_rescale, tau)
+    return out, bound
+
+
+def assert_within_skip_bound(got, full, bound, what=""):
+    """got may drop any subset of the tokens covered by `bound`: the error left
+    after taking `bound` off must meet the ordinary attention bounds."""
+    got = np.asarray(got, np.float64)
+    rms = math.sqrt(float(np.mean(full * full)))
+    excess = np.maximum(np.abs(got - full) - bound, 0.0)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert float(excess.max()) <= MAX_ABS_REL * rms, f"{what}: max excess {excess.max():.3e}"
+    assert math.sqrt(float(np.mean(excess * excess))) <= RMS_REL * rms, f"{what}: rms excess"

@@ -1,0 +1,85 @@
+"""GPU parity of sparse-V decode (V skipped for softmax weights below tau).
+
+The kernel may skip any token whose normalised weight is below tau (it never
+skips others), so its output must lie within the oracle's bound of what the
+skipped tokens can add; the bound is taken at 2 tau to cover the rounding of
+the kernel's own weights.  Sharp queries (q scaled up) make most weights tiny,
+so most tiles are skipped.
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import quantized_kv_cache_flash_gb300 as tqf
+from quantized_kv_cache_flash_gb300 import workloads as wl
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+DEV = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    global DEV
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_kv_cache_flash_gb300 import build
+    build.build()
+    DEV = torch.device("cuda", 0)
+    yield
+
+
+CASES = [
+    # mode, B, Hq, Hkv, lengths, Tq, cap, q scale, tau
+    ("turbo4", 2, 32, 8, [3000, 1777], 1, 3008, 32.0, 1e-6),
+    ("turbo3", 1, 32, 8, [2600], 4, 2608, 32.0, 1e-6),            # Tq 4: 16 rows, causal block
+    ("turbo4_asym", 1, 28, 4, [4100], 1, 4112, 4.0, 1e-6),
+    ("turbo3_asym", 1, 8, 2, [900], 1, 912, 32.0, 0.05),          # large tau: skips are visible
+    ("turbo4k_3v", 2, 12, 4, [700, 1500], 2, 1504, 32.0, 0.05),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-tau{c[8]:g}")
+def test_sparse_v_within_bound_of_full_decode(case):
+    mode, B, Hq, Hkv, lengths, Tq, cap, qs, tau = case
+    key = 9100 + sum(lengths) + Hq
+    kd, kn, vd, vn = H.random_cache(mode, B, Hkv, cap, key)
+    q_np = (wl.random_fp16(key + 3, (B, Hq, Tq, 128)).astype(np.float32) * qs).astype(np.float16)
+    cache = H.gpu_cache_from_records(mode, B, Hkv, cap, lengths, kd, kn, vd, vn, DEV, v_rescale=0.75)
+    ctx = tqf.Context()
+    q = H.upload(q_np, DEV)
+    sparse = torch.empty_like(q)
+    full = torch.empty_like(q)
+    tqf.tq_decode_attention_sparse_v(ctx, cache, q, sparse, max(lengths), tau)
+    tqf.tq_decode_attention(ctx, cache, q, full, max(lengths))
+    torch.cuda.synchronize()
+    assert tqf.tq_get_status(ctx) == 0
+    units = {(b, h): H.oracle_unit_from_records(mode, kd, kn, vd, vn, b, h, lengths[b])
+             for b in range(B) for h in range(Hkv)}
+    sc = 1 / math.sqrt(128)
+    want_full = H.oracle_decode(mode, q_np, units, lengths, Hkv, Tq, sc, 0.75)
+    _, bound = H.oracle_decode_sparse_v(mode, q_np, units, lengths, Hkv, Tq, sc, 0.75, 2 * tau)
+    got = sparse.float().cpu().numpy()
+    H.assert_attention_close(full.float().cpu().numpy(), want_full, f"{case} full")
+    H.assert_within_skip_bound(got, want_full, bound, str(case))
+    if tau >= 0.01:
+        # the skip really happened: dropped weights of this size show in fp16
+        rms = math.sqrt(float(np.mean(want_full ** 2)))
+        assert float(np.abs(got - full.float().cpu().numpy()).max()) > 1e-3 * rms
+
+
+def test_sparse_v_zero_threshold_is_the_plain_decode():
+    mode, B, Hq, Hkv, L, cap = "turbo4", 1, 16, 4, 1234, 1248
+    kd, kn, vd, vn = H.random_cache(mode, B, Hkv, cap, 77)
+    cache = H.gpu_cache_from_records(mode, B, Hkv, cap, [L], kd, kn, vd, vn, DEV)
+    q = H.upload(wl.random_fp16(78, (B, Hq, 1, 128)), DEV)
+    a, b = torch.empty_like(q), torch.empty_like(q)
+    ctx = tqf.Context()
+    tqf.tq_decode_attention_sparse_v(ctx, cache, q, a, L, 0.0)
+    tqf.tq_decode_attention(ctx, cache, q, b, L)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)

@@ -142,6 +142,14 @@ def test_errors_pointers(lib):
     assert _decode(lib, _cache(mode=4, k_norm=None)) == tqf.TQ_ERR_INVALID_ARG   # 4-bit K needs them
 
 
+def test_errors_sparse_v_threshold(lib):
+    for tau in (-1e-6, float("nan"), float("inf")):
+        ctx = ctypes.c_void_p(None)
+        r = lib.tq_decode_attention_sparse_v(ctypes.byref(ctx), ctypes.byref(_cache()), FAKE + 65536,
+                                             4, 1, 32, 0.0, tau, FAKE + 131072, None)
+        assert r == tqf.TQ_ERR_INVALID_ARG and ctx.value is None
+
+
 def test_errors_codebook(lib):
     cb = tqf.tq_lloyd_max_codebook(3)
     asym = list(cb); asym[0] -= 1e-3
