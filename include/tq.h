@@ -187,8 +187,9 @@ int tq_decode_attention_sparse_v(tq_ctx **ctx, const tq_cache *cache, const void
  *   status: device pointer to a caller-owned uint32 into which the kernels OR
  *           TQ_STATUS_* bits (the caller clears it), or NULL to drop them.
  *   Returns TQ_ERR_CAPACITY when the problem needs more scratch than the
- *   array holds (batch * num_kv_heads * ceil(rows/16) split slots of 8320
- *   bytes each must fit; the split count is reduced to fit when possible).
+ *   array holds: one 8320-byte slot per decode CTA and one per (batch, kv
+ *   head, row group) unit must fit (a row group is 8 query rows, or 16 when a
+ *   kv head has more than 8); the CTA count is reduced to fit when possible.
  * The first call on a device, with that device current, looks up the array's
  * address (cudaGetSymbolAddress, once per device); make that first call before
  * any stream capture.  All calls share the one array and it keeps the last
@@ -215,8 +216,12 @@ int tq_lloyd_max_codebook(int32_t bits, float *out);
 /* Host-only: bytes of one packed record: 48 (bits 3), 64 (bits 4), 256 (16 = fp16). */
 int tq_record_bytes(int32_t bits);
 
-/* Host-only: the split-K plan tq_decode_attention would use: tokens per split
- * and number of splits (per sequence and row group). */
+/* Host-only: the decode grid tq_decode_attention would launch when every
+ * sequence is max_len_hint long.  The grid is two waves of CTAs that split the
+ * context's 32-token chunks over all (batch, kv head, row group) units evenly
+ * (the split follows the actual lengths on the device):
+ *   *num_splits   = number of decode CTAs;
+ *   *split_tokens = tokens each CTA streams at that length (a multiple of 32). */
 int tq_plan_splits(int32_t mode, int32_t batch, int32_t num_kv_heads,
                    int32_t rows_per_kv_head, int32_t max_len_hint,
                    int32_t *split_tokens, int32_t *num_splits);

@@ -235,21 +235,15 @@ int prepare_kmap(tq_ctx* ctx, const tq_cache* c) {
     return TQ_OK;
 }
 
-void plan(int kb, int vb, int group_rows, int batch, int hkv, int row_groups, int max_len,
-          int* split_tokens, int* nsplit) {
-    const long long units = 1ll * batch * hkv * row_groups;
-    const int cps = tq::decode_ctas_per_sm(kb, vb, group_rows);
-    // aim for ~2 waves of CTAs over the context, splits a multiple of 32 tokens
-    const long long target_ctas = 2ll * kSMs * cps;
-    long long per_unit = (target_ctas + units - 1) / units;
-    if (per_unit < 1) per_unit = 1;
-    long long st = (max_len + per_unit - 1) / per_unit;
-    st = ((st + 31) / 32) * 32;
-    st = std::max<long long>(st, 256);
-    st = std::min<long long>(st, 1ll << 20);
-    *split_tokens = int(st);
-    *nsplit = int((max_len + st - 1) / st);
-    if (*nsplit < 1) *nsplit = 1;
+// Decode grid: two waves of resident CTAs (the second lets the block
+// scheduler even out SMs that run at different speeds), fewer when the
+// context (at the hint length) gives a CTA less than two 32-token chunks per
+// warp.
+int plan_ctas(int kb, int vb, int group_rows, long long units, int max_len) {
+    const long long slots = 2ll * kSMs * tq::decode_ctas_per_sm(kb, vb, group_rows);
+    const long long chunks = units * ((max_len + 31) / 32);
+    long long ctas = std::min(slots, (chunks + 7) / 8);
+    return int(std::max<long long>(ctas, 1));
 }
 
 int ensure_work(tq_ctx* ctx, size_t bytes) {
@@ -325,8 +319,11 @@ int tq_plan_splits(int32_t mode, int32_t batch, int32_t num_kv_heads, int32_t ro
         split_tokens == nullptr || num_splits == nullptr)
         return TQ_ERR_INVALID_ARG;
     const int gr = tq::group_rows_for(rows_per_kv_head);
-    const int rg = (rows_per_kv_head + gr - 1) / gr;
-    plan(kb, vb, gr, batch, num_kv_heads, rg, max_len_hint, split_tokens, num_splits);
+    const long long units = 1ll * batch * num_kv_heads * ((rows_per_kv_head + gr - 1) / gr);
+    const int ctas = plan_ctas(kb, vb, gr, units, max_len_hint);
+    const long long chunks = units * ((max_len_hint + 31) / 32);
+    *num_splits = ctas;
+    *split_tokens = int(std::min<long long>((chunks + ctas - 1) / ctas * 32, 1ll << 30));
     return TQ_OK;
 }
 
@@ -396,10 +393,9 @@ int decode_impl(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_h
 
     const int group_rows = tq::group_rows_for(rows);
     const int row_groups = (rows + group_rows - 1) / group_rows;
-    int split_tokens, nsplit;
-    plan(kb, vb, group_rows, c->batch, c->num_kv_heads, row_groups, max_len_hint, &split_tokens,
-         &nsplit);
-    const size_t slots = size_t(c->batch) * c->num_kv_heads * row_groups * nsplit * 16;
+    const long long units = 1ll * c->batch * c->num_kv_heads * row_groups;
+    const int ctas = plan_ctas(kb, vb, group_rows, units, max_len_hint);
+    const size_t slots = size_t(ctas + units) * 16;
     if ((r = ensure_work(ctx, slots * (kD + 2) * sizeof(float))) != TQ_OK) return r;
 
     const float sc = (scale == 0.f) ? 1.0f / std::sqrt(float(kD)) : scale;
@@ -423,8 +419,7 @@ int decode_impl(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_h
     p.group_rows = group_rows;
     p.cap = c->capacity;
     p.max_len = max_len_hint;
-    p.split_tokens = split_tokens;
-    p.nsplit = nsplit;
+    p.num_ctas = ctas;
     p.scale_log2e = sc * 1.4426950408889634f;
     p.sparse_tau = tau;
     if (kb != 16) std::memcpy(p.ktab, ctx->ktab.tab, sizeof(p.ktab));
@@ -463,8 +458,7 @@ int decode_impl(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_h
     cp.row_groups = row_groups;
     cp.group_rows = group_rows;
     cp.max_len = max_len_hint;
-    cp.split_tokens = split_tokens;
-    cp.nsplit = nsplit;
+    cp.num_ctas = ctas;
     cp.v_rescale = c->v_rescale;
     std::memcpy(cp.signs, ctx->signs, sizeof(cp.signs));
     return cuda_err(static_cast<cudaError_t>(tq::launch_combine(cp, s)));

@@ -7,17 +7,15 @@
 // V is never brought back to the original basis: P.V accumulates
 // p(t) * n_v(t) * c[idx_v(t)] and only the [rows, 128] result is
 // inverse-rotated, in the combine kernel (mlxcel pull request #369, Change:
-// "inverse-rotates only the small [B, Hq, Tq, D] output").
+// the per-token inverse transform of a full V dequant is avoided by rotating
+// the small output back instead).
 //
-// Work split: CTA = 4 warps on one (split of the context, batch*kv-head, row
-// group).  Each warp streams its own 32-token chunks through a private ring
-// of shared-memory stages filled by 1-D bulk copies (tensor-map tile copies
-// with 128-byte swizzle for fp16 K), dequantizes in registers and runs the
-// two contractions as warp MMAs with the query rows as M = 16:
-//   S[16 x 8 tok]   = Rot(q)[16 x 128] . C_k^T            (8 k-steps)
-//   O[16 x 128]    += (P * n_v)[16 x 16 tok] . C_v[16 x 128] (16 n-tiles)
-// The K operand of a thread is its own token's quarter record (32 dims); the
-// V operand comes from the same dequant followed by an 8x8 transpose.
+// Work split: two waves of CTAs, each taking an equal share of the context's
+// 32-token chunks over all (batch, kv head, row group) units.  A CTA's 4 warps
+// stream their own chunks through private rings of shared-memory stages
+// filled by 1-D bulk copies (tensor-map tile copies with 128-byte swizzle for
+// fp16 K), dequantize in registers and run both contractions as warp MMAs
+// with the 16 tokens of a tile as M and up to 8 query rows per n-tile as N.
 #include <float.h>
 
 #include <type_traits>
@@ -27,10 +25,12 @@
 
 namespace tq {
 
+constexpr int kChunkTokens = 32;  // tokens per warp pipeline stage (2 MMA tiles)
+
 template <int KB, int VB, int NT>
 struct DecCfg {
     static constexpr int kWarps = 4;
-    static constexpr int kChunk = 32;                       // tokens per warp stage (2 MMA tiles)
+    static constexpr int kChunk = kChunkTokens;
     static constexpr int kStages = (KB == 0 || NT == 1) ? 2 : 3;
     static constexpr int kRows = 8 * NT;                    // query rows per row group
     static constexpr int kMinCtas = (NT == 1) ? 4 : 3;      // resident CTAs per SM targeted
@@ -48,7 +48,8 @@ struct DecCfg {
     static constexpr int kPipeBytes = kWarps * kStages * kStage;
     static constexpr int kQOff = kPipeBytes;                 // fp32 [kRows][128] query rows
     static constexpr int kBarOff = kQOff + kRows * kD * 4;
-    static constexpr int kSmem = kBarOff + kWarps * kStages * 8;
+    static constexpr int kScanOff = (kBarOff + kWarps * kStages * 8 + 15) / 16 * 16;
+    static constexpr int kSmem = kScanOff + kWarps * 4 * 32 * 4;  // per-warp batch scan
     static constexpr int kSmemAlloc = kSmem + 1024;          // base alignment slack
     // epilogue scratch (reuses the pipeline): per warp O[kRows][kOStride] + (m, l)[kRows]
     static constexpr int kOStride = kD + 4;
@@ -77,8 +78,103 @@ __device__ __forceinline__ void dequant_quarter(const uint8_t* rec, const Tables
     }
 }
 
-// One CTA: 4 warps on one (split, batch*kv-head, row group).  Per 16-token
-// tile a warp runs
+// Work split (token-balanced): the (batch, kv head, row group) units
+// are laid end to end as 32-token chunks, unit u holding ceil(min(len_b,
+// max_len) / 32) chunks of batch b; CTA c of P takes the global chunks
+// [c*C/P, (c+1)*C/P) of the C in total, so every CTA streams the same number
+// of bytes whatever the length mix.  A CTA's range can cover the end of one
+// unit and the start of the next: it writes one partial per unit it touches,
+// into slot c + u (unique: a later CTA never touches an earlier unit).
+__device__ __forceinline__ int unit_chunks(const int32_t* lengths, int b, int max_len) {
+    const int L = min(lengths[b], max_len);
+    return L > 0 ? (L + kChunkTokens - 1) / kChunkTokens : 0;
+}
+
+// Chunk bookkeeping over the batch, warp-parallel and warp-uniform in its
+// results.  Lane i holds batch i of the first 32 (its length, its chunks over
+// all per_b units, and the inclusive prefix of those): for batches of up to 32
+// sequences one load of `lengths` per lane serves the whole kernel; larger
+// batches rescan global memory block by block.  Chunk counts stay below 2^30
+// (cache rows < 2^31, at most 16 row groups).
+struct BatchScan {
+    int* s;  // this warp's copy in shared memory: len, nch, v, inc, 32 ints each
+
+    __device__ __forceinline__ void init(int* smem_scan, const int32_t* lengths, int batch,
+                                         int per_b, int max_len, int lane) {
+        s = smem_scan;
+        const int len = lane < batch ? lengths[lane] : 0;
+        const int nch = lane < batch ? unit_chunks(lengths, lane, max_len) : 0;
+        const int v = nch * per_b;
+        int inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        s[lane] = len;
+        s[32 + lane] = nch;
+        s[64 + lane] = v;
+        s[96 + lane] = inc;
+        __syncwarp();
+    }
+
+    __device__ __forceinline__ int total(const int32_t* lengths, int batch, int per_b, int max_len,
+                                         int lane) const {
+        const int first = s[96 + 31];  // the first 32 batches
+        int sum = 0;
+        for (int b = 32 + lane; b < batch; b += 32) sum += unit_chunks(lengths, b, max_len) * per_b;
+        if (batch > 32) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        }
+        return first + sum;
+    }
+
+    // batch b holding global chunk pos, the chunks of all batches before it,
+    // b's length and chunks per unit
+    __device__ __forceinline__ void locate(const int32_t* lengths, int batch, int per_b, int max_len,
+                                           int pos, int lane, int& b, int& before, int& L,
+                                           int& nchunk) const {
+        unsigned hit = __ballot_sync(0xffffffffu, s[96 + lane] > pos && lane < batch);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            b = l;
+            before = s[96 + l] - s[64 + l];
+            L = s[l];
+            nchunk = s[32 + l];
+            return;
+        }
+        int cum = s[96 + 31];
+        for (int base = 32; base < batch; base += 32) {
+            const int bb = base + lane;
+            const int n = bb < batch ? unit_chunks(lengths, bb, max_len) : 0;
+            const int w = n * per_b;
+            int c = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, c, o);
+                if (lane >= o) c += y;
+            }
+            hit = __ballot_sync(0xffffffffu, bb < batch && cum + c > pos);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                b = base + l;
+                before = cum + __shfl_sync(0xffffffffu, c - w, l);
+                L = lengths[b];
+                nchunk = __shfl_sync(0xffffffffu, n, l);
+                return;
+            }
+            cum += __shfl_sync(0xffffffffu, c, 31);
+        }
+        b = batch;  // pos past the end (not reached by the callers)
+        before = cum;
+        L = 0;
+        nchunk = 0;
+    }
+};
+
+// One CTA: 4 warps over this CTA's chunk range, one unit segment at a time.
+// Per 16-token tile a warp runs
 //   S^T[16 tok x 8 rows]  = C_k[16 x 128] . Rot(q)^T      (8 k-steps per row tile)
 //   O^T[128 x 8 rows]    += C_v^T[128 x 16 tok] . (P n_v)^T (8 dim tiles)
 // with the tokens (M = 16) dequantised in registers: a thread owns tokens g and
@@ -98,411 +194,446 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int split = blockIdx.x, unit = blockIdx.y, rg = blockIdx.z;
-    const int b = unit / p.hkv, h = unit - b * p.hkv;
-    const int L = p.lengths[b];
-    const int t_lim = min(L, p.max_len);
-    const int t_begin = split * p.split_tokens;
-    const int t_end = min(t_begin + p.split_tokens, t_lim);
-    if (t_begin >= t_end) return;  // no tokens in this split (uniform over the CTA)
-    const int nchunks = (t_end - t_begin + C::kChunk - 1) / C::kChunk;
-    const size_t row0 = static_cast<size_t>(unit) * p.cap;
+    const int per_b = p.hkv * p.row_groups;
+    BatchScan scan;
+    scan.init(reinterpret_cast<int*>(smem + C::kScanOff) + warp * 128, p.lengths, p.batch, per_b,
+              p.max_len, lane);
+    // (each value the copies and masks derive from goes through a lane-0
+    // shuffle, which lets the compiler keep them in uniform registers)
+    const int C_all = __shfl_sync(0xffffffffu, scan.total(p.lengths, p.batch, per_b, p.max_len, lane), 0);
+    // floor(c * C_all / P) in 32-bit arithmetic: c * (C_all mod P) < P^2 < 2^31
+    const int P = static_cast<int>(gridDim.x), cq = C_all / P, cr = C_all - cq * P;
+    const int c_me = static_cast<int>(blockIdx.x);
+    const int lo = c_me * cq + (c_me * cr) / P;
+    const int hi = (c_me + 1) * cq + ((c_me + 1) * cr) / P;
+    if (lo >= hi) return;  // no chunks for this CTA (uniform over the CTA)
 
     uint8_t* wpipe = smem + warp * C::kStages * C::kStage;
     const uint32_t bar0 = smem_u32(smem + C::kBarOff) + warp * C::kStages * 8;
-
-    auto issue = [&](int c, int stage) {  // lane 0 only
-        const int tok0 = t_begin + c * C::kChunk;
-        const int nval = min(C::kChunk, t_end - tok0);
-        const uint32_t dst = smem_u32(wpipe + stage * C::kStage);
-        const uint32_t bar = bar0 + stage * 8;
-        const uint32_t nb = static_cast<uint32_t>((nval + 7) & ~7) * 2;  // norms, 16-B multiple
-        uint32_t bytes = nval * C::kRbV + nb;
-        if (KB == 0) bytes += 2 * 4096;
-        else bytes += nval * C::kRbK + nb;
-        mbar_arrive_expect_tx(bar, bytes);
-        if constexpr (KB == 0) {
-            tma_g2s_2d(dst, &kmap, 0, static_cast<int32_t>(row0 + tok0), bar);
-            tma_g2s_2d(dst + 4096, &kmap, 64, static_cast<int32_t>(row0 + tok0), bar);
-        } else {
-            bulk_g2s(dst, p.k_codes + (row0 + tok0) * C::kRbK, nval * C::kRbK, bar);
-            bulk_g2s(dst + C::kKnOff, p.k_norm + row0 + tok0, nb, bar);
-        }
-        bulk_g2s(dst + C::kVOff, p.v_codes + (row0 + tok0) * C::kRbV, nval * C::kRbV, bar);
-        bulk_g2s(dst + C::kVnOff, p.v_norm + row0 + tok0, nb, bar);
-    };
-
     if (lane == 0) {
         for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_barrier_init();
-        for (int s = 0; s < C::kStages; ++s) {
-            const int c = warp + C::kWarps * s;
-            if (c < nchunks) issue(c, s);
-        }
     }
     __syncwarp();
-
-    // ---- query rows of this row group -> shared (rotated for quantized K) ----
     float* sQ = reinterpret_cast<float*>(smem + C::kQOff);
-    const int rbase = rg * C::kRows;
-    for (int r = warp; r < C::kRows; r += C::kWarps) {
-        const int rr = rbase + r;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (rr < p.rows) {
-            const int hl = rr / p.tq, j = rr - hl * p.tq;
-            const __half* qp =
-                p.q + ((static_cast<size_t>(b) * p.hq + h * p.group + hl) * p.tq + j) * kD + lane * 4;
-            const uint2 raw = *reinterpret_cast<const uint2*>(qp);
-            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-            v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
-            if constexpr (KB != 0) {
-                const uint32_t sn = sign_nibble(p.signs, lane);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) v[i] = ((sn >> i) & 1u) ? -v[i] : v[i];
-                wht128_lane4(v, lane);
-                const float inv = 0.08838834764831845f;  // 1/sqrt(128)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) v[i] *= inv;
-            }
-        }
-        *reinterpret_cast<float4*>(sQ + r * kD + lane * 4) = make_float4(v[0], v[1], v[2], v[3]);
-    }
-    __syncthreads();
-
-    // B fragments of the score MMA (k = head dims, n = query rows).  Quantized
-    // K: a thread's A operand is its tokens' quarter `t` in order, so logical
-    // k-index 16*kc + 2*t + e maps to dim 32*t + 4*kc + e (and +8 -> +2).
-    uint32_t qb[NT][8][2];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-        const float* qr = sQ + (8 * n + g) * kD;
-#pragma unroll
-        for (int kc = 0; kc < 8; ++kc) {
-            int d0, d1;
-            if constexpr (KB != 0) { d0 = 32 * t + 4 * kc; d1 = d0 + 2; }
-            else { d0 = 16 * kc + 2 * t; d1 = d0 + 8; }
-            qb[n][kc][0] = pack_half2(qr[d0], qr[d0 + 1]);
-            qb[n][kc][1] = pack_half2(qr[d1], qr[d1 + 1]);
-        }
-    }
-
     const Tables kt{p.ktab[0], p.ktab[1], p.ktab[2], p.ktab[3]};
     const Tables vt{p.vtab[0], p.vtab[1], p.vtab[2], p.vtab[3]};
-    // last visible token (inclusive) of the rows 8n + 2t + e this thread owns
-    int lim[NT][2];
-#pragma unroll
-    for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) lim[n][e] = L - p.tq + ((rbase + 8 * n + 2 * t + e) % p.tq);
-    const int all_visible_below = L - p.tq + 1;  // tokens below this are seen by every row
-    // rows of this thread that are real query rows (not padding of the group)
-    bool row_ok[NT][2];
-#pragma unroll
-    for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) row_ok[n][e] = rbase + 8 * n + 2 * t + e < p.rows;
     const bool sparse = p.sparse_tau > 0.f;
 
-    float O[NT][8][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) O[n][i][0] = O[n][i][1] = O[n][i][2] = O[n][i][3] = 0.f;
-    float m[NT][2], l[NT][2];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) m[n][0] = m[n][1] = -INFINITY, l[n][0] = l[n][1] = 0.f;
-    bool stalled = false;
-
-    // One 32-token chunk of this warp.  FULL: all 32 tokens valid and visible
-    // to every row (no masking); otherwise the tail / causal path.
-    auto process = [&](const uint8_t* st, const int tok0, auto full_tag) {
-        constexpr bool FULL = decltype(full_tag)::value;
-        const int nvalid = FULL ? C::kChunk : min(C::kChunk, t_end - tok0);
-        const bool two = FULL || nvalid > 16;
-            // ---------------- scores S^T = C_k . Rot(q)^T ----------------
-            float x[2][NT][4];
-    #pragma unroll
-            for (int tile = 0; tile < 2; ++tile) {
-    #pragma unroll
-                for (int n = 0; n < NT; ++n) x[tile][n][0] = x[tile][n][1] = x[tile][n][2] = x[tile][n][3] = 0.f;
-                if (!FULL && tile == 1 && !two) break;
-                if constexpr (KB == 0) {
-                    const int mi = lane >> 3;
-                    const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
-    #pragma unroll
-                    for (int kc = 0; kc < 8; ++kc) {
-                        const int db = 2 * kc + (mi >> 1);  // 16-byte chunk 0..15 of the row
-                        const uint32_t addr = smem_u32(st) + (db >> 3) * 4096 + row * 128 +
-                                              (((db & 7) ^ (row & 7)) << 4);
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x4(addr, a0, a1, a2, a3);
-    #pragma unroll
-                        for (int n = 0; n < NT; ++n) mma_f16(x[tile][n], a0, a1, a2, a3, qb[n][kc][0], qb[n][kc][1]);
-                    }
-                } else {
-                    // A quad of k-step kc: (token g, dims 2kc), (token g+8, 2kc),
-                    // (token g, 2kc+1), (token g+8, 2kc+1) in quarter-pair units
-                    uint32_t aq[8][4];
-                    dequant_quarter_q<KB, 0>(st + (tile * 16 + g) * C::kRbK + t * (C::kRbK / 4), kt, aq);
-                    dequant_quarter_q<KB, 1>(st + (tile * 16 + g + 8) * C::kRbK + t * (C::kRbK / 4), kt, aq);
-    #pragma unroll
-                    for (int kc = 0; kc < 8; ++kc)
-    #pragma unroll
-                        for (int n = 0; n < NT; ++n)
-                            mma_f16(x[tile][n], aq[kc][0], aq[kc][1], aq[kc][2], aq[kc][3],
-                                    qb[n][kc][0], qb[n][kc][1]);
-                }
-            }
-
-            // ---------------- online softmax (log2 domain) ----------------
-            // thread's tokens: tile*16 + g (c0, c1) and tile*16 + g + 8 (c2, c3);
-            // rows 8n + 2t (c0, c2) and 8n + 2t + 1 (c1, c3)
-            float nv[2][2];
-    #pragma unroll
-            for (int tile = 0; tile < 2; ++tile) {
-                const int ta = tile * 16 + g, tb = ta + 8;
-                float ka = p.scale_log2e, kb2 = p.scale_log2e;
-                if constexpr (KB != 0) {
-                    ka *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * ta));
-                    kb2 *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * tb));
-                }
-                nv[tile][0] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * ta));
-                nv[tile][1] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * tb));
-    #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    x[tile][n][0] *= ka; x[tile][n][1] *= ka;
-                    x[tile][n][2] *= kb2; x[tile][n][3] *= kb2;
-                }
-                if constexpr (!FULL) {
-                    const int ga = tok0 + ta, gb = tok0 + tb;
-                    const bool va = ga < t_end && (tile == 0 || two);
-                    const bool vb = gb < t_end && (tile == 0 || two);
-    #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        x[tile][n][0] = (va && ga <= lim[n][0]) ? x[tile][n][0] : -INFINITY;
-                        x[tile][n][1] = (va && ga <= lim[n][1]) ? x[tile][n][1] : -INFINITY;
-                        x[tile][n][2] = (vb && gb <= lim[n][0]) ? x[tile][n][2] : -INFINITY;
-                        x[tile][n][3] = (vb && gb <= lim[n][1]) ? x[tile][n][3] : -INFINITY;
-                    }
-                    if (!va) nv[tile][0] = 0.f;
-                    if (!vb) nv[tile][1] = 0.f;
-                }
-            }
-            // The exp2 base of a row stays at its running max until a score exceeds
-            // it by more than kSlack (log2 units); only then (warp-uniform slow
-            // path) is the true max taken and O, l rescaled.  So p <= 2^kSlack.
-            constexpr float kSlack = 4.f;
-            bool grow = false;
-    #pragma unroll
-            for (int n = 0; n < NT; ++n)
-    #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float lim_x = m[n][e] + kSlack;
-                    grow |= x[0][n][e] > lim_x || x[0][n][e + 2] > lim_x ||
-                            x[1][n][e] > lim_x || x[1][n][e + 2] > lim_x;
-                }
-            if (__any_sync(0xffffffffu, grow)) {
-    #pragma unroll
-                for (int n = 0; n < NT; ++n)
-    #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        float mx = fmaxf(fmaxf(x[0][n][e], x[0][n][e + 2]), fmaxf(x[1][n][e], x[1][n][e + 2]));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                        const float mn = fmaxf(m[n][e], mx);
-                        const float al = (m[n][e] == -INFINITY) ? 0.f : fast_exp2(m[n][e] - mn);
-                        m[n][e] = mn;
-                        l[n][e] *= al;
-    #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            O[n][i][e] *= al;
-                            O[n][i][e + 2] *= al;
-                        }
-                    }
-            }
-    #pragma unroll
-            for (int n = 0; n < NT; ++n)
-    #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float base = (m[n][e] == -INFINITY) ? 0.f : m[n][e];
-                    float s = 0.f;
-    #pragma unroll
-                    for (int tile = 0; tile < 2; ++tile) {
-                        x[tile][n][e] = fast_exp2(x[tile][n][e] - base);
-                        x[tile][n][e + 2] = fast_exp2(x[tile][n][e + 2] - base);
-                        s += x[tile][n][e] + x[tile][n][e + 2];
-                    }
-                    l[n][e] += s;
-                }
-
-            // Sparse V: a tile whose weights are all below tau for every real row
-            // skips its V dequant and P.V.  Here p = 2^(x - base) with base at
-            // most the running max, so p is never below the final normalised
-            // weight: only tokens the definition skips can be skipped.
-            bool keep[2] = {true, true};
-            if (sparse) {
-    #pragma unroll
-                for (int tile = 0; tile < 2; ++tile) {
-                    float mx = 0.f;
-    #pragma unroll
-                    for (int n = 0; n < NT; ++n)
-    #pragma unroll
-                        for (int e = 0; e < 2; ++e)
-                            if (row_ok[n][e]) mx = fmaxf(mx, fmaxf(x[tile][n][e], x[tile][n][e + 2]));
-                    keep[tile] = __any_sync(0xffffffffu, mx >= p.sparse_tau);
-                }
-            }
-
-            // ---------------- O^T += C_v^T . (P n_v)^T (rotated basis) ----------------
-    #pragma unroll
-            for (int tile = 0; tile < 2; ++tile) {
-                if (!FULL && tile == 1 && !two) break;
-                if (!keep[tile]) continue;
-                uint32_t pb0[NT], pb1[NT];
-    #pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    pb0[n] = movtrans(pack_half2(x[tile][n][0] * nv[tile][0], x[tile][n][1] * nv[tile][0]));
-                    pb1[n] = movtrans(pack_half2(x[tile][n][2] * nv[tile][1], x[tile][n][3] * nv[tile][1]));
-                }
-                // A quad of dim tile mt: transposed pairs 2mt, 2mt+1 of token block 0
-                // (tokens 0-7 of the tile) then of block 1 (tokens 8-15)
-                uint32_t vq[8][4];
-                {
-                    uint32_t hv[16];
-                    dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g) * C::kRbV + t * (C::kRbV / 4), vt, hv);
-    #pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        vq[mt][0] = movtrans(hv[2 * mt]);
-                        vq[mt][1] = movtrans(hv[2 * mt + 1]);
-                    }
-                }
-                {
-                    uint32_t hv[16];
-                    dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g + 8) * C::kRbV + t * (C::kRbV / 4), vt, hv);
-    #pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        vq[mt][2] = movtrans(hv[2 * mt]);
-                        vq[mt][3] = movtrans(hv[2 * mt + 1]);
-                    }
-                }
-    #pragma unroll
-                for (int mt = 0; mt < 8; ++mt)
-    #pragma unroll
-                    for (int n = 0; n < NT; ++n)
-                        mma_f16(O[n][mt], vq[mt][0], vq[mt][1], vq[mt][2], vq[mt][3], pb0[n], pb1[n]);
-            }
-
-    };
-
+    // the copy ring continues across segments: every copy issued in a segment
+    // is consumed in it, so (stage, phase) carry over
     int stage = 0;
     uint32_t phase = 0;
-    int c = warp;
-    for (; c < nchunks; c += C::kWarps) {
-        const bool ok = mbar_wait_bounded(bar0 + 8 * stage, phase);
-        if (__any_sync(0xffffffffu, !ok)) { stalled = true; break; }
-        const uint8_t* st = wpipe + stage * C::kStage;
-        const int tok0 = t_begin + c * C::kChunk;
-        if (tok0 + C::kChunk <= t_end && tok0 + C::kChunk <= all_visible_below)
-            process(st, tok0, std::true_type{});
-        else
-            process(st, tok0, std::false_type{});
-        __syncwarp();
-        const int cn = c + C::kWarps * C::kStages;
-        if (cn < nchunks && lane == 0) {
-            fence_proxy_async();
-            issue(cn, stage);
-        }
-        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-    }
+    int pos = lo;
+    while (pos < hi) {
+        int b, before, L, nch;
+        scan.locate(p.lengths, p.batch, per_b, p.max_len, pos, lane, b, before, L, nch);
+        b = __shfl_sync(0xffffffffu, b, 0);
+        before = __shfl_sync(0xffffffffu, before, 0);
+        L = __shfl_sync(0xffffffffu, L, 0);
+        nch = __shfl_sync(0xffffffffu, nch, 0);
+        const int local = pos - before;
+        const int ui = local / nch;  // h * row_groups + rg
+        const int k0 = local - ui * nch;
+        const int k1 = min(nch, k0 + (hi - pos));
+        const int h = ui / p.row_groups, rg = ui - h * p.row_groups;
+        const int unit = b * per_b + ui;  // global unit index, row group included
+        const int t_lim = min(L, p.max_len);
+        const int t_begin = k0 * C::kChunk;
+        const int t_end = min(k1 * C::kChunk, t_lim);
+        const int nchunks = k1 - k0;
+        const size_t row0 = static_cast<size_t>(b * p.hkv + h) * p.cap;
 
-    if (stalled) {
-        // Drain this warp's copies still in flight (bounded), flag, and stop.
-        for (int k = 0; k < C::kStages; ++k) {
-            if (c + C::kWarps * k >= nchunks) break;
-            (void)mbar_wait_bounded(bar0 + 8 * stage, phase);
+        auto issue = [&](int c, int st_idx) {  // lane 0 only
+            const int tok0 = t_begin + c * C::kChunk;
+            const int nval = min(C::kChunk, t_end - tok0);
+            const uint32_t dst = smem_u32(wpipe + st_idx * C::kStage);
+            const uint32_t bar = bar0 + st_idx * 8;
+            const uint32_t nb = static_cast<uint32_t>((nval + 7) & ~7) * 2;  // norms, 16-B multiple
+            uint32_t bytes = nval * C::kRbV + nb;
+            if (KB == 0) bytes += 2 * 4096;
+            else bytes += nval * C::kRbK + nb;
+            mbar_arrive_expect_tx(bar, bytes);
+            if constexpr (KB == 0) {
+                tma_g2s_2d(dst, &kmap, 0, static_cast<int32_t>(row0 + tok0), bar);
+                tma_g2s_2d(dst + 4096, &kmap, 64, static_cast<int32_t>(row0 + tok0), bar);
+            } else {
+                bulk_g2s(dst, p.k_codes + (row0 + tok0) * C::kRbK, nval * C::kRbK, bar);
+                bulk_g2s(dst + C::kKnOff, p.k_norm + row0 + tok0, nb, bar);
+            }
+            bulk_g2s(dst + C::kVOff, p.v_codes + (row0 + tok0) * C::kRbV, nval * C::kRbV, bar);
+            bulk_g2s(dst + C::kVnOff, p.v_norm + row0 + tok0, nb, bar);
+        };
+
+        if (lane == 0) {
+            for (int s = 0; s < C::kStages; ++s) {
+                const int c = warp + C::kWarps * s;
+                int si = stage + s;
+                if (si >= C::kStages) si -= C::kStages;
+                if (c < nchunks) issue(c, si);
+            }
+        }
+        __syncwarp();
+
+        // ---- query rows of this row group -> shared (rotated for quantized K) ----
+        const int rbase = rg * C::kRows;
+        for (int r = warp; r < C::kRows; r += C::kWarps) {
+            const int rr = rbase + r;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (rr < p.rows) {
+                const int hl = rr / p.tq, j = rr - hl * p.tq;
+                const __half* qp =
+                    p.q + ((static_cast<size_t>(b) * p.hq + h * p.group + hl) * p.tq + j) * kD + lane * 4;
+                const uint2 raw = *reinterpret_cast<const uint2*>(qp);
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+                v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+                if constexpr (KB != 0) {
+                    const uint32_t sn = sign_nibble(p.signs, lane);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = ((sn >> i) & 1u) ? -v[i] : v[i];
+                    wht128_lane4(v, lane);
+                    const float inv = 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] *= inv;
+                }
+            }
+            *reinterpret_cast<float4*>(sQ + r * kD + lane * 4) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+        __syncthreads();
+
+        // B fragments of the score MMA (k = head dims, n = query rows).  Quantized
+        // K: a thread's A operand is its tokens' quarter `t` in order, so logical
+        // k-index 16*kc + 2*t + e maps to dim 32*t + 4*kc + e (and +8 -> +2).
+        uint32_t qb[NT][8][2];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const float* qr = sQ + (8 * n + g) * kD;
+#pragma unroll
+            for (int kc = 0; kc < 8; ++kc) {
+                int d0, d1;
+                if constexpr (KB != 0) { d0 = 32 * t + 4 * kc; d1 = d0 + 2; }
+                else { d0 = 16 * kc + 2 * t; d1 = d0 + 8; }
+                qb[n][kc][0] = pack_half2(qr[d0], qr[d0 + 1]);
+                qb[n][kc][1] = pack_half2(qr[d1], qr[d1 + 1]);
+            }
+        }
+
+        // last visible token (inclusive) of the rows 8n + 2t + e this thread owns
+        int lim[NT][2];
+        bool row_ok[NT][2];  // real query rows (not padding of the group)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                lim[n][e] = L - p.tq + ((rbase + 8 * n + 2 * t + e) % p.tq);
+                row_ok[n][e] = rbase + 8 * n + 2 * t + e < p.rows;
+            }
+        const int all_visible_below = L - p.tq + 1;  // tokens below this are seen by every row
+
+        float O[NT][8][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) O[n][i][0] = O[n][i][1] = O[n][i][2] = O[n][i][3] = 0.f;
+        float m[NT][2], l[NT][2];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) m[n][0] = m[n][1] = -INFINITY, l[n][0] = l[n][1] = 0.f;
+        bool stalled = false;
+
+        // One 32-token chunk of this warp.  FULL: all 32 tokens valid and visible
+        // to every row (no masking); otherwise the tail / causal path.
+        auto process = [&](const uint8_t* st, const int tok0, auto full_tag) {
+            constexpr bool FULL = decltype(full_tag)::value;
+            const int nvalid = FULL ? C::kChunk : min(C::kChunk, t_end - tok0);
+            const bool two = FULL || nvalid > 16;
+                // ---------------- scores S^T = C_k . Rot(q)^T ----------------
+                float x[2][NT][4];
+        #pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+        #pragma unroll
+                    for (int n = 0; n < NT; ++n) x[tile][n][0] = x[tile][n][1] = x[tile][n][2] = x[tile][n][3] = 0.f;
+                    if (!FULL && tile == 1 && !two) break;
+                    if constexpr (KB == 0) {
+                        const int mi = lane >> 3;
+                        const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
+        #pragma unroll
+                        for (int kc = 0; kc < 8; ++kc) {
+                            const int db = 2 * kc + (mi >> 1);  // 16-byte chunk 0..15 of the row
+                            const uint32_t addr = smem_u32(st) + (db >> 3) * 4096 + row * 128 +
+                                                  (((db & 7) ^ (row & 7)) << 4);
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4(addr, a0, a1, a2, a3);
+        #pragma unroll
+                            for (int n = 0; n < NT; ++n) mma_f16(x[tile][n], a0, a1, a2, a3, qb[n][kc][0], qb[n][kc][1]);
+                        }
+                    } else {
+                        // A quad of k-step kc: (token g, dims 2kc), (token g+8, 2kc),
+                        // (token g, 2kc+1), (token g+8, 2kc+1) in quarter-pair units
+                        uint32_t aq[8][4];
+                        dequant_quarter_q<KB, 0>(st + (tile * 16 + g) * C::kRbK + t * (C::kRbK / 4), kt, aq);
+                        dequant_quarter_q<KB, 1>(st + (tile * 16 + g + 8) * C::kRbK + t * (C::kRbK / 4), kt, aq);
+        #pragma unroll
+                        for (int kc = 0; kc < 8; ++kc)
+        #pragma unroll
+                            for (int n = 0; n < NT; ++n)
+                                mma_f16(x[tile][n], aq[kc][0], aq[kc][1], aq[kc][2], aq[kc][3],
+                                        qb[n][kc][0], qb[n][kc][1]);
+                    }
+                }
+
+                // ---------------- online softmax (log2 domain) ----------------
+                // thread's tokens: tile*16 + g (c0, c1) and tile*16 + g + 8 (c2, c3);
+                // rows 8n + 2t (c0, c2) and 8n + 2t + 1 (c1, c3)
+                float nv[2][2];
+        #pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+                    const int ta = tile * 16 + g, tb = ta + 8;
+                    float ka = p.scale_log2e, kb2 = p.scale_log2e;
+                    if constexpr (KB != 0) {
+                        ka *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * ta));
+                        kb2 *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * tb));
+                    }
+                    nv[tile][0] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * ta));
+                    nv[tile][1] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * tb));
+        #pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        x[tile][n][0] *= ka; x[tile][n][1] *= ka;
+                        x[tile][n][2] *= kb2; x[tile][n][3] *= kb2;
+                    }
+                    if constexpr (!FULL) {
+                        const int ga = tok0 + ta, gb = tok0 + tb;
+                        const bool va = ga < t_end && (tile == 0 || two);
+                        const bool vb = gb < t_end && (tile == 0 || two);
+        #pragma unroll
+                        for (int n = 0; n < NT; ++n) {
+                            x[tile][n][0] = (va && ga <= lim[n][0]) ? x[tile][n][0] : -INFINITY;
+                            x[tile][n][1] = (va && ga <= lim[n][1]) ? x[tile][n][1] : -INFINITY;
+                            x[tile][n][2] = (vb && gb <= lim[n][0]) ? x[tile][n][2] : -INFINITY;
+                            x[tile][n][3] = (vb && gb <= lim[n][1]) ? x[tile][n][3] : -INFINITY;
+                        }
+                        if (!va) nv[tile][0] = 0.f;
+                        if (!vb) nv[tile][1] = 0.f;
+                    }
+                }
+                // The exp2 base of a row stays at its running max until a score exceeds
+                // it by more than kSlack (log2 units); only then (warp-uniform slow
+                // path) is the true max taken and O, l rescaled.  So p <= 2^kSlack.
+                constexpr float kSlack = 4.f;
+                bool grow = false;
+        #pragma unroll
+                for (int n = 0; n < NT; ++n)
+        #pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float lim_x = m[n][e] + kSlack;
+                        grow |= x[0][n][e] > lim_x || x[0][n][e + 2] > lim_x ||
+                                x[1][n][e] > lim_x || x[1][n][e + 2] > lim_x;
+                    }
+                if (__any_sync(0xffffffffu, grow)) {
+        #pragma unroll
+                    for (int n = 0; n < NT; ++n)
+        #pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            float mx = fmaxf(fmaxf(x[0][n][e], x[0][n][e + 2]), fmaxf(x[1][n][e], x[1][n][e + 2]));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                            const float mn = fmaxf(m[n][e], mx);
+                            const float al = (m[n][e] == -INFINITY) ? 0.f : fast_exp2(m[n][e] - mn);
+                            m[n][e] = mn;
+                            l[n][e] *= al;
+        #pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                O[n][i][e] *= al;
+                                O[n][i][e + 2] *= al;
+                            }
+                        }
+                }
+        #pragma unroll
+                for (int n = 0; n < NT; ++n)
+        #pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float base = (m[n][e] == -INFINITY) ? 0.f : m[n][e];
+                        float s = 0.f;
+        #pragma unroll
+                        for (int tile = 0; tile < 2; ++tile) {
+                            x[tile][n][e] = fast_exp2(x[tile][n][e] - base);
+                            x[tile][n][e + 2] = fast_exp2(x[tile][n][e + 2] - base);
+                            s += x[tile][n][e] + x[tile][n][e + 2];
+                        }
+                        l[n][e] += s;
+                    }
+
+                // Sparse V: a tile whose weights are all below tau for every real row
+                // skips its V dequant and P.V.  Here p = 2^(x - base) with base at
+                // most the running max, so p is never below the final normalised
+                // weight: only tokens the definition skips can be skipped.
+                bool keep[2] = {true, true};
+                if (sparse) {
+        #pragma unroll
+                    for (int tile = 0; tile < 2; ++tile) {
+                        float mx = 0.f;
+        #pragma unroll
+                        for (int n = 0; n < NT; ++n)
+        #pragma unroll
+                            for (int e = 0; e < 2; ++e)
+                                if (row_ok[n][e]) mx = fmaxf(mx, fmaxf(x[tile][n][e], x[tile][n][e + 2]));
+                        keep[tile] = __any_sync(0xffffffffu, mx >= p.sparse_tau);
+                    }
+                }
+
+                // ---------------- O^T += C_v^T . (P n_v)^T (rotated basis) ----------------
+        #pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+                    if (!FULL && tile == 1 && !two) break;
+                    if (!keep[tile]) continue;
+                    uint32_t pb0[NT], pb1[NT];
+        #pragma unroll
+                    for (int n = 0; n < NT; ++n) {
+                        pb0[n] = movtrans(pack_half2(x[tile][n][0] * nv[tile][0], x[tile][n][1] * nv[tile][0]));
+                        pb1[n] = movtrans(pack_half2(x[tile][n][2] * nv[tile][1], x[tile][n][3] * nv[tile][1]));
+                    }
+                    // A quad of dim tile mt: transposed pairs 2mt, 2mt+1 of token block 0
+                    // (tokens 0-7 of the tile) then of block 1 (tokens 8-15)
+                    uint32_t vq[8][4];
+                    {
+                        uint32_t hv[16];
+                        dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g) * C::kRbV + t * (C::kRbV / 4), vt, hv);
+        #pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            vq[mt][0] = movtrans(hv[2 * mt]);
+                            vq[mt][1] = movtrans(hv[2 * mt + 1]);
+                        }
+                    }
+                    {
+                        uint32_t hv[16];
+                        dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g + 8) * C::kRbV + t * (C::kRbV / 4), vt, hv);
+        #pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            vq[mt][2] = movtrans(hv[2 * mt]);
+                            vq[mt][3] = movtrans(hv[2 * mt + 1]);
+                        }
+                    }
+        #pragma unroll
+                    for (int mt = 0; mt < 8; ++mt)
+        #pragma unroll
+                        for (int n = 0; n < NT; ++n)
+                            mma_f16(O[n][mt], vq[mt][0], vq[mt][1], vq[mt][2], vq[mt][3], pb0[n], pb1[n]);
+                }
+
+        };
+
+        int c = warp;
+        for (; c < nchunks; c += C::kWarps) {
+            const bool ok = mbar_wait_bounded(bar0 + 8 * stage, phase);
+            if (__any_sync(0xffffffffu, !ok)) { stalled = true; break; }
+            const uint8_t* st = wpipe + stage * C::kStage;
+            const int tok0 = t_begin + c * C::kChunk;
+            if (tok0 + C::kChunk <= t_end && tok0 + C::kChunk <= all_visible_below)
+                process(st, tok0, std::true_type{});
+            else
+                process(st, tok0, std::false_type{});
+            __syncwarp();
+            const int cn = c + C::kWarps * C::kStages;
+            if (cn < nchunks && lane == 0) {
+                fence_proxy_async();
+                issue(cn, stage);
+            }
             if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
-        if (lane == 0) atomicOr(p.status, kStatusPipelineStall);
-    }
 
-    // ---- combine the 4 warps of the CTA, write this split's partial ----
-#pragma unroll
-    for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            l[n][e] += __shfl_xor_sync(0xffffffffu, l[n][e], 4);
-            l[n][e] += __shfl_xor_sync(0xffffffffu, l[n][e], 8);
-            l[n][e] += __shfl_xor_sync(0xffffffffu, l[n][e], 16);
-        }
-    __syncthreads();  // every warp is done with its pipeline stages
-    float* sO = reinterpret_cast<float*>(smem) + warp * C::kRows * C::kOStride;
-    float* sML = reinterpret_cast<float*>(smem) + C::kWarps * C::kRows * C::kOStride;
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-        const int r0 = 8 * n + 2 * t;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const int dlo = 32 * (g >> 1) + 4 * mt + (g & 1);
-            sO[r0 * C::kOStride + dlo] = O[n][mt][0];
-            sO[(r0 + 1) * C::kOStride + dlo] = O[n][mt][1];
-            sO[r0 * C::kOStride + dlo + 2] = O[n][mt][2];
-            sO[(r0 + 1) * C::kOStride + dlo + 2] = O[n][mt][3];
-        }
-        if (g == 0) {
-            sML[(warp * C::kRows + r0) * 2 + 0] = m[n][0];
-            sML[(warp * C::kRows + r0) * 2 + 1] = l[n][0];
-            sML[(warp * C::kRows + r0 + 1) * 2 + 0] = m[n][1];
-            sML[(warp * C::kRows + r0 + 1) * 2 + 1] = l[n][1];
-        }
-    }
-    __syncthreads();
-    {
-        constexpr int kPerRow = 128 / C::kRows;      // threads per row
-        constexpr int kDims = kD / kPerRow;          // dims per thread
-        const int r = threadIdx.x / kPerRow;
-        const int d0 = (threadIdx.x % kPerRow) * kDims;
-        if (rbase + r < p.rows) {
-            float mw[C::kWarps], M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < C::kWarps; ++w) {
-                mw[w] = sML[(w * C::kRows + r) * 2];
-                M = fmaxf(M, mw[w]);
+        if (stalled) {
+            // Drain this warp's copies still in flight (bounded), flag, and stop.
+            for (int k = 0; k < C::kStages; ++k) {
+                if (c + C::kWarps * k >= nchunks) break;
+                (void)mbar_wait_bounded(bar0 + 8 * stage, phase);
+                if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
             }
-            float sc[C::kWarps], lsum = 0.f;
-#pragma unroll
-            for (int w = 0; w < C::kWarps; ++w) {
-                sc[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
-                lsum += sc[w] * sML[(w * C::kRows + r) * 2 + 1];
+            if (lane == 0) atomicOr(p.status, kStatusPipelineStall);
+        }
+
+        // ---- combine the 4 warps of the CTA, write this segment's partial ----
+    #pragma unroll
+        for (int n = 0; n < NT; ++n)
+    #pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                l[n][e] += __shfl_xor_sync(0xffffffffu, l[n][e], 4);
+                l[n][e] += __shfl_xor_sync(0xffffffffu, l[n][e], 8);
+                l[n][e] += __shfl_xor_sync(0xffffffffu, l[n][e], 16);
             }
-            const size_t pidx =
-                ((static_cast<size_t>(unit) * p.row_groups + rg) * p.nsplit + split) * 16 + r;
-            float* po = p.part_o + pidx * kD + d0;
-#pragma unroll
-            for (int d = 0; d < kDims; d += 4) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
+        __syncthreads();  // every warp is done with its pipeline stages
+        float* sO = reinterpret_cast<float*>(smem) + warp * C::kRows * C::kOStride;
+        float* sML = reinterpret_cast<float*>(smem) + C::kWarps * C::kRows * C::kOStride;
+    #pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int r0 = 8 * n + 2 * t;
+    #pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const int dlo = 32 * (g >> 1) + 4 * mt + (g & 1);
+                sO[r0 * C::kOStride + dlo] = O[n][mt][0];
+                sO[(r0 + 1) * C::kOStride + dlo] = O[n][mt][1];
+                sO[r0 * C::kOStride + dlo + 2] = O[n][mt][2];
+                sO[(r0 + 1) * C::kOStride + dlo + 2] = O[n][mt][3];
+            }
+            if (g == 0) {
+                sML[(warp * C::kRows + r0) * 2 + 0] = m[n][0];
+                sML[(warp * C::kRows + r0) * 2 + 1] = l[n][0];
+                sML[(warp * C::kRows + r0 + 1) * 2 + 0] = m[n][1];
+                sML[(warp * C::kRows + r0 + 1) * 2 + 1] = l[n][1];
+            }
+        }
+        __syncthreads();
+        {
+            constexpr int kPerRow = 128 / C::kRows;      // threads per row
+            constexpr int kDims = kD / kPerRow;          // dims per thread
+            const int r = threadIdx.x / kPerRow;
+            const int d0 = (threadIdx.x % kPerRow) * kDims;
+            if (rbase + r < p.rows) {
+                float mw[C::kWarps], M = -INFINITY;
+    #pragma unroll
                 for (int w = 0; w < C::kWarps; ++w) {
-                    const float* src = reinterpret_cast<float*>(smem) + (w * C::kRows + r) * C::kOStride + d0 + d;
-                    acc.x += sc[w] * src[0];
-                    acc.y += sc[w] * src[1];
-                    acc.z += sc[w] * src[2];
-                    acc.w += sc[w] * src[3];
+                    mw[w] = sML[(w * C::kRows + r) * 2];
+                    M = fmaxf(M, mw[w]);
                 }
-                *reinterpret_cast<float4*>(po + d) = acc;
-            }
-            if ((threadIdx.x % kPerRow) == 0) {
-                p.part_ml[pidx * 2 + 0] = M;
-                p.part_ml[pidx * 2 + 1] = lsum;
+                float sc[C::kWarps], lsum = 0.f;
+    #pragma unroll
+                for (int w = 0; w < C::kWarps; ++w) {
+                    sc[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
+                    lsum += sc[w] * sML[(w * C::kRows + r) * 2 + 1];
+                }
+                const size_t pidx = (static_cast<size_t>(blockIdx.x) + unit) * 16 + r;
+                float* po = p.part_o + pidx * kD + d0;
+    #pragma unroll
+                for (int d = 0; d < kDims; d += 4) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    #pragma unroll
+                    for (int w = 0; w < C::kWarps; ++w) {
+                        const float* src = reinterpret_cast<float*>(smem) + (w * C::kRows + r) * C::kOStride + d0 + d;
+                        acc.x += sc[w] * src[0];
+                        acc.y += sc[w] * src[1];
+                        acc.z += sc[w] * src[2];
+                        acc.w += sc[w] * src[3];
+                    }
+                    *reinterpret_cast<float4*>(po + d) = acc;
+                }
+                if ((threadIdx.x % kPerRow) == 0) {
+                    p.part_ml[pidx * 2 + 0] = M;
+                    p.part_ml[pidx * 2 + 1] = lsum;
+                }
             }
         }
+
+        // the next segment reuses the pipeline area the epilogue just read
+        if (__syncthreads_or(stalled)) break;
+        pos += nchunks;
     }
 }
 
-// One warp per output row (b, q head, query j): merge the split partials with
-// their log-sum-exp weights, apply v_rescale, leave the rotated basis
-// (Rot^-1(y) = s * (H y) / sqrt(128)) and store fp16.
+
+// One warp per output row (b, q head, query j): merge the partials of the
+// CTAs that covered the row's unit with their log-sum-exp weights, apply
+// v_rescale, leave the rotated basis (Rot^-1(y) = s * (H y) / sqrt(128)) and
+// store fp16.
 __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__ CombineParams p) {
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -514,17 +645,45 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
     const int kv = hq / p.group, hl = hq - kv * p.group;
     const int r = hl * p.tq + j;
     const int rg = r / p.group_rows, rl = r - rg * p.group_rows;
-    const int unit = b * p.hkv + kv;
-    const int L = min(p.lengths[b], p.max_len);
-    const int ns = min(p.nsplit, (L + p.split_tokens - 1) / p.split_tokens);
-    const size_t base = (static_cast<size_t>(unit) * p.row_groups + rg) * p.nsplit * 16 + rl;
+    const int per_b = p.hkv * p.row_groups;
+    const int ui = kv * p.row_groups + rg;
+    const int unit = b * per_b + ui;
 
+    // the unit's global chunk range [k_first, k_first + nch) and the CTAs over it
+    long long before = 0, all = 0;
+    for (int bb = lane; bb < p.batch; bb += 32) {
+        const long long v = 1ll * unit_chunks(p.lengths, bb, p.max_len) * per_b;
+        all += v;
+        if (bb < b) before += v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+        all += __shfl_xor_sync(0xffffffffu, all, o);
+    }
+    const int nch = unit_chunks(p.lengths, b, p.max_len);
+    const long long P = p.num_ctas;
+    int c0 = 0, c1 = -1;
+    if (nch > 0) {
+        const long long k_first = before + static_cast<long long>(ui) * nch;
+        const long long k_last = k_first + nch - 1;
+        c0 = static_cast<int>(((k_first + 1) * P - 1) / all);  // the CTA holding chunk k
+        c1 = static_cast<int>(((k_last + 1) * P - 1) / all);
+    }
+
+    // with at least one chunk per CTA every CTA in [c0, c1] wrote a partial;
+    // otherwise skip the CTAs whose share is empty
+    const bool some_empty = all < P;
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, p.part_ml[(base + s * 16) * 2]);
+    for (int c = c0; c <= c1; ++c) {
+        if (some_empty && c * all / P == (c + 1) * all / P) continue;
+        M = fmaxf(M, p.part_ml[((static_cast<size_t>(c) + unit) * 16 + rl) * 2]);
+    }
     float den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < ns; ++s) {
-        const size_t pi = base + s * 16;
+    for (int c = c0; c <= c1; ++c) {
+        if (some_empty && c * all / P == (c + 1) * all / P) continue;
+        const size_t pi = (static_cast<size_t>(c) + unit) * 16 + rl;
         const float m = p.part_ml[pi * 2];
         const float w = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
         den += w * p.part_ml[pi * 2 + 1];
@@ -557,7 +716,7 @@ static int launch_decode_t(const DecodeParams& p, const CUtensorMap* kmap, cudaS
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid(p.nsplit, p.batch * p.hkv, p.row_groups);
+    dim3 grid(p.num_ctas);
     if (ev0) cudaEventRecord(ev0, stream);
     tq_decode_kernel<KB, VB, NT><<<grid, C::kWarps * 32, C::kSmemAlloc, stream>>>(p, *kmap);
     cudaError_t e = cudaGetLastError();

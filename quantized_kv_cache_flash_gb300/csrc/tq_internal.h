@@ -21,11 +21,11 @@ struct DecodeParams {
     const __half* v_norm;     // fp16 V norms
     const int32_t* lengths;   // [B]
     const __half* q;          // [B, Hq, Tq, 128]
-    float* part_o;            // [units, row_groups, nsplit, 16, 128]
-    float* part_ml;           // [units, row_groups, nsplit, 16, 2]  (running max in log2 units, sum)
+    float* part_o;            // [num_ctas + units, 16, 128], units = batch * hkv * row_groups
+    float* part_ml;           // [num_ctas + units, 16, 2]  (running max in log2 units, sum)
     uint32_t* status;
     int32_t batch, hkv, hq, group, tq, rows, row_groups, group_rows, cap, max_len;
-    int32_t split_tokens, nsplit;
+    int32_t num_ctas;         // decode grid (one wave of token-balanced CTAs)
     float scale_log2e;        // softmax scale * log2(e)
     float sparse_tau;         // sparse-V threshold on the softmax weight (0: off)
     uint32_t ktab[4];         // prmt byte tables of the K codebook (lo0, lo1, hi0, hi1)
@@ -39,7 +39,7 @@ struct CombineParams {
     const int32_t* lengths;
     __half* out;              // [B, Hq, Tq, 128]
     uint32_t* status;
-    int32_t batch, hkv, hq, group, tq, row_groups, group_rows, max_len, split_tokens, nsplit;
+    int32_t batch, hkv, hq, group, tq, row_groups, group_rows, max_len, num_ctas;
     float v_rescale;
     uint32_t signs[4];
 };

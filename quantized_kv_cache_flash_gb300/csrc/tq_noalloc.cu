@@ -144,21 +144,16 @@ extern "C" int tq_decode_attention_noalloc(const tq_cache* c, const void* q, int
     const int group_rows = tq::group_rows_for(rows);
     const int row_groups = (rows + group_rows - 1) / group_rows;
 
-    // split plan, limited to what the fixed scratch holds
-    int split_tokens = 0, nsplit = 0;
-    r = tq_plan_splits(c->mode, c->batch, c->num_kv_heads, rows, max_len_hint, &split_tokens, &nsplit);
+    // decode grid, limited to what the fixed scratch holds (one slot per CTA
+    // and per unit)
+    int tokens_per_cta = 0, ctas = 0;
+    r = tq_plan_splits(c->mode, c->batch, c->num_kv_heads, rows, max_len_hint, &tokens_per_cta, &ctas);
     if (r != TQ_OK) return r;
     const size_t slot_bytes = size_t(16) * (kD + 2) * sizeof(float);
     const size_t units = size_t(c->batch) * c->num_kv_heads * row_groups;
     const size_t max_slots = (size_t(TQ_NOALLOC_SCRATCH_BYTES) - kStatusBytes) / slot_bytes;
-    if (units > max_slots) return TQ_ERR_CAPACITY;   // does not fit the fixed scratch
-    if (units * size_t(nsplit) > max_slots) {
-        nsplit = int(max_slots / units);
-        long long st = (max_len_hint + nsplit - 1) / nsplit;
-        st = ((st + 31) / 32) * 32;
-        split_tokens = int(st);
-        nsplit = int((max_len_hint + st - 1) / st);
-    }
+    if (units >= max_slots) return TQ_ERR_CAPACITY;   // does not fit the fixed scratch
+    if (units + size_t(ctas) > max_slots) ctas = int(max_slots - units);
 
     void* base = nullptr;
     if ((r = scratch_address(&base)) != TQ_OK) return r;
@@ -169,7 +164,7 @@ extern "C" int tq_decode_attention_noalloc(const tq_cache* c, const void* q, int
         if (cudaMemsetAsync(st_word, 0, sizeof(uint32_t), s) != cudaSuccess) return TQ_ERR_CUDA;
     }
     float* part = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kStatusBytes);
-    const size_t slots = units * nsplit * 16;
+    const size_t slots = (units + size_t(ctas)) * 16;
 
     tq::DecodeParams p{};
     p.k_codes = static_cast<const uint8_t*>(c->k_data);
@@ -191,8 +186,7 @@ extern "C" int tq_decode_attention_noalloc(const tq_cache* c, const void* q, int
     p.group_rows = group_rows;
     p.cap = c->capacity;
     p.max_len = max_len_hint;
-    p.split_tokens = split_tokens;
-    p.nsplit = nsplit;
+    p.num_ctas = ctas;
     p.scale_log2e = ((scale == 0.f) ? 1.0f / std::sqrt(float(kD)) : scale) * 1.4426950408889634f;
     if (kb != 16) tables(c->codebook_k, kb, p.ktab);
     tables(c->codebook_v, vb, p.vtab);
@@ -234,8 +228,7 @@ extern "C" int tq_decode_attention_noalloc(const tq_cache* c, const void* q, int
     cp.row_groups = row_groups;
     cp.group_rows = group_rows;
     cp.max_len = max_len_hint;
-    cp.split_tokens = split_tokens;
-    cp.nsplit = nsplit;
+    cp.num_ctas = ctas;
     cp.v_rescale = c->v_rescale;
     std::memcpy(cp.signs, p.signs, sizeof(cp.signs));
     return tq::launch_combine(cp, s) == 0 ? TQ_OK : TQ_ERR_CUDA;

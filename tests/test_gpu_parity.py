@@ -64,6 +64,7 @@ DECODE_CASES = [
     ("turbo4k_3v", 1, 4, 1, [1], 1, 16, 0.0, 1.0),              # 4-bit K + 3-bit V, context 1
     ("turbo4k_3v", 3, 12, 4, [100, 513, 4000], 1, 4000, 0.0, 1.0),
     ("turbo4k_3v", 1, 32, 2, [777], 4, 784, 0.05, 1.0),         # 64 rows, custom scale
+    ("turbo4", 40, 8, 2, [(37 * i) % 290 + 1 for i in range(40)], 1, 304, 0.0, 1.0),  # > 32 sequences
 ]
 
 
@@ -95,6 +96,22 @@ def test_decode_short_context_rows_are_zero_and_flagged():
     units = {(0, 0): H.oracle_unit_from_records(mode, kd, kn, vd, vn, 0, 0, 2)}
     want = H.oracle_decode(mode, q, units, [2], Hkv, 4, 1 / math.sqrt(128), 1.0)
     H.assert_attention_close(got[:, :, 2:], want[:, :, 2:])
+
+
+def test_decode_empty_sequences_in_a_large_batch():
+    # 45 sequences, some of length 0: their rows are 0 and flagged, the rest exact
+    mode, B, Hq, Hkv, cap = "turbo3", 45, 4, 1, 96
+    lengths = [0 if i % 7 == 3 else (11 * i) % 96 + 1 for i in range(B)]
+    kd, kn, vd, vn = H.random_cache(mode, B, Hkv, cap, 123)
+    q = wl.random_fp16(124, (B, Hq, 1, 128))
+    cache = H.gpu_cache_from_records(mode, B, Hkv, cap, lengths, kd, kn, vd, vn, DEV)
+    got, status, _ = _run_decode(cache, q, 1, cap)
+    assert status & tqf.TQ_STATUS_SHORT_CONTEXT
+    live = [b for b in range(B) if lengths[b] > 0]
+    assert np.all(got[[b for b in range(B) if lengths[b] == 0]] == 0)
+    units = {(b, 0): H.oracle_unit_from_records(mode, kd, kn, vd, vn, b, 0, lengths[b]) for b in live}
+    want = H.oracle_decode(mode, q, units, lengths, Hkv, 1, 1 / math.sqrt(128), 1.0)
+    H.assert_attention_close(got[live], want[live])
 
 
 def test_decode_lengths_beyond_hint_are_clamped():

@@ -55,10 +55,15 @@ def test_record_bytes(lib):
 @pytest.mark.parametrize("B,Hkv,rows,L", [(1, 2, 2, 256), (1, 4, 7, 8192), (1, 4, 7, 16384),
                                           (32, 8, 4, 32768), (4, 8, 16, 131072), (2, 2, 64, 777),
                                           (1, 1, 1, 1)])
-def test_split_plan_covers_context(lib, mode, B, Hkv, rows, L):
-    st, ns = tqf.tq_plan_splits(mode, B, Hkv, rows, L)
-    assert st % 32 == 0 and st >= 256
-    assert ns * st >= L and (ns - 1) * st < L
+def test_decode_grid_covers_context(lib, mode, B, Hkv, rows, L):
+    st, ctas = tqf.tq_plan_splits(mode, B, Hkv, rows, L)
+    units = B * Hkv * -(-rows // (8 if rows <= 8 else 16))
+    chunks = units * -(-L // 32)
+    assert 1 <= ctas <= 2 * 152 * 4                   # two waves at most
+    assert st % 32 == 0 and ctas * st >= chunks * 32  # the CTAs cover every chunk
+    assert st == -(-chunks // ctas) * 32              # the largest share, in tokens
+    assert chunks >= ctas                             # every CTA has work
+    assert ctas == 1 or st >= 8 * 32                  # at least two chunks per warp
 
 
 def test_decode_records_helper_reads_the_format():

@@ -63,7 +63,7 @@ def test_noalloc_matches_regular_decode_on_two_calls(dev, case):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(dev):
-    # 64 x 32 (batch x kv heads) split slots of 8320 bytes exceed the 16 MiB array
+    # 64 x 32 (batch x kv heads) unit slots of 8320 bytes exceed the 16 MiB array
     cache = tqf.Cache(tqf.TQ_TURBO4, 64, 32, 16, dev)
     q = torch.zeros(64, 32, 1, 128, dtype=torch.float16, device=dev)
     out = torch.empty_like(q)
