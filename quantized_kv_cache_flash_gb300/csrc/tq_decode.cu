@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
+    griddep_wait();  // lengths, cache and q come from earlier work on the stream
     const int per_b = p.hkv * p.row_groups;
     BatchScan scan;
     scan.init(reinterpret_cast<int*>(smem + C::kScanOff) + warp * 128, p.lengths, p.batch, per_b,
@@ -542,6 +543,7 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
             if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
 
+        if (pos + nchunks >= hi) griddep_launch_dependents();  // last segment: let the merge launch
         if (stalled) {
             // Drain this warp's copies still in flight (bounded), flag, and stop.
             for (int k = 0; k < C::kStages; ++k) {
@@ -633,8 +635,11 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
 // One warp per output row (b, q head, query j): merge the partials of the
 // CTAs that covered the row's unit with their log-sum-exp weights, apply
 // v_rescale, leave the rotated basis (Rot^-1(y) = s * (H y) / sqrt(128)) and
-// store fp16.
+// store fp16.  The lanes first split the partials' (max, sum) pairs between
+// them; then every lane walks the partials for its 4 dims, 8 loads in flight,
+// taking each partial's weight from the lane that computed it.
 __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__ CombineParams p) {
+    griddep_wait();  // the decode kernel's partials
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int total = p.batch * p.hq * p.tq;
@@ -650,9 +655,9 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
     const int unit = b * per_b + ui;
 
     // the unit's global chunk range [k_first, k_first + nch) and the CTAs over it
-    long long before = 0, all = 0;
+    int before = 0, all = 0;
     for (int bb = lane; bb < p.batch; bb += 32) {
-        const long long v = 1ll * unit_chunks(p.lengths, bb, p.max_len) * per_b;
+        const int v = unit_chunks(p.lengths, bb, p.max_len) * per_b;
         all += v;
         if (bb < b) before += v;
     }
@@ -662,34 +667,59 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
         all += __shfl_xor_sync(0xffffffffu, all, o);
     }
     const int nch = unit_chunks(p.lengths, b, p.max_len);
-    const long long P = p.num_ctas;
-    int c0 = 0, c1 = -1;
+    const int P = p.num_ctas, cq = all / P, cr = all - cq * P;
+    const bool some_empty = all < P;  // then some CTAs have no chunk and wrote nothing
+    int c0 = 0, n = 0;
     if (nch > 0) {
-        const long long k_first = before + static_cast<long long>(ui) * nch;
-        const long long k_last = k_first + nch - 1;
-        c0 = static_cast<int>(((k_first + 1) * P - 1) / all);  // the CTA holding chunk k
-        c1 = static_cast<int>(((k_last + 1) * P - 1) / all);
+        const int k_first = before + ui * nch;
+        c0 = static_cast<int>((static_cast<long long>(k_first + 1) * P - 1) / all);
+        const int c1 = static_cast<int>((static_cast<long long>(k_first + nch) * P - 1) / all);
+        n = c1 - c0 + 1;
     }
+    auto used = [&](int i) {
+        const int c = c0 + i;
+        return i < n && (!some_empty || c * cq + (c * cr) / P < (c + 1) * cq + ((c + 1) * cr) / P);
+    };
+    const size_t row0 = (static_cast<size_t>(c0) + unit) * 16 + rl;  // partial of CTA c0
 
-    // with at least one chunk per CTA every CTA in [c0, c1] wrote a partial;
-    // otherwise skip the CTAs whose share is empty
-    const bool some_empty = all < P;
     float M = -INFINITY;
-    for (int c = c0; c <= c1; ++c) {
-        if (some_empty && c * all / P == (c + 1) * all / P) continue;
-        M = fmaxf(M, p.part_ml[((static_cast<size_t>(c) + unit) * 16 + rl) * 2]);
-    }
+    for (int i = lane; i < n; i += 32)
+        if (used(i)) M = fmaxf(M, __ldcg(p.part_ml + (row0 + 16 * static_cast<size_t>(i)) * 2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+
     float den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = c0; c <= c1; ++c) {
-        if (some_empty && c * all / P == (c + 1) * all / P) continue;
-        const size_t pi = (static_cast<size_t>(c) + unit) * 16 + rl;
-        const float m = p.part_ml[pi * 2];
-        const float w = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
-        den += w * p.part_ml[pi * 2 + 1];
-        const float4 o = *reinterpret_cast<const float4*>(p.part_o + pi * kD + lane * 4);
-        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+        float w = 0.f;
+        if (used(i0 + lane)) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + row0 +
+                                     16 * static_cast<size_t>(i0 + lane));
+            if (ml.x != -INFINITY) w = fast_exp2(ml.x - M);
+            den += w * ml.y;
+        }
+        const int nb = min(32, n - i0);
+        for (int k0 = 0; k0 < nb; k0 += 8) {
+            float wk[8];
+            float4 o[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                wk[k] = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
+                o[k] = (k0 + k < nb && wk[k] != 0.f)
+                           ? __ldcg(reinterpret_cast<const float4*>(
+                                        p.part_o + (row0 + 16 * static_cast<size_t>(i0 + k0 + k)) * kD) +
+                                    lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                acc.x += wk[k] * o[k].x; acc.y += wk[k] * o[k].y;
+                acc.z += wk[k] * o[k].z; acc.w += wk[k] * o[k].w;
+            }
+        }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     float inv = 0.f;
     if (den > 0.f) inv = p.v_rescale / den;
     else if (lane == 0) atomicOr(p.status, kStatusShortContext);
@@ -699,10 +729,10 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
     const float nrm = 0.08838834764831845f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = ((sn >> i) & 1u) ? -v[i] * nrm : v[i] * nrm;
-    uint2 o;
-    o.x = pack_half2(v[0], v[1]);
-    o.y = pack_half2(v[2], v[3]);
-    *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(row) * kD + lane * 4) = o;
+    uint2 out;
+    out.x = pack_half2(v[0], v[1]);
+    out.y = pack_half2(v[2], v[3]);
+    *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(row) * kD + lane * 4) = out;
 }
 
 template <int KB, int VB, int NT>
@@ -718,8 +748,8 @@ static int launch_decode_t(const DecodeParams& p, const CUtensorMap* kmap, cudaS
     }
     dim3 grid(p.num_ctas);
     if (ev0) cudaEventRecord(ev0, stream);
-    tq_decode_kernel<KB, VB, NT><<<grid, C::kWarps * 32, C::kSmemAlloc, stream>>>(p, *kmap);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(tq_decode_kernel<KB, VB, NT>, grid, dim3(C::kWarps * 32),
+                               C::kSmemAlloc, stream, p, *kmap);
     if (ev1) cudaEventRecord(ev1, stream);
     return e;
 }
@@ -744,8 +774,7 @@ int launch_decode(int kbits, int vbits, const DecodeParams& p, const CUtensorMap
 
 int launch_combine(const CombineParams& p, cudaStream_t stream) {
     const int rows = p.batch * p.hq * p.tq;
-    tq_combine_kernel<<<(rows + 3) / 4, 128, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(tq_combine_kernel, dim3((rows + 3) / 4), dim3(128), 0, stream, p);
 }
 
 template <int KB, int VB>

@@ -328,6 +328,8 @@ constexpr int kEncVecs = 8 * kEncWarps;
 template <int KB, int VB>
 __global__ void __launch_bounds__(32 * kEncWarps)
     tq_encode_kernel(const __grid_constant__ EncodeParams p, int k_blocks) {
+    griddep_wait();                // inputs and lengths come from earlier work on the stream
+    griddep_launch_dependents();   // the decode that follows may start launching
     const int lane = threadIdx.x & 31;
     const int q = lane & 3;
     const unsigned gmask = 0xFu << (lane & ~3);
@@ -464,6 +466,8 @@ __device__ __forceinline__ void encode_vector_warp(const __half* src, uint8_t* d
 // grid: 4 warps per CTA, warp = (K-or-V, vector).  KB = 0 copies fp16 K rows.
 template <int KB, int VB>
 __global__ void __launch_bounds__(128) tq_encode_small_kernel(const __grid_constant__ EncodeParams p) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const long long gw = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     const long long nvec = static_cast<long long>(p.batch) * p.hkv * p.t_new;
@@ -500,25 +504,22 @@ __global__ void __launch_bounds__(128) tq_encode_small_kernel(const __grid_const
 int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stream) {
     const long long nvec = 1ll * p.batch * p.hkv * p.t_new;
     if (nvec <= 4096) {   // a warp per vector: short chains for small appends
-        const unsigned int sblocks = static_cast<unsigned int>((2 * nvec + 3) / 4);
-        if (kbits == 16 && vbits == 4) tq_encode_small_kernel<0, 4><<<sblocks, 128, 0, stream>>>(p);
-        else if (kbits == 3 && vbits == 3) tq_encode_small_kernel<3, 3><<<sblocks, 128, 0, stream>>>(p);
-        else if (kbits == 4 && vbits == 4) tq_encode_small_kernel<4, 4><<<sblocks, 128, 0, stream>>>(p);
-        else if (kbits == 16 && vbits == 3) tq_encode_small_kernel<0, 3><<<sblocks, 128, 0, stream>>>(p);
-        else if (kbits == 4 && vbits == 3) tq_encode_small_kernel<4, 3><<<sblocks, 128, 0, stream>>>(p);
-        else return cudaErrorInvalidValue;
-        return cudaGetLastError();
+        const dim3 grid(static_cast<unsigned int>((2 * nvec + 3) / 4)), block(128);
+        if (kbits == 16 && vbits == 4) return launch_pdl(tq_encode_small_kernel<0, 4>, grid, block, 0, stream, p);
+        if (kbits == 3 && vbits == 3) return launch_pdl(tq_encode_small_kernel<3, 3>, grid, block, 0, stream, p);
+        if (kbits == 4 && vbits == 4) return launch_pdl(tq_encode_small_kernel<4, 4>, grid, block, 0, stream, p);
+        if (kbits == 16 && vbits == 3) return launch_pdl(tq_encode_small_kernel<0, 3>, grid, block, 0, stream, p);
+        if (kbits == 4 && vbits == 3) return launch_pdl(tq_encode_small_kernel<4, 3>, grid, block, 0, stream, p);
+        return cudaErrorInvalidValue;
     }
     const int kblocks = static_cast<int>((nvec + kEncVecs - 1) / kEncVecs);
-    const unsigned int blocks = static_cast<unsigned int>(2 * kblocks);
-    const int thr = 32 * kEncWarps;
-    if (kbits == 16 && vbits == 4) tq_encode_kernel<0, 4><<<blocks, thr, 0, stream>>>(p, kblocks);
-    else if (kbits == 3 && vbits == 3) tq_encode_kernel<3, 3><<<blocks, thr, 0, stream>>>(p, kblocks);
-    else if (kbits == 4 && vbits == 4) tq_encode_kernel<4, 4><<<blocks, thr, 0, stream>>>(p, kblocks);
-    else if (kbits == 16 && vbits == 3) tq_encode_kernel<0, 3><<<blocks, thr, 0, stream>>>(p, kblocks);
-    else if (kbits == 4 && vbits == 3) tq_encode_kernel<4, 3><<<blocks, thr, 0, stream>>>(p, kblocks);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    const dim3 grid(static_cast<unsigned int>(2 * kblocks)), block(32 * kEncWarps);
+    if (kbits == 16 && vbits == 4) return launch_pdl(tq_encode_kernel<0, 4>, grid, block, 0, stream, p, kblocks);
+    if (kbits == 3 && vbits == 3) return launch_pdl(tq_encode_kernel<3, 3>, grid, block, 0, stream, p, kblocks);
+    if (kbits == 4 && vbits == 4) return launch_pdl(tq_encode_kernel<4, 4>, grid, block, 0, stream, p, kblocks);
+    if (kbits == 16 && vbits == 3) return launch_pdl(tq_encode_kernel<0, 3>, grid, block, 0, stream, p, kblocks);
+    if (kbits == 4 && vbits == 3) return launch_pdl(tq_encode_kernel<4, 3>, grid, block, 0, stream, p, kblocks);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace tq

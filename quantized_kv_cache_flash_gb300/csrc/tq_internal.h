@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "tq.h"
 
 namespace tq {
@@ -73,6 +75,25 @@ int decode_ctas_per_sm(int kbits, int vbits, int group_rows);
 
 // Query rows per row group for `rows` query rows of one KV head.
 inline int group_rows_for(int rows) { return rows <= 8 ? 8 : 16; }
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while its predecessor in the stream finishes (every kernel of this library
+// waits for its predecessor with griddep_wait() before touching memory).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // (K bits, V bits) of a mode; 16 = fp16 K.
 inline int mode_bits(int mode, int* kb, int* vb) {

@@ -114,6 +114,24 @@ def test_decode_empty_sequences_in_a_large_batch():
     H.assert_attention_close(got[live], want[live])
 
 
+def test_decode_hint_far_above_lengths():
+    # the grid is planned for 4096 tokens per sequence but the sequences hold
+    # 5..70: most CTAs get no chunk, units span CTAs with empty shares
+    mode, B, Hq, Hkv, cap = "turbo4", 3, 8, 2, 4096
+    lengths = [5, 70, 33]
+    kd, kn, vd, vn = H.random_cache(mode, B, Hkv, cap, 321)
+    q = wl.random_fp16(322, (B, Hq, 1, 128))
+    cache = H.gpu_cache_from_records(mode, B, Hkv, cap, lengths, kd, kn, vd, vn, DEV)
+    ctx = tqf.Context()
+    for _ in range(3):   # repeated calls reuse the arrival counters
+        got, status, _ = _run_decode(cache, q, 1, cap, ctx=ctx)
+        assert status == 0
+        units = {(b, h): H.oracle_unit_from_records(mode, kd, kn, vd, vn, b, h, lengths[b])
+                 for b in range(B) for h in range(Hkv)}
+        want = H.oracle_decode(mode, q, units, lengths, Hkv, 1, 1 / math.sqrt(128), 1.0)
+        H.assert_attention_close(got, want)
+
+
 def test_decode_lengths_beyond_hint_are_clamped():
     # tokens past max_len_hint are not read: equals the oracle on the first 64
     mode = "turbo4"
