@@ -372,7 +372,7 @@ def gpu_arm(args, rank, world, device_index):
         "step_bytes": sum(step_bytes) / steps, "clocks": clk,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": (achieved / peak) if achieved else None,
-                     "traffic": load_traffic(w),
+                     "traffic": load_traffic(w, sum(kern_bytes) / max(kern_n, 1)),
                      "kernel": "tq_decode_kernel (split-K)",
                      "kernel_ms": kern_ms / kern_n if kern_n else None,
                      "kernel_bytes": sum(kern_bytes) / max(kern_n, 1),
@@ -394,13 +394,32 @@ def workload(args) -> wl.Workload:
     return w
 
 
-def load_traffic(w):
-    """DRAM bytes per decode launch from the committed ncu summary, if it
-    covers this workload and the current kernel; else None."""
+TRAFFIC_SOURCES = ["quantized_kv_cache_flash_gb300/csrc/tq_decode.cu",
+                   "quantized_kv_cache_flash_gb300/csrc/tq_device.cuh",
+                   "quantized_kv_cache_flash_gb300/csrc/tq_internal.h"]
+
+
+def decode_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(w, kernel_bytes):
+    """DRAM bytes (read + write) per decode launch: the committed ncu capture's
+    DRAM bytes per algorithmic byte (profiles/traffic.json, taken on a smaller
+    batch of the same workload, traffic growing with the units processed)
+    times this launch's algorithmic bytes.  None when the capture does not
+    cover this workload or the decode kernel sources changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        d = json.load(open(p))
-        return d.get(w.name)
+        d = json.load(open(p)).get(w.name)
+        if not d or d.get("source_hash") != decode_source_hash():
+            return None
+        return float(d["dram_bytes_per_algorithmic_byte"]) * kernel_bytes
     except Exception:
         return None
 

@@ -122,9 +122,10 @@ typedef struct {
 } tq_cache;
 
 /*
- * Append t_new tokens per sequence (the cache update of the decode step,
- * mlxcel pull request #369, Change: "uses v_rescale and mutates cache state
- * identically ... (only self.update)").
+ * Append t_new tokens per sequence: the cache update that precedes the
+ * attention of a decode step (mlxcel pull request #369, Change: the decode
+ * path updates the packed cache exactly as the plain update does, then
+ * attends over the visible prefix).
  *   k_new, v_new: fp16 [batch, num_kv_heads, t_new, 128] device pointers.
  *   Token j of sequence b is written at position lengths[b] + j; afterwards
  *   lengths[b] += t_new.  A sequence with lengths[b] + t_new > capacity is left

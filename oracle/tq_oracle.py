@@ -8,17 +8,18 @@ shares no code, table or constant generator with the CUDA path.
 What it computes (plain, slow, obviously correct; float64 unless stated):
 
 * Sign vector: splitmix64 seeded with ``rot_seed``; s_i = -1 iff the top bit of
-  output i is set.  The pages name a "seeded sign flip" but no generator
-  (mlxcel PR #369 "route Turbo4Asym decode through dequant-SDPA", Change), so
-  this is a format reading.
+  output i is set.  The pages call for a seeded sign flip but name no
+  generator (mlxcel PR #369 "route Turbo4Asym decode through dequant-SDPA",
+  Change), so this is a format reading.
 * Rotation: Rot(x) = H (s * x) / sqrt(D), Rot^-1(y) = s * (H y) / sqrt(D), H the
   Sylvester Hadamard matrix H[i][j] = (-1)^popcount(i & j), D = 128 -- the
-  "WHT-rotated basis" of mlxcel PR #369 (Change) and the "128-element rotation
-  group" of turboquant_plus smem-dequant-experiment.md (Hypothesis 1).
+  Walsh-Hadamard rotated basis of mlxcel PR #369 (Change), over the 128-element
+  rotation group of turboquant_plus smem-dequant-experiment.md (Hypothesis 1).
 * Codebook: Lloyd-Max quantiser of N(0, 1/128) with 2^b levels, iterated in
   fp64 to a fixed point and rounded to fp32; the fp32 values are the codebook
-  both sides use.  "3-bit = sign + 4 magnitudes" (smem-dequant-experiment.md,
-  "4-mag LUT"); "4bit PolarQuant" (mlxcel PR #369, Result).
+  both sides use.  The 3-bit codebook is a sign and four magnitudes (the
+  four-magnitude lookup table of smem-dequant-experiment.md); the 4-bit one is
+  the V codec of mlxcel PR #369 (Result).
 * Encode: n16 = fp16 round-to-nearest-even of the exact L2 norm of the fp16
   input; u = Rot(x) / n (unrounded fp64 n), rounded to fp32; idx = the nearest
   codebook entry to that fp32 u in exact arithmetic, ties to the lower index.
@@ -29,8 +30,8 @@ What it computes (plain, slow, obviously correct; float64 unless stated):
 * Attention (the definition the fast path must reproduce): full dequant of K
   and V to the original basis, then softmax(q K^T * scale) V with the GQA map
   kv_head = q_head // G, query j of a Tq block seeing tokens [0, L - Tq + j],
-  times the scalar v_rescale -- the "exact full-dequant attention" the mlxcel
-  parity test compares against (PR #369, Result and commit ce39cbb).
+  times the scalar v_rescale -- the exact attention over the fully dequantised
+  cache that the mlxcel parity test compares against (PR #369, Result).
 * The rotated-basis shortcut rotate(SDPA(q,k,v)) == SDPA(q,k,rotate(v))
   (PR #369, Change) is computed separately in ``decode_rotated_unit`` and checked
   against the definition by the tests; it is never used to produce the
@@ -69,7 +70,8 @@ def sign_vector(rot_seed: int, d: int = D) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
-# rotation (mlxcel PR #369 "WHT-rotated basis"; sign flip then normalised WHT)
+# rotation (mlxcel PR #369, Change: the Walsh-Hadamard rotated basis; sign flip
+# then normalised WHT)
 # --------------------------------------------------------------------------
 def hadamard(d: int = D) -> np.ndarray:
     """Sylvester Hadamard matrix, H[i][j] = (-1)^popcount(i & j), as float64."""

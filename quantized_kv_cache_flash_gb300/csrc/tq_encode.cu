@@ -11,9 +11,10 @@
 //   code = sign-magnitude index of the nearest codebook entry to u, decided
 //          with thresholds that make the fp32 comparison exact against the
 //          true midpoints of neighbouring centroids (ties to the lower index).
-// ("seeded sign flip + WHT + nearest centroid + bit-pack": mlxcel pull request
-// #369, Change; turboquant_plus smem-dequant experiment, Hypothesis 1, for the
-// 128-element rotation group with one norm per group.)
+// (The encode of mlxcel pull request #369, Change: seeded sign flip, Walsh-
+// Hadamard rotation, nearest codebook entry, bit packing; turboquant_plus
+// smem-dequant experiment, Hypothesis 1: a 128-element rotation group with
+// one norm per group.)
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
