@@ -45,7 +45,9 @@ import numpy as np
 D = 128
 MASK64 = (1 << 64) - 1
 MODES = {"turbo4_asym": (None, 4), "turbo3": (3, 3), "turbo4": (4, 4),
-         "turbo3_asym": (None, 3), "turbo4k_3v": (4, 3)}
+         "turbo3_asym": (None, 3), "turbo4k_3v": (4, 3), "turbo3_table": (3, 3)}
+# modes whose records carry the centroid x norm table instead of a norm
+TABLE_MODES = {"turbo3_table"}
 
 
 # --------------------------------------------------------------------------
@@ -344,6 +346,41 @@ def dequant_rotated(idx: np.ndarray, n16: np.ndarray, cb32: np.ndarray) -> np.nd
     return np.asarray(n16, np.float64)[..., None] * cb32.astype(np.float64)[idx]
 
 
+def centroid_norm_table(n16: np.ndarray, cb32: np.ndarray) -> np.ndarray:
+    """fp16 [..., 2^b]: entry j = fp16 round-to-nearest-even of c_j * n16.
+
+    The record format of turboquant_plus smem-dequant-experiment.md, "What
+    Would Actually Work" item 1: the pre-multiplied centroid x norm values of
+    each 128-element group stored with its block.  c_j (fp32) times n16 (fp16)
+    is exact in fp64, so this is one rounding of the exact product.
+    """
+    prod = np.asarray(n16, np.float16).astype(np.float64)[..., None] * cb32.astype(np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        return prod.astype(np.float16)
+
+
+def pack_table_records(idx: np.ndarray, table16: np.ndarray) -> np.ndarray:
+    """3-bit codes (the 48-byte layout of pack_codes) followed by the 8-entry
+    fp16 table in ascending index order, little-endian: 64 bytes per record."""
+    codes = pack_codes(idx, 3)
+    tab = np.ascontiguousarray(np.asarray(table16, np.float16)).astype("<f2").view(np.uint8)
+    return np.concatenate([codes, tab.reshape(*codes.shape[:-1], 16)], axis=-1)
+
+
+def unpack_table_records(rec: np.ndarray):
+    """Inverse of pack_table_records: (ascending indices [..., 128], fp16 table [..., 8])."""
+    rec = np.ascontiguousarray(rec, np.uint8)
+    idx = unpack_codes(rec[..., :48], 3)
+    tab = np.ascontiguousarray(rec[..., 48:64]).view("<f2").astype(np.float16)
+    return idx, tab
+
+
+def dequant_table(idx: np.ndarray, table16: np.ndarray) -> np.ndarray:
+    """table[idx] in the rotated basis (fp64): the whole dequant of the table format."""
+    t = np.asarray(table16, np.float16).astype(np.float64)
+    return np.take_along_axis(t, np.asarray(idx, np.int64), axis=-1)
+
+
 def dequant_full(idx, n16, cb32, s) -> np.ndarray:
     """Rot^-1(n16 * c[idx]): the vector back in the original basis."""
     return rotate_inv(dequant_rotated(idx, n16, cb32), s)
@@ -411,8 +448,12 @@ def visible_counts(L: int, tq: int) -> np.ndarray:
 def unit_kv_full(mode: str, unit: dict, cbk, cbv, s):
     """Original-basis K and V (fp64) for one (b, kv-head) from its cache record.
 
-    unit keys: 'k' (fp16 [L,128], asym only) or 'k_idx','k_norm'; 'v_idx','v_norm'.
+    unit keys: 'k' (fp16 [L,128], asym only) or 'k_idx','k_norm'; 'v_idx','v_norm';
+    the table modes: 'k_idx','k_table','v_idx','v_table' (fp16 [L, 8] tables).
     """
+    if mode in TABLE_MODES:
+        return (rotate_inv(dequant_table(unit["k_idx"], unit["k_table"]), s),
+                rotate_inv(dequant_table(unit["v_idx"], unit["v_table"]), s))
     if MODES[mode][0] is None:
         K = np.asarray(unit["k"], np.float64)
     else:
@@ -457,11 +498,15 @@ def decode_rotated_unit(mode: str, q_rows, unit: dict, L: int, tq: int, G: int,
     V stays rotated; only the output is inverse-rotated.
     """
     q = np.asarray(q_rows, np.float64).reshape(G * tq, D)
-    if MODES[mode][0] is None:
+    if mode in TABLE_MODES:
+        qk, K = rotate(q, s), dequant_table(unit["k_idx"], unit["k_table"])
+        Vr = dequant_table(unit["v_idx"], unit["v_table"])
+    elif MODES[mode][0] is None:
         qk, K = q, np.asarray(unit["k"], np.float64)
+        Vr = dequant_rotated(unit["v_idx"], unit["v_norm"], cbv)
     else:
         qk, K = rotate(q, s), dequant_rotated(unit["k_idx"], unit["k_norm"], cbk)
-    Vr = dequant_rotated(unit["v_idx"], unit["v_norm"], cbv)
+        Vr = dequant_rotated(unit["v_idx"], unit["v_norm"], cbv)
     vis = np.tile(visible_counts(L, tq), G)
     o_rot = softmax_attention(qk, K[:L], Vr[:L], scale, vis)
     return (rotate_inv(o_rot, s) * v_rescale).reshape(G, tq, D)
@@ -476,7 +521,8 @@ def encode_append(cache: dict, k_new: np.ndarray, v_new: np.ndarray, cbk, cbv, s
 
     cache (numpy, modified in place): 'mode', 'lengths' int32 [B], 'capacity',
     'k' fp16 [B,Hkv,C,128] (asym) or 'k_data' uint8 [B,Hkv,C,RB] + 'k_norm' fp16
-    [B,Hkv,C]; 'v_data', 'v_norm'.  A sequence whose append would pass the
+    [B,Hkv,C]; 'v_data', 'v_norm' (the table modes: 'k_data', 'v_data' with
+    64-byte records and no norms).  A sequence whose append would pass the
     capacity is left untouched.  Returns per-sequence error flags
     (bit 0 = capacity, bit 1 = norm overflow).
     """
@@ -490,6 +536,14 @@ def encode_append(cache: dict, k_new: np.ndarray, v_new: np.ndarray, cbk, cbv, s
             err[b] |= 1
             continue
         for h in range(H):
+            if mode in TABLE_MODES:
+                for x, cb, key in ((k_new, cbk, "k_data"), (v_new, cbv, "v_data")):
+                    idx, n16, _, ov = encode(x[b, h], cb, s)
+                    cache[key][b, h, L:L + T] = pack_table_records(
+                        idx, centroid_norm_table(n16, cb))
+                    if ov.any():
+                        err[b] |= 2
+                continue
             if kb is None:
                 cache["k"][b, h, L:L + T] = k_new[b, h]
             else:

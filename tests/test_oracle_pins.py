@@ -334,6 +334,11 @@ def _random_unit(rng, mode, L, cbk, cbv):
     kb, vb = o.MODES[mode]
     unit = {"v_idx": rng.integers(0, 1 << vb, (L, 128)).astype(np.uint8),
             "v_norm": (rng.random(L) * 12 + 1).astype(np.float16)}
+    if mode in o.TABLE_MODES:
+        unit["k_idx"] = rng.integers(0, 1 << kb, (L, 128)).astype(np.uint8)
+        unit["k_table"] = o.centroid_norm_table((rng.random(L) * 12 + 1).astype(np.float16), cbk)
+        unit["v_table"] = o.centroid_norm_table(unit.pop("v_norm"), cbv)
+        return unit
     if kb is None:
         unit["k"] = rng.standard_normal((L, 128)).astype(np.float16)
     else:
@@ -342,7 +347,8 @@ def _random_unit(rng, mode, L, cbk, cbv):
     return unit
 
 
-@pytest.mark.parametrize("mode", ["turbo4_asym", "turbo3", "turbo4", "turbo3_asym", "turbo4k_3v"])
+@pytest.mark.parametrize("mode", ["turbo4_asym", "turbo3", "turbo4", "turbo3_asym", "turbo4k_3v",
+                                  "turbo3_table"])
 def test_rotated_basis_identity(mode):
     """rotate(SDPA(q,k,v)) == SDPA(q,k,rotate(v)): the shortcut equals full dequant."""
     rng = np.random.default_rng(11)
@@ -510,3 +516,84 @@ def test_sparse_v_decode_unit_reduces_to_decode_unit_at_zero_tau():
     assert np.array_equal(got, want) and not bound.any()
     got, bound = o.decode_unit_sparse_v("turbo3", q, unit, 33, 3, 2, cb, cb, s, 0.1, -0.5, 2.0)
     assert not got.any() and np.all(bound >= np.abs(want) - 1e-12)
+
+
+# --------------------------------------------------------------------------
+# centroid x norm table records (format B)
+# --------------------------------------------------------------------------
+def _fp16_rne_fraction(x: Fraction) -> float:
+    """Round an exact rational to fp16 (normal range), ties to even, by brute
+    force over the binade's grid."""
+    sign = -1 if x < 0 else 1
+    a = abs(x)
+    e = 0
+    while a >= 2:
+        a /= 2; e += 1
+    while a < 1:
+        a *= 2; e -= 1
+    step = Fraction(1, 1024)
+    lo = (a // step) * step
+    hi = lo + step
+    d_lo, d_hi = a - lo, hi - a
+    if d_lo < d_hi or (d_lo == d_hi and (lo / step) % 2 == 0):
+        r = lo
+    else:
+        r = hi
+    return sign * float(r * Fraction(2) ** e)
+
+
+def test_centroid_norm_table_is_one_rounding_of_the_exact_product():
+    rng = np.random.default_rng(31)
+    cb = o.codebook(3)
+    n16 = (rng.random(50) * 30 + 0.5).astype(np.float16)
+    tab = o.centroid_norm_table(n16, cb)
+    for i in range(50):
+        for j in range(8):
+            exact = Fraction(float(n16[i])) * Fraction(float(cb[j]))
+            assert float(tab[i, j]) == _fp16_rne_fraction(exact), (i, j)
+    # a zero norm gives an all-zero table; symmetry of the codebook carries over
+    assert not o.centroid_norm_table(np.float16(0), cb).astype(np.float64).any()
+    assert np.array_equal(tab[:, :4].astype(np.float64), -tab[:, ::-1][:, :4].astype(np.float64))
+
+
+def test_table_record_bytes_and_roundtrip():
+    cb = o.codebook(3)
+    idx = np.zeros((1, 128), np.uint8)
+    idx[0, 0] = 7
+    n16 = np.array([2.0], np.float16)
+    rec = o.pack_table_records(idx, o.centroid_norm_table(n16, cb))
+    assert rec.shape == (1, 64)
+    assert np.array_equal(rec[0, :48], o.pack_codes(idx, 3)[0])
+    # bytes 48..63: fp16 little-endian 2*c_0 .. 2*c_7
+    want = (2.0 * cb.astype(np.float64)).astype(np.float16).astype("<f2").view(np.uint8)
+    assert np.array_equal(rec[0, 48:], want)
+    rng = np.random.default_rng(32)
+    idx = rng.integers(0, 8, (9, 128)).astype(np.uint8)
+    tab = o.centroid_norm_table((rng.random(9) * 5).astype(np.float16), cb)
+    i2, t2 = o.unpack_table_records(o.pack_table_records(idx, tab))
+    assert np.array_equal(i2, idx) and np.array_equal(t2.view(np.uint16), tab.view(np.uint16))
+
+
+def test_table_dequant_is_the_fp16_rounding_of_the_norm_format():
+    rng = np.random.default_rng(33)
+    cb = o.codebook(3)
+    idx = rng.integers(0, 8, (20, 128)).astype(np.uint8)
+    n16 = (rng.random(20) * 9 + 1).astype(np.float16)
+    a = o.dequant_rotated(idx, n16, cb)
+    b = o.dequant_table(idx, o.centroid_norm_table(n16, cb))
+    assert np.all(np.abs(a - b) <= np.abs(a) * 2.0 ** -11)
+    assert np.any(a != b)
+
+
+def test_table_mode_append_matches_encode():
+    s = o.sign_vector(42); cb = o.codebook(3)
+    rng = np.random.default_rng(34)
+    x = rng.standard_normal((1, 2, 5, 128)).astype(np.float16)
+    cache = {"mode": "turbo3_table", "capacity": 16, "lengths": np.array([3], np.int32),
+             "k_data": np.zeros((1, 2, 16, 64), np.uint8), "v_data": np.zeros((1, 2, 16, 64), np.uint8)}
+    assert not o.encode_append(cache, x, -x, cb, cb, s).any()
+    assert cache["lengths"][0] == 8
+    idx, tab = o.unpack_table_records(cache["k_data"][0, 1, 3:8])
+    ei, en, _, _ = o.encode(x[0, 1], cb, s)
+    assert np.array_equal(idx, ei)
+    assert np.array_equal(tab.view(np.uint16), o.centroid_norm_table(en, cb).view(np.uint16))
