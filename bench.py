@@ -41,7 +41,10 @@ if ROOT not in sys.path:
 from quantized_kv_cache_flash_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "quantized-KV decode attention: effective HBM GB/s (% of peak), tokens/s"
-REC = {"turbo4_asym": (256, 66), "turbo3": (50, 50), "turbo4": (66, 66)}   # bytes/token/head (K, V)
+# bytes per token per kv head (K, V): packed record + fp16 norm, or fp16 K, or
+# a table record (codes + centroid x norm table, no norm)
+REC = {"turbo4_asym": (256, 66), "turbo3": (50, 50), "turbo4": (66, 66),
+       "turbo3_asym": (256, 50), "turbo4k_3v": (66, 50), "turbo3_table": (64, 64)}
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -135,15 +138,19 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle sample (run in a child process with one BLAS thread)
 # ---------------------------------------------------------------------------
-def oracle_sample(wnum: int, budget_s: float, seed: int = 0):
+def oracle_sample(wnum: int, budget_s: float, seed: int = 0, mode=None):
     """Run the oracle on (b, kv-head) units of the workload until budget_s is
     spent: append of the step's new token (encode) + decode over the unit's
     visible context, on a packed cache of random records.  Returns
     (bytes, seconds, units, description)."""
+    import dataclasses
     from oracle import tq_oracle as o
     w = wl.by_number(wnum)
+    if mode:
+        w = dataclasses.replace(w, mode=mode)
     lens = wl.lengths(w)
-    kb, vb = {"turbo4_asym": (None, 4), "turbo3": (3, 3), "turbo4": (4, 4)}[w.mode]
+    kb, vb = o.MODES[w.mode]
+    table = w.mode in o.TABLE_MODES
     cbk = o.codebook(kb) if kb else None
     cbv = o.codebook(vb)
     s = o.sign_vector(w.rot_seed)
@@ -172,7 +179,11 @@ def oracle_sample(wnum: int, budget_s: float, seed: int = 0):
             o.encode(knew, cbk, s)
         o.encode(knew, cbv, s)
         unit = {"v_idx": o.unpack_codes(vdat, vb), "v_norm": vnorm}
-        if kb is None:
+        if table:
+            o.centroid_norm_table(o.encode(knew, cbv, s)[1], cbv)  # the records' tables
+            unit = {"k_idx": o.unpack_codes(kdat, kb), "k_table": o.centroid_norm_table(knorm, cbk),
+                    "v_idx": unit["v_idx"], "v_table": o.centroid_norm_table(vnorm, cbv)}
+        elif kb is None:
             unit["k"] = kdat
         else:
             unit["k_idx"] = o.unpack_codes(kdat, kb)
@@ -187,10 +198,10 @@ def oracle_sample(wnum: int, budget_s: float, seed: int = 0):
     return total_b, t_spent, units, desc
 
 
-def run_cpu_baseline(wnum: int, budget_s: float):
+def run_cpu_baseline(wnum: int, budget_s: float, mode=None):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     cmd = [sys.executable, os.path.abspath(__file__), "--_oracle-sample", str(wnum),
-           "--_budget", str(budget_s)]
+           "--_budget", str(budget_s)] + (["--mode", mode] if mode else [])
     r = subprocess.run(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
                        timeout=600)
     if r.returncode != 0:
@@ -391,6 +402,8 @@ def workload(args) -> wl.Workload:
         if args.batch > w.batch:
             raise SystemExit("--batch can only shrink a workload")
         w = dataclasses.replace(w, batch=args.batch, name=f"{w.name}__batch{args.batch}")
+    if args.mode and args.mode != w.mode:
+        w = dataclasses.replace(w, mode=args.mode, name=f"{w.name}__{args.mode}")
     return w
 
 
@@ -450,12 +463,14 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (small profiling cases only)")
+    ap.add_argument("--mode", default=None, choices=sorted(REC),
+                    help="run the workload's shapes in another cache mode (format and mode A/B)")
     ap.add_argument("--_oracle-sample", type=int, default=None, dest="oracle_sample")
     ap.add_argument("--_budget", type=float, default=10.0, dest="budget")
     args = ap.parse_args()
 
     if args.oracle_sample is not None:
-        b, s, u, desc = oracle_sample(args.oracle_sample, args.budget)
+        b, s, u, desc = oracle_sample(args.oracle_sample, args.budget, mode=args.mode)
         print(json.dumps({"bytes": b, "seconds": s, "units": u, "desc": desc}))
         return
 
@@ -470,11 +485,11 @@ def main():
         # each step: the oracle on a bounded sample of the workload
         per_step = max(1.0, min(10.0, 150.0 / max(args.steps + args.warmup, 1)))
         for i in range(args.warmup):
-            oracle_sample(args.workload, per_step / 4, seed=i)
+            oracle_sample(args.workload, per_step / 4, seed=i, mode=args.mode)
         tb, ts = 0, 0.0
         desc = ""
         for i in range(args.steps):
-            b, s, u, desc = oracle_sample(args.workload, per_step, seed=1000 + i)
+            b, s, u, desc = oracle_sample(args.workload, per_step, seed=1000 + i, mode=args.mode)
             tb += b
             ts += s
         v = tb / ts / 1e9
@@ -496,7 +511,8 @@ def main():
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     r = gpu_arm(args, rank, world, local)
-    cpu = run_cpu_baseline(args.workload, args.cpu_budget) if (rank == 0 and world == 1) else None
+    cpu = (run_cpu_baseline(args.workload, args.cpu_budget, args.mode)
+           if (rank == 0 and world == 1) else None)
     if rank == 0:
         rf = r["roofline"]
         line = {

@@ -65,6 +65,12 @@ extern "C" {
 #define TQ_TURBO4       2
 #define TQ_TURBO3_ASYM  3
 #define TQ_TURBO4K_3V   4
+/* turbo3 K and V in the centroid x norm table format (turboquant_plus
+ * smem-dequant experiment, "What Would Actually Work" item 1): each 64-byte
+ * record is the 48-byte 3-bit code layout followed by eight fp16 values
+ * fp16(c_j * n16), j = 0..7 in ascending codebook order, in place of the norm
+ * (k_norm and v_norm are not used and may be NULL). */
+#define TQ_TURBO3_TABLE 5
 
 /* device status bits (tq_get_status) */
 #define TQ_STATUS_CAPACITY        1u  /* an append would pass `capacity`; that sequence was skipped */
@@ -77,12 +83,14 @@ typedef struct tq_ctx tq_ctx;
 /*
  * The packed cache (caller-owned device memory).
  *
- *   k_data  TQ_TURBO4_ASYM: fp16 [batch, num_kv_heads, capacity, 128], unrotated.
- *           otherwise: uint8 [batch, num_kv_heads, capacity, rb_k] packed codes,
- *           rb_k = tq_record_bytes(bits_k) (48 for 3-bit, 64 for 4-bit).
- *   k_norm  fp16 [batch, num_kv_heads, capacity] (NULL for TQ_TURBO4_ASYM).
+ *   k_data  TQ_TURBO4_ASYM / TQ_TURBO3_ASYM: fp16 [batch, num_kv_heads,
+ *           capacity, 128], unrotated.  Otherwise: uint8 [batch, num_kv_heads,
+ *           capacity, rb_k] packed codes, rb_k = tq_record_bytes(bits_k) (48
+ *           for 3-bit, 64 for 4-bit; 64 for TQ_TURBO3_TABLE records).
+ *   k_norm  fp16 [batch, num_kv_heads, capacity] (NULL for the fp16-K modes
+ *           and TQ_TURBO3_TABLE).
  *   v_data  uint8 [batch, num_kv_heads, capacity, rb_v] packed codes.
- *   v_norm  fp16 [batch, num_kv_heads, capacity].
+ *   v_norm  fp16 [batch, num_kv_heads, capacity] (NULL for TQ_TURBO3_TABLE).
  *   lengths int32 [batch]: visible tokens per sequence; tq_encode_append
  *           advances it on the device.
  *   Code layout of one record (dimension d, code kappa = sign<<(b-1) | rank,

@@ -27,10 +27,15 @@ TQ_TURBO3 = 1
 TQ_TURBO4 = 2
 TQ_TURBO3_ASYM = 3
 TQ_TURBO4K_3V = 4
+TQ_TURBO3_TABLE = 5
 MODES = {"turbo4_asym": TQ_TURBO4_ASYM, "turbo3": TQ_TURBO3, "turbo4": TQ_TURBO4,
-         "turbo3_asym": TQ_TURBO3_ASYM, "turbo4k_3v": TQ_TURBO4K_3V}
+         "turbo3_asym": TQ_TURBO3_ASYM, "turbo4k_3v": TQ_TURBO4K_3V,
+         "turbo3_table": TQ_TURBO3_TABLE}
 MODE_BITS = {TQ_TURBO4_ASYM: (16, 4), TQ_TURBO3: (3, 3), TQ_TURBO4: (4, 4),
-             TQ_TURBO3_ASYM: (16, 3), TQ_TURBO4K_3V: (4, 3)}
+             TQ_TURBO3_ASYM: (16, 3), TQ_TURBO4K_3V: (4, 3), TQ_TURBO3_TABLE: (3, 3)}
+# modes whose 64-byte records carry the centroid x norm table (no norm arrays)
+TABLE_MODES = {TQ_TURBO3_TABLE}
+TABLE_RECORD_BYTES = 64
 
 TQ_STATUS_CAPACITY = 1
 TQ_STATUS_NORM_OVERFLOW = 2
@@ -175,19 +180,25 @@ class Cache:
         import torch
         kb, vb = MODE_BITS[mode]
         self.mode, self.batch, self.num_kv_heads, self.capacity = mode, batch, num_kv_heads, capacity
+        table = mode in TABLE_MODES
         if kb == 16:
             self.k_data = torch.zeros(batch, num_kv_heads, capacity, 128, dtype=torch.float16,
                                       device=device)
+            self.k_norm = None
+        elif table:
+            self.k_data = torch.zeros(batch, num_kv_heads, capacity, TABLE_RECORD_BYTES,
+                                      dtype=torch.uint8, device=device)
             self.k_norm = None
         else:
             self.k_data = torch.zeros(batch, num_kv_heads, capacity, tq_record_bytes(kb),
                                       dtype=torch.uint8, device=device)
             self.k_norm = torch.zeros(batch, num_kv_heads, capacity, dtype=torch.float16,
                                       device=device)
-        self.v_data = torch.zeros(batch, num_kv_heads, capacity, tq_record_bytes(vb),
+        self.v_data = torch.zeros(batch, num_kv_heads, capacity,
+                                  TABLE_RECORD_BYTES if table else tq_record_bytes(vb),
                                   dtype=torch.uint8, device=device)
-        self.v_norm = torch.zeros(batch, num_kv_heads, capacity, dtype=torch.float16,
-                                  device=device)
+        self.v_norm = None if table else torch.zeros(batch, num_kv_heads, capacity,
+                                                     dtype=torch.float16, device=device)
         self.lengths = torch.zeros(batch, dtype=torch.int32, device=device)
         cbk = codebook_k if codebook_k is not None else (
             tq_lloyd_max_codebook(kb) if kb != 16 else [])

@@ -174,10 +174,12 @@ int check_cache(const tq_cache* c, int* kb, int* vb) {
     if (c->head_dim != kD) return TQ_ERR_UNSUPPORTED;
     if (c->batch <= 0 || c->num_kv_heads <= 0 || c->capacity <= 0 || (c->capacity % 16) != 0)
         return TQ_ERR_INVALID_ARG;
-    if (c->k_data == nullptr || c->v_data == nullptr || c->v_norm == nullptr || c->lengths == nullptr)
+    const bool table = tq::mode_table(c->mode);  // table records: no norm arrays
+    if (c->k_data == nullptr || c->v_data == nullptr || c->lengths == nullptr)
         return TQ_ERR_INVALID_ARG;
-    if (*kb != 16 && c->k_norm == nullptr) return TQ_ERR_INVALID_ARG;
-    if (!aligned16(c->k_data) || !aligned16(c->v_data) || !aligned16(c->v_norm) ||
+    if (!table && (c->v_norm == nullptr || (*kb != 16 && c->k_norm == nullptr)))
+        return TQ_ERR_INVALID_ARG;
+    if (!aligned16(c->k_data) || !aligned16(c->v_data) || (c->v_norm && !aligned16(c->v_norm)) ||
         (c->k_norm && !aligned16(c->k_norm)))
         return TQ_ERR_INVALID_ARG;
     const long long rows = 1ll * c->batch * c->num_kv_heads * c->capacity;
@@ -239,8 +241,8 @@ int prepare_kmap(tq_ctx* ctx, const tq_cache* c) {
 // scheduler even out SMs that run at different speeds), fewer when the
 // context (at the hint length) gives a CTA less than two 32-token chunks per
 // warp.
-int plan_ctas(int kb, int vb, int group_rows, long long units, int max_len) {
-    const long long slots = 2ll * kSMs * tq::decode_ctas_per_sm(kb, vb, group_rows);
+int plan_ctas(int kb, int vb, bool table, int group_rows, long long units, int max_len) {
+    const long long slots = 2ll * kSMs * tq::decode_ctas_per_sm(kb, vb, group_rows, table);
     const long long chunks = units * ((max_len + 31) / 32);
     long long ctas = std::min(slots, (chunks + 7) / 8);
     return int(std::max<long long>(ctas, 1));
@@ -320,7 +322,7 @@ int tq_plan_splits(int32_t mode, int32_t batch, int32_t num_kv_heads, int32_t ro
         return TQ_ERR_INVALID_ARG;
     const int gr = tq::group_rows_for(rows_per_kv_head);
     const long long units = 1ll * batch * num_kv_heads * ((rows_per_kv_head + gr - 1) / gr);
-    const int ctas = plan_ctas(kb, vb, gr, units, max_len_hint);
+    const int ctas = plan_ctas(kb, vb, tq::mode_table(mode), gr, units, max_len_hint);
     const long long chunks = units * ((max_len_hint + 31) / 32);
     *num_splits = ctas;
     *split_tokens = int(std::min<long long>((chunks + ctas - 1) / ctas * 32, 1ll << 30));
@@ -361,6 +363,11 @@ int tq_encode_append(tq_ctx** pctx, const tq_cache* c, const void* k_new, const 
     }
     std::memcpy(p.v_gt, ctx->vtab.gt, sizeof(p.v_gt));
     std::memcpy(p.v_ge, ctx->vtab.ge, sizeof(p.v_ge));
+    if (tq::mode_table(c->mode)) {
+        p.table = 1;
+        std::memcpy(p.k_cb, c->codebook_k, sizeof(p.k_cb));
+        std::memcpy(p.v_cb, c->codebook_v, sizeof(p.v_cb));
+    }
     return cuda_err(static_cast<cudaError_t>(
         tq::launch_encode(kb, vb, p, static_cast<cudaStream_t>(stream))));
 }
@@ -394,7 +401,7 @@ int decode_impl(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_h
     const int group_rows = tq::group_rows_for(rows);
     const int row_groups = (rows + group_rows - 1) / group_rows;
     const long long units = 1ll * c->batch * c->num_kv_heads * row_groups;
-    const int ctas = plan_ctas(kb, vb, group_rows, units, max_len_hint);
+    const int ctas = plan_ctas(kb, vb, tq::mode_table(c->mode), group_rows, units, max_len_hint);
     const size_t slots = size_t(ctas + units) * 16;
     if ((r = ensure_work(ctx, slots * (kD + 2) * sizeof(float))) != TQ_OK) return r;
 
@@ -422,6 +429,7 @@ int decode_impl(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_h
     p.num_ctas = ctas;
     p.scale_log2e = sc * 1.4426950408889634f;
     p.sparse_tau = tau;
+    p.table = tq::mode_table(c->mode) ? 1 : 0;
     if (kb != 16) std::memcpy(p.ktab, ctx->ktab.tab, sizeof(p.ktab));
     std::memcpy(p.vtab, ctx->vtab.tab, sizeof(p.vtab));
     std::memcpy(p.signs, ctx->signs, sizeof(p.signs));

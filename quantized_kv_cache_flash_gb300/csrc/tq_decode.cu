@@ -27,22 +27,26 @@ namespace tq {
 
 constexpr int kChunkTokens = 32;  // tokens per warp pipeline stage (2 MMA tiles)
 
-template <int KB, int VB, int NT>
+// TAB: 3-bit records that carry their own centroid x norm table (48 bytes of
+// codes + 8 fp16 values c_j * n, 64 bytes, no norm array).
+template <int KB, int VB, int NT, bool TAB = false>
 struct DecCfg {
     static constexpr int kWarps = 4;
     static constexpr int kChunk = kChunkTokens;
     static constexpr int kStages = (KB == 0 || NT == 1) ? 2 : 3;
     static constexpr int kRows = 8 * NT;                    // query rows per row group
     static constexpr int kMinCtas = (NT == 1) ? 4 : 3;      // resident CTAs per SM targeted
-    static constexpr int kRbK = (KB == 0) ? 256 : KB * 16;  // bytes per K record
-    static constexpr int kRbV = VB * 16;
+    static constexpr int kRbK = TAB ? 64 : (KB == 0) ? 256 : KB * 16;  // bytes per K record
+    static constexpr int kRbV = TAB ? 64 : VB * 16;
+    static constexpr int kQuarterK = TAB ? 12 : kRbK / 4;   // a thread's 32 dims of codes
+    static constexpr int kQuarterV = TAB ? 12 : kRbV / 4;
     static constexpr int kKBytes = kChunk * kRbK;
     static constexpr int kVOff = kKBytes;
     static constexpr int kVBytes = kChunk * kRbV;
     static constexpr int kKnOff = kVOff + kVBytes;
-    static constexpr int kKnBytes = (KB == 0) ? 0 : kChunk * 2;
+    static constexpr int kKnBytes = (KB == 0 || TAB) ? 0 : kChunk * 2;
     static constexpr int kVnOff = kKnOff + kKnBytes;
-    static constexpr int kStageRaw = kVnOff + kChunk * 2;
+    static constexpr int kStageRaw = kVnOff + (TAB ? 0 : kChunk * 2);
     static constexpr int kStageAlign = (KB == 0) ? 1024 : 128;
     static constexpr int kStage = (kStageRaw + kStageAlign - 1) / kStageAlign * kStageAlign;
     static constexpr int kPipeBytes = kWarps * kStages * kStage;
@@ -173,17 +177,35 @@ struct BatchScan {
     }
 };
 
+// prmt byte tables (indexed by the 3-bit code kappa = sign << 2 | rank) from a
+// record's 8 fp16 values t_0..t_7 in ascending index order: code kappa < 4 is
+// index 4 + kappa, code 4 + r is index 3 - r.
+__device__ __forceinline__ Tables record_tables(const uint8_t* tab16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(tab16);
+    return Tables{prmt(w.z, w.w, 0x6420u), prmt(w.x, w.y, 0x0246u), prmt(w.z, w.w, 0x7531u),
+                  prmt(w.x, w.y, 0x1357u)};
+}
+
+// V tables of a table record.  Stage slots past the end of the context hold
+// stale bytes whose table could decode to inf or NaN, and a zero weight times
+// inf is NaN in the MMA, so those tokens get an all-zero table.
+template <bool FULL>
+__device__ __forceinline__ Tables v_tables(const uint8_t* rec, bool valid) {
+    if (FULL || valid) return record_tables(rec + 48);
+    return Tables{0u, 0u, 0u, 0u};
+}
+
 // One CTA: 4 warps over this CTA's chunk range, one unit segment at a time.
 // Per 16-token tile a warp runs
 //   S^T[16 tok x 8 rows]  = C_k[16 x 128] . Rot(q)^T      (8 k-steps per row tile)
 //   O^T[128 x 8 rows]    += C_v^T[128 x 16 tok] . (P n_v)^T (8 dim tiles)
 // with the tokens (M = 16) dequantised in registers: a thread owns tokens g and
 // g+8 of the tile and decodes its quarter t (32 dims) of both records.
-template <int KB, int VB, int NT>
-__global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
+template <int KB, int VB, int NT, bool TAB>
+__global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
     tq_decode_kernel(const __grid_constant__ DecodeParams p,
                      const __grid_constant__ CUtensorMap kmap) {
-    using C = DecCfg<KB, VB, NT>;
+    using C = DecCfg<KB, VB, NT, TAB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, derived from smem_raw by an integer offset so the
     // compiler keeps every access in the shared window (LDS, not generic loads)
@@ -251,19 +273,19 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
             const uint32_t dst = smem_u32(wpipe + st_idx * C::kStage);
             const uint32_t bar = bar0 + st_idx * 8;
             const uint32_t nb = static_cast<uint32_t>((nval + 7) & ~7) * 2;  // norms, 16-B multiple
-            uint32_t bytes = nval * C::kRbV + nb;
+            uint32_t bytes = nval * C::kRbV + (TAB ? 0u : nb);
             if (KB == 0) bytes += 2 * 4096;
-            else bytes += nval * C::kRbK + nb;
+            else bytes += nval * C::kRbK + (TAB ? 0u : nb);
             mbar_arrive_expect_tx(bar, bytes);
             if constexpr (KB == 0) {
                 tma_g2s_2d(dst, &kmap, 0, static_cast<int32_t>(row0 + tok0), bar);
                 tma_g2s_2d(dst + 4096, &kmap, 64, static_cast<int32_t>(row0 + tok0), bar);
             } else {
                 bulk_g2s(dst, p.k_codes + (row0 + tok0) * C::kRbK, nval * C::kRbK, bar);
-                bulk_g2s(dst + C::kKnOff, p.k_norm + row0 + tok0, nb, bar);
+                if (!TAB) bulk_g2s(dst + C::kKnOff, p.k_norm + row0 + tok0, nb, bar);
             }
             bulk_g2s(dst + C::kVOff, p.v_codes + (row0 + tok0) * C::kRbV, nval * C::kRbV, bar);
-            bulk_g2s(dst + C::kVnOff, p.v_norm + row0 + tok0, nb, bar);
+            if (!TAB) bulk_g2s(dst + C::kVnOff, p.v_norm + row0 + tok0, nb, bar);
         };
 
         if (lane == 0) {
@@ -372,8 +394,15 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
                         // A quad of k-step kc: (token g, dims 2kc), (token g+8, 2kc),
                         // (token g, 2kc+1), (token g+8, 2kc+1) in quarter-pair units
                         uint32_t aq[8][4];
-                        dequant_quarter_q<KB, 0>(st + (tile * 16 + g) * C::kRbK + t * (C::kRbK / 4), kt, aq);
-                        dequant_quarter_q<KB, 1>(st + (tile * 16 + g + 8) * C::kRbK + t * (C::kRbK / 4), kt, aq);
+                        const uint8_t* ra = st + (tile * 16 + g) * C::kRbK;
+                        const uint8_t* rb = st + (tile * 16 + g + 8) * C::kRbK;
+                        if constexpr (TAB) {
+                            dequant_quarter_q<KB, 0>(ra + t * C::kQuarterK, record_tables(ra + 48), aq);
+                            dequant_quarter_q<KB, 1>(rb + t * C::kQuarterK, record_tables(rb + 48), aq);
+                        } else {
+                            dequant_quarter_q<KB, 0>(ra + t * C::kQuarterK, kt, aq);
+                            dequant_quarter_q<KB, 1>(rb + t * C::kQuarterK, kt, aq);
+                        }
         #pragma unroll
                         for (int kc = 0; kc < 8; ++kc)
         #pragma unroll
@@ -391,12 +420,16 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
                 for (int tile = 0; tile < 2; ++tile) {
                     const int ta = tile * 16 + g, tb = ta + 8;
                     float ka = p.scale_log2e, kb2 = p.scale_log2e;
-                    if constexpr (KB != 0) {
+                    if constexpr (KB != 0 && !TAB) {  // table records carry the norm in their values
                         ka *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * ta));
                         kb2 *= __half2float(*reinterpret_cast<const __half*>(st + C::kKnOff + 2 * tb));
                     }
-                    nv[tile][0] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * ta));
-                    nv[tile][1] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * tb));
+                    if constexpr (TAB) {
+                        nv[tile][0] = nv[tile][1] = 1.f;
+                    } else {
+                        nv[tile][0] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * ta));
+                        nv[tile][1] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * tb));
+                    }
         #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         x[tile][n][0] *= ka; x[tile][n][1] *= ka;
@@ -499,7 +532,8 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
                     uint32_t vq[8][4];
                     {
                         uint32_t hv[16];
-                        dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g) * C::kRbV + t * (C::kRbV / 4), vt, hv);
+                        const uint8_t* rv = st + C::kVOff + (tile * 16 + g) * C::kRbV;
+                        dequant_quarter<VB>(rv + t * C::kQuarterV, TAB ? v_tables<FULL>(rv, tok0 + tile * 16 + g < t_end) : vt, hv);
         #pragma unroll
                         for (int mt = 0; mt < 8; ++mt) {
                             vq[mt][0] = movtrans(hv[2 * mt]);
@@ -508,7 +542,8 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT>::kMinCtas)
                     }
                     {
                         uint32_t hv[16];
-                        dequant_quarter<VB>(st + C::kVOff + (tile * 16 + g + 8) * C::kRbV + t * (C::kRbV / 4), vt, hv);
+                        const uint8_t* rv = st + C::kVOff + (tile * 16 + g + 8) * C::kRbV;
+                        dequant_quarter<VB>(rv + t * C::kQuarterV, TAB ? v_tables<FULL>(rv, tok0 + tile * 16 + g + 8 < t_end) : vt, hv);
         #pragma unroll
                         for (int mt = 0; mt < 8; ++mt) {
                             vq[mt][2] = movtrans(hv[2 * mt]);
@@ -735,20 +770,20 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
     *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(row) * kD + lane * 4) = out;
 }
 
-template <int KB, int VB, int NT>
+template <int KB, int VB, int NT, bool TAB = false>
 static int launch_decode_t(const DecodeParams& p, const CUtensorMap* kmap, cudaStream_t stream,
                            cudaEvent_t ev0, cudaEvent_t ev1) {
-    using C = DecCfg<KB, VB, NT>;
+    using C = DecCfg<KB, VB, NT, TAB>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tq_decode_kernel<KB, VB, NT>,
+        cudaError_t e = cudaFuncSetAttribute(tq_decode_kernel<KB, VB, NT, TAB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     dim3 grid(p.num_ctas);
     if (ev0) cudaEventRecord(ev0, stream);
-    cudaError_t e = launch_pdl(tq_decode_kernel<KB, VB, NT>, grid, dim3(C::kWarps * 32),
+    cudaError_t e = launch_pdl(tq_decode_kernel<KB, VB, NT, TAB>, grid, dim3(C::kWarps * 32),
                                C::kSmemAlloc, stream, p, *kmap);
     if (ev1) cudaEventRecord(ev1, stream);
     return e;
@@ -757,6 +792,10 @@ static int launch_decode_t(const DecodeParams& p, const CUtensorMap* kmap, cudaS
 template <int NT>
 static int launch_decode_nt(int kbits, int vbits, const DecodeParams& p, const CUtensorMap* kmap,
                             cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
+    if (p.table) {
+        if (kbits == 3 && vbits == 3) return launch_decode_t<3, 3, NT, true>(p, kmap, stream, ev0, ev1);
+        return cudaErrorInvalidValue;
+    }
     if (kbits == 16 && vbits == 4) return launch_decode_t<0, 4, NT>(p, kmap, stream, ev0, ev1);
     if (kbits == 3 && vbits == 3) return launch_decode_t<3, 3, NT>(p, kmap, stream, ev0, ev1);
     if (kbits == 4 && vbits == 4) return launch_decode_t<4, 4, NT>(p, kmap, stream, ev0, ev1);
@@ -777,15 +816,16 @@ int launch_combine(const CombineParams& p, cudaStream_t stream) {
     return launch_pdl(tq_combine_kernel, dim3((rows + 3) / 4), dim3(128), 0, stream, p);
 }
 
-template <int KB, int VB>
+template <int KB, int VB, bool TAB = false>
 static int smem_of(int nt) {
-    return nt == 1 ? DecCfg<KB, VB, 1>::kSmemAlloc : DecCfg<KB, VB, 2>::kSmemAlloc;
+    return nt == 1 ? DecCfg<KB, VB, 1, TAB>::kSmemAlloc : DecCfg<KB, VB, 2, TAB>::kSmemAlloc;
 }
 
-int decode_ctas_per_sm(int kbits, int vbits, int group_rows) {
+int decode_ctas_per_sm(int kbits, int vbits, int group_rows, bool table) {
     const int nt = group_rows <= 8 ? 1 : 2;
     int smem = 0;
-    if (kbits == 16) smem = vbits == 4 ? smem_of<0, 4>(nt) : smem_of<0, 3>(nt);
+    if (table) smem = smem_of<3, 3, true>(nt);
+    else if (kbits == 16) smem = vbits == 4 ? smem_of<0, 4>(nt) : smem_of<0, 3>(nt);
     else if (kbits == 3) smem = smem_of<3, 3>(nt);
     else smem = vbits == 4 ? smem_of<4, 4>(nt) : smem_of<4, 3>(nt);
     int by_smem = (228 * 1024) / (smem + 1024);  // 1 KB per CTA is reserved

@@ -195,11 +195,32 @@ __device__ __forceinline__ uint32_t quantize_code(float u, const float* gt, cons
 
 // Encode the vectors of one warp: 8 vectors, 4 lanes each; lane quarter q
 // holds dims 32q .. 32q+31.  `valid` marks lanes whose vector exists.
+// The record's norm (norm format) or, for table records (tcb != nullptr), the
+// eight fp16 values c_j * n16 after the 48 code bytes: c_j (fp32) times n16
+// (fp16) is exact in double, so each value is one rounding of the exact
+// product.
+__device__ __forceinline__ void store_norm(__half* dst_norm, uint8_t* dst, const float* tcb,
+                                           unsigned short nb) {
+    if (tcb == nullptr) {
+        dst_norm[0] = __ushort_as_half(nb);
+        return;
+    }
+    const double n = static_cast<double>(__half2float(__ushort_as_half(nb)));
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t a = __half_as_ushort(__double2half(static_cast<double>(tcb[2 * k]) * n));
+        const uint32_t b = __half_as_ushort(__double2half(static_cast<double>(tcb[2 * k + 1]) * n));
+        w[k] = a | (b << 16);
+    }
+    *reinterpret_cast<uint4*>(dst + 48) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 template <int BITS>
 __device__ __forceinline__ void encode_group(const __half* src, uint8_t* dst, __half* dst_norm,
-                                             const uint32_t (&signs)[4], const float* gt,
-                                             const float* ge, bool valid, uint32_t* status,
-                                             int q, unsigned gmask) {
+                                             const float* tcb, const uint32_t (&signs)[4],
+                                             const float* gt, const float* ge, bool valid,
+                                             uint32_t* status, int q, unsigned gmask) {
     float x[32];
     if (valid) {
         const uint4* s4 = reinterpret_cast<const uint4*>(src + q * 32);
@@ -228,7 +249,7 @@ __device__ __forceinline__ void encode_group(const __half* src, uint8_t* dst, __
     const float S32 = __shfl_sync(0xffffffffu, ss, 0, 4);   // one rounding order per group
     const unsigned short nb = norm_fp16(src, q, valid, S32, gmask);
     if (valid && q == 0) {
-        dst_norm[0] = __ushort_as_half(nb);
+        store_norm(dst_norm, dst, tcb, nb);
         if (nb >= 0x7C00u) atomicOr(status, kStatusNormOverflow);
     }
 
@@ -359,12 +380,14 @@ __global__ void __launch_bounds__(32 * kEncWarps)
                 for (int i = 0; i < 4; ++i) d4[i] = s4[i];
             }
         } else {
-            encode_group<KB>(src, p.k_codes + pos * (KB * 16), p.k_norm + pos, p.signs, p.k_gt,
-                             p.k_ge, valid, p.status, q, gmask);
+            encode_group<KB>(src, p.k_codes + pos * (p.table ? 64 : KB * 16), p.k_norm + pos,
+                             p.table ? p.k_cb : nullptr, p.signs, p.k_gt, p.k_ge, valid, p.status,
+                             q, gmask);
         }
     } else {
-        encode_group<VB>(src, p.v_codes + pos * (VB * 16), p.v_norm + pos, p.signs, p.v_gt,
-                         p.v_ge, valid, p.status, q, gmask);
+        encode_group<VB>(src, p.v_codes + pos * (p.table ? 64 : VB * 16), p.v_norm + pos,
+                         p.table ? p.v_cb : nullptr, p.signs, p.v_gt, p.v_ge, valid, p.status, q,
+                         gmask);
     }
 
     finish_append(p, gridDim.x * kEncWarps, lane);
@@ -375,9 +398,9 @@ __global__ void __launch_bounds__(32 * kEncWarps)
 // per lane is short.  Same arithmetic and output as encode_group.
 template <int BITS>
 __device__ __forceinline__ void encode_vector_warp(const __half* src, uint8_t* dst,
-                                                   __half* dst_norm, const uint32_t (&signs)[4],
-                                                   const float* gt, const float* ge,
-                                                   uint32_t* status, int lane) {
+                                                   __half* dst_norm, const float* tcb,
+                                                   const uint32_t (&signs)[4], const float* gt,
+                                                   const float* ge, uint32_t* status, int lane) {
     const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
     const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
     const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
@@ -404,7 +427,7 @@ __device__ __forceinline__ void encode_vector_warp(const __half* src, uint8_t* d
         nb = norm_to_half(S);
     }
     if (lane == 0) {
-        dst_norm[0] = __ushort_as_half(nb);
+        store_norm(dst_norm, dst, tcb, nb);
         if (nb >= 0x7C00u) atomicOr(status, kStatusNormOverflow);
     }
 
@@ -490,11 +513,13 @@ __global__ void __launch_bounds__(128) tq_encode_small_kernel(const __grid_const
                     reinterpret_cast<uint2*>(p.k_codes + pos * 256)[lane] =
                         reinterpret_cast<const uint2*>(src)[lane];
                 } else {
-                    encode_vector_warp<KB>(src, p.k_codes + pos * (KB * 16), p.k_norm + pos,
-                                           p.signs, p.k_gt, p.k_ge, p.status, lane);
+                    encode_vector_warp<KB>(src, p.k_codes + pos * (p.table ? 64 : KB * 16),
+                                           p.k_norm + pos, p.table ? p.k_cb : nullptr, p.signs,
+                                           p.k_gt, p.k_ge, p.status, lane);
                 }
             } else {
-                encode_vector_warp<VB>(src, p.v_codes + pos * (VB * 16), p.v_norm + pos, p.signs,
+                encode_vector_warp<VB>(src, p.v_codes + pos * (p.table ? 64 : VB * 16),
+                                       p.v_norm + pos, p.table ? p.v_cb : nullptr, p.signs,
                                        p.v_gt, p.v_ge, p.status, lane);
             }
         }

@@ -30,6 +30,7 @@ struct DecodeParams {
     int32_t num_ctas;         // decode grid (one wave of token-balanced CTAs)
     float scale_log2e;        // softmax scale * log2(e)
     float sparse_tau;         // sparse-V threshold on the softmax weight (0: off)
+    int32_t table;            // 1: records carry their centroid x norm table (no norms)
     uint32_t ktab[4];         // prmt byte tables of the K codebook (lo0, lo1, hi0, hi1)
     uint32_t vtab[4];
     uint32_t signs[4];        // bit d set <=> s_d = -1
@@ -61,6 +62,9 @@ struct EncodeParams {
     // decision thresholds on |u| over the positive half of the codebook:
     // a > tau_k  <=>  a >= gt[k];   a >= tau_k  <=>  a >= ge[k]   (fp32, exact)
     float k_gt[7], k_ge[7], v_gt[7], v_ge[7];
+    // table records: 48 bytes of 3-bit codes + fp16(c_j * n16), j = 0..7
+    int32_t table;
+    float k_cb[8], v_cb[8];
 };
 
 // Launchers (return a cudaError_t value).
@@ -71,7 +75,7 @@ int launch_combine(const CombineParams& p, cudaStream_t stream);
 int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stream);
 
 // Resident CTAs per SM of a decode variant (for the host split planner).
-int decode_ctas_per_sm(int kbits, int vbits, int group_rows);
+int decode_ctas_per_sm(int kbits, int vbits, int group_rows, bool table);
 
 // Query rows per row group for `rows` query rows of one KV head.
 inline int group_rows_for(int rows) { return rows <= 8 ? 8 : 16; }
@@ -95,6 +99,9 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Records that carry a centroid x norm table instead of a norm.
+inline bool mode_table(int mode) { return mode == TQ_TURBO3_TABLE; }
+
 // (K bits, V bits) of a mode; 16 = fp16 K.
 inline int mode_bits(int mode, int* kb, int* vb) {
     switch (mode) {
@@ -103,6 +110,7 @@ inline int mode_bits(int mode, int* kb, int* vb) {
         case TQ_TURBO4: *kb = 4; *vb = 4; return TQ_OK;
         case TQ_TURBO3_ASYM: *kb = 16; *vb = 3; return TQ_OK;
         case TQ_TURBO4K_3V: *kb = 4; *vb = 3; return TQ_OK;
+        case TQ_TURBO3_TABLE: *kb = 3; *vb = 3; return TQ_OK;
         default: return TQ_ERR_UNSUPPORTED;
     }
 }

@@ -123,10 +123,11 @@ extern "C" int tq_decode_attention_noalloc(const tq_cache* c, const void* q, int
     if (c->head_dim != kD) return TQ_ERR_UNSUPPORTED;
     if (c->batch <= 0 || c->num_kv_heads <= 0 || c->capacity <= 0 || (c->capacity % 16) != 0)
         return TQ_ERR_INVALID_ARG;
-    if (c->k_data == nullptr || c->v_data == nullptr || c->v_norm == nullptr ||
-        c->lengths == nullptr || (kb != 16 && c->k_norm == nullptr))
+    const bool table = tq::mode_table(c->mode);  // table records: no norm arrays
+    if (c->k_data == nullptr || c->v_data == nullptr || c->lengths == nullptr ||
+        (!table && (c->v_norm == nullptr || (kb != 16 && c->k_norm == nullptr))))
         return TQ_ERR_INVALID_ARG;
-    if (!aligned16(c->k_data) || !aligned16(c->v_data) || !aligned16(c->v_norm) ||
+    if (!aligned16(c->k_data) || !aligned16(c->v_data) || (c->v_norm && !aligned16(c->v_norm)) ||
         (c->k_norm && !aligned16(c->k_norm)))
         return TQ_ERR_INVALID_ARG;
     if (1ll * c->batch * c->num_kv_heads * c->capacity >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;
@@ -187,6 +188,7 @@ extern "C" int tq_decode_attention_noalloc(const tq_cache* c, const void* q, int
     p.cap = c->capacity;
     p.max_len = max_len_hint;
     p.num_ctas = ctas;
+    p.table = table ? 1 : 0;
     p.scale_log2e = ((scale == 0.f) ? 1.0f / std::sqrt(float(kD)) : scale) * 1.4426950408889634f;
     if (kb != 16) tables(c->codebook_k, kb, p.ktab);
     tables(c->codebook_v, vb, p.vtab);

@@ -15,7 +15,8 @@ BOUNDARY = 1e-5
 BOUNDARY_FRACTION = 1e-4
 
 MODE_BITS = {"turbo4_asym": (16, 4), "turbo3": (3, 3), "turbo4": (4, 4),
-             "turbo3_asym": (16, 3), "turbo4k_3v": (4, 3)}
+             "turbo3_asym": (16, 3), "turbo4k_3v": (4, 3), "turbo3_table": (3, 3)}
+TABLE_MODES = {"turbo3_table"}
 
 
 def attention_errors(got, want):
@@ -87,7 +88,8 @@ def gpu_cache_from_records(mode, B, Hkv, cap, lengths, kdata, knorm, vdata, vnor
     if c.k_norm is not None:
         c.k_norm.copy_(upload(knorm, device))
     c.v_data.copy_(upload(vdata, device))
-    c.v_norm.copy_(upload(vnorm, device))
+    if c.v_norm is not None:
+        c.v_norm.copy_(upload(vnorm, device))
     c.lengths.copy_(torch.from_numpy(np.asarray(lengths, np.int32)))
     return c
 
@@ -96,6 +98,17 @@ def random_cache(mode, B, Hkv, cap, key):
     """Random packed records straight from the input generator (numpy)."""
     kb, vb = MODE_BITS[mode]
     rows = B * Hkv * cap
+    if mode in TABLE_MODES:
+        # random 3-bit codes and tables built from random norms (the table is
+        # format data: values drawn from the generator, not computed by the kernels)
+        kcodes = wl.random_codes(key, rows, 48).reshape(B, Hkv, cap, 48)
+        vcodes = wl.random_codes(key + 1, rows, 48).reshape(B, Hkv, cap, 48)
+        cb = o.codebook(3)
+        kt = o.centroid_norm_table(wl.random_norms(key, rows).reshape(B, Hkv, cap), cb)
+        vt = o.centroid_norm_table(wl.random_norms(key + 1, rows).reshape(B, Hkv, cap), cb)
+        kdata = np.concatenate([kcodes, kt.astype("<f2").view(np.uint8)], axis=-1)
+        vdata = np.concatenate([vcodes, vt.astype("<f2").view(np.uint8)], axis=-1)
+        return kdata, None, vdata, None
     if kb == 16:
         kdata = wl.random_fp16(key, (B, Hkv, cap, 128))
         knorm = None
@@ -110,6 +123,10 @@ def random_cache(mode, B, Hkv, cap, key):
 def oracle_unit_from_records(mode, kdata, knorm, vdata, vnorm, b, h, L):
     """Oracle view of unit (b, h) of a record cache (the oracle unpacks the bytes)."""
     kb, vb = MODE_BITS[mode]
+    if mode in TABLE_MODES:
+        ki, kt = o.unpack_table_records(kdata[b, h, :L])
+        vi, vt = o.unpack_table_records(vdata[b, h, :L])
+        return {"k_idx": ki, "k_table": kt, "v_idx": vi, "v_table": vt}
     unit = {"v_idx": o.unpack_codes(vdata[b, h, :L], vb), "v_norm": vnorm[b, h, :L]}
     if kb == 16:
         unit["k"] = kdata[b, h, :L]

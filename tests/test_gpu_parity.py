@@ -65,6 +65,8 @@ DECODE_CASES = [
     ("turbo4k_3v", 3, 12, 4, [100, 513, 4000], 1, 4000, 0.0, 1.0),
     ("turbo4k_3v", 1, 32, 2, [777], 4, 784, 0.05, 1.0),         # 64 rows, custom scale
     ("turbo4", 40, 8, 2, [(37 * i) % 290 + 1 for i in range(40)], 1, 304, 0.0, 1.0),  # > 32 sequences
+    ("turbo3_table", 2, 8, 2, [37, 1300], 1, 1312, 0.0, 1.0),  # centroid x norm table records
+    ("turbo3_table", 1, 32, 8, [2049], 4, 2064, 0.0, 0.5),     # 16 rows, causal block
 ]
 
 
@@ -164,7 +166,8 @@ def _crafted_vectors():
 # T = 300 runs the warp-per-vector kernel (small appends), T = 700 the
 # four-lanes-per-vector kernel (more than 4096 vectors per stream)
 @pytest.mark.parametrize("T", [300, 700])
-@pytest.mark.parametrize("mode", ["turbo3", "turbo4", "turbo4_asym", "turbo3_asym", "turbo4k_3v"])
+@pytest.mark.parametrize("mode", ["turbo3", "turbo4", "turbo4_asym", "turbo3_asym", "turbo4k_3v",
+                                  "turbo3_table"])
 def test_encode_append_bit_exact(mode, T):
     kb, vb = H.MODE_BITS[mode]
     B, Hkv, cap = 2, 3, 720
@@ -192,8 +195,15 @@ def test_encode_append_bit_exact(mode, T):
                 assert np.array_equal(got_rec.view(np.float16), x[b])
                 continue
             idx, n16, u, ov = o.encode(x[b], o.codebook(bits), s)
-            got_n = norm[b, :, L0:L0 + T].cpu().numpy()
-            assert np.array_equal(got_n.view(np.uint16), n16.view(np.uint16)), (which, b)
+            if mode in H.TABLE_MODES:
+                # the record's table replaces the norm: bit-exact fp16 c_j * n16
+                want_t = o.centroid_norm_table(n16, o.codebook(bits))
+                got_t = np.ascontiguousarray(got_rec[..., 48:64]).view("<u2")
+                assert np.array_equal(got_t, want_t.view(np.uint16)), (which, b)
+                got_rec = np.ascontiguousarray(got_rec[..., :48])
+            else:
+                got_n = norm[b, :, L0:L0 + T].cpu().numpy()
+                assert np.array_equal(got_n.view(np.uint16), n16.view(np.uint16)), (which, b)
             got_idx = H.decode_records(got_rec, bits)
             dist = o.boundary_distance(u, o.codebook(bits))
             finite = ~ov[..., None] & np.ones_like(got_idx, bool)
@@ -244,7 +254,11 @@ def _e2e(mode, B, Hq, Hkv, L, Tq, cap, outliers_key):
         for h in range(Hkv):
             vi, vn, _, _ = o.encode(v[b, h], o.codebook(vb), s)
             u = {"v_idx": vi, "v_norm": vn}
-            if kb == 16:
+            if mode in H.TABLE_MODES:
+                ki, kn, _, _ = o.encode(k[b, h], o.codebook(kb), s)
+                u = {"k_idx": ki, "k_table": o.centroid_norm_table(kn, o.codebook(kb)),
+                     "v_idx": vi, "v_table": o.centroid_norm_table(vn, o.codebook(vb))}
+            elif kb == 16:
                 u["k"] = k[b, h]
             else:
                 ki, kn, _, _ = o.encode(k[b, h], o.codebook(kb), s)
@@ -261,6 +275,7 @@ def _e2e(mode, B, Hq, Hkv, L, Tq, cap, outliers_key):
     ("turbo3", 1, 32, 8, 600, 4, 608),
     ("turbo3_asym", 1, 28, 4, 900, 1, 912),
     ("turbo4k_3v", 2, 32, 8, 500, 2, 512),
+    ("turbo3_table", 1, 28, 4, 700, 1, 704),
 ])
 def test_end_to_end_own_encodings(mode, B, Hq, Hkv, L, Tq, cap):
     _e2e(mode, B, Hq, Hkv, L, Tq, cap, 400 + L)

@@ -51,7 +51,7 @@ def test_record_bytes(lib):
         tqf.tq_record_bytes(5)
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4, 5])
 @pytest.mark.parametrize("B,Hkv,rows,L", [(1, 2, 2, 256), (1, 4, 7, 8192), (1, 4, 7, 16384),
                                           (32, 8, 4, 32768), (4, 8, 16, 131072), (2, 2, 64, 777),
                                           (1, 1, 1, 1)])
@@ -118,7 +118,7 @@ def test_errors_unsupported_head_dim_and_mode(lib):
     assert _decode(lib, _cache(head_dim=96)) == tqf.TQ_ERR_UNSUPPORTED
     assert _append(lib, _cache(head_dim=256)) == tqf.TQ_ERR_UNSUPPORTED
     assert _decode(lib, _cache(mode=7)) == tqf.TQ_ERR_UNSUPPORTED
-    assert _decode(lib, _cache(mode=5)) == tqf.TQ_ERR_UNSUPPORTED
+    assert _decode(lib, _cache(mode=6)) == tqf.TQ_ERR_UNSUPPORTED
 
 
 def test_errors_gqa_and_shapes(lib):
@@ -145,6 +145,10 @@ def test_errors_pointers(lib):
     assert _decode(lib, _cache(mode=0, k_norm=None), q=None) == tqf.TQ_ERR_INVALID_ARG
     assert _decode(lib, _cache(mode=3, k_norm=None), q=None) == tqf.TQ_ERR_INVALID_ARG
     assert _decode(lib, _cache(mode=4, k_norm=None)) == tqf.TQ_ERR_INVALID_ARG   # 4-bit K needs them
+    assert _decode(lib, _cache(mode=1, v_norm=None)) == tqf.TQ_ERR_INVALID_ARG   # turbo3 needs V norms
+    # table records carry their norms: NULL norm arrays pass (rejected here only for q)
+    assert _decode(lib, _cache(mode=5, k_norm=None, v_norm=None), q=None) == tqf.TQ_ERR_INVALID_ARG
+    assert _append(lib, _cache(mode=5, k_norm=None, v_norm=None), k=None) == tqf.TQ_ERR_INVALID_ARG
 
 
 def test_errors_sparse_v_threshold(lib):
