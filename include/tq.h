@@ -161,6 +161,23 @@ int tq_decode_attention(tq_ctx **ctx, const tq_cache *cache, const void *q,
                         float scale, void *out, void *stream);
 
 /*
+ * Chunked-prefill attention: the same result as tq_decode_attention (query j
+ * of the Tq block attends to tokens [0, lengths[b] - tq + j]) for blocks of
+ * many queries, typically a prompt chunk just appended with tq_encode_append.
+ * The scores and P.V run on the 5th-generation tensor cores (tcgen05, fp32
+ * accumulators in tensor memory) over K/V tiles dequantised once per 128
+ * query rows.  (The pages' second workload: the 8K-prefill leg of the mlxcel
+ * measurement sweep, advisor commit of pull request #369.)
+ *   Arguments and layouts as tq_decode_attention; any tq >= 1 and any group
+ *   size up to 128 (num_q_heads / num_kv_heads); batch * num_kv_heads at most
+ *   65535.  TQ_TURBO3_TABLE is not supported (TQ_ERR_UNSUPPORTED).
+ *   The call allocates nothing beyond the context created on first use.
+ */
+int tq_prefill_attention(tq_ctx **ctx, const tq_cache *cache, const void *q,
+                         int32_t num_q_heads, int32_t tq, int32_t max_len_hint,
+                         float scale, void *out, void *stream);
+
+/*
  * Sparse-V decode: tq_decode_attention, except that a token whose softmax
  * weight is below tau adds nothing to the weighted sum of V (its weight still
  * counts in the normaliser).  This is the V skip of turboquant_plus

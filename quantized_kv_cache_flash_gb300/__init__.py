@@ -50,6 +50,9 @@ _SIGS = {
     "tq_decode_attention": (_c.c_int, [_c.POINTER(_c.c_void_p), _c.c_void_p, _c.c_void_p,
                                        _c.c_int32, _c.c_int32, _c.c_int32, _c.c_float,
                                        _c.c_void_p, _c.c_void_p]),
+    "tq_prefill_attention": (_c.c_int, [_c.POINTER(_c.c_void_p), _c.c_void_p, _c.c_void_p,
+                                        _c.c_int32, _c.c_int32, _c.c_int32, _c.c_float,
+                                        _c.c_void_p, _c.c_void_p]),
     "tq_decode_attention_sparse_v": (_c.c_int, [_c.POINTER(_c.c_void_p), _c.c_void_p,
                                                 _c.c_void_p, _c.c_int32, _c.c_int32, _c.c_int32,
                                                 _c.c_float, _c.c_float, _c.c_void_p,
@@ -243,6 +246,21 @@ def tq_decode_attention(ctx: Context, cache: Cache, q, out, max_len_hint: int,
                                      _ptr(q), int(q.shape[1]), int(q.shape[2]),
                                      int(max_len_hint), float(scale), _ptr(out),
                                      _stream(stream)), "tq_decode_attention")
+
+
+def tq_prefill_attention(ctx: Context, cache: Cache, q, out, max_len_hint: int,
+                         scale: float = 0.0, stream=None) -> None:
+    """Attention of a block of many queries q[B, Hq, Tq, 128] (a prefill chunk
+    already appended to the cache) on the tcgen05 tensor cores."""
+    import torch
+    if q.dtype != torch.float16 or not q.is_contiguous() or q.dim() != 4:
+        raise ValueError("q must be contiguous fp16 [B, Hq, Tq, 128]")
+    if out.dtype != torch.float16 or not out.is_contiguous() or out.shape != q.shape:
+        raise ValueError("out must be contiguous fp16 shaped like q")
+    _check(lib().tq_prefill_attention(ctypes.byref(ctx.ptr), ctypes.byref(cache.struct),
+                                      _ptr(q), int(q.shape[1]), int(q.shape[2]),
+                                      int(max_len_hint), float(scale), _ptr(out),
+                                      _stream(stream)), "tq_prefill_attention")
 
 
 def tq_decode_attention_sparse_v(ctx: Context, cache: Cache, q, out, max_len_hint: int,

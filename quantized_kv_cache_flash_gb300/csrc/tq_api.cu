@@ -488,6 +488,60 @@ int tq_decode_attention_sparse_v(tq_ctx** pctx, const tq_cache* c, const void* q
     return decode_impl(pctx, c, q, num_q_heads, tq_rows, max_len_hint, scale, tau, out, stream);
 }
 
+int tq_prefill_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_heads,
+                         int32_t tq_rows, int32_t max_len_hint, float scale, void* out,
+                         void* stream) {
+    int kb, vb;
+    int r = check_cache(c, &kb, &vb);
+    if (r != TQ_OK) return r;
+    if (tq::mode_table(c->mode)) return TQ_ERR_UNSUPPORTED;
+    if (q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+    if (tq_rows <= 0 || max_len_hint <= 0 || max_len_hint > c->capacity) return TQ_ERR_INVALID_ARG;
+    if (tq_rows > max_len_hint) return TQ_ERR_INVALID_ARG;
+    if (!(scale >= 0.f) || !std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
+    if (!std::isfinite(c->v_rescale)) return TQ_ERR_INVALID_ARG;
+    const int group = num_q_heads / c->num_kv_heads;
+    if (group > 128) return TQ_ERR_UNSUPPORTED;
+    const long long units = 1ll * c->batch * c->num_kv_heads;
+    if (units > 65535) return TQ_ERR_UNSUPPORTED;
+    const int pos_per_tile = 128 / group;
+    const long long mtiles = (tq_rows + pos_per_tile - 1) / pos_per_tile;
+    tq_ctx* ctx;
+    if ((r = get_ctx(pctx, &ctx)) != TQ_OK) return r;
+    if ((r = prepare_tables(ctx, c, kb, vb)) != TQ_OK) return r;
+    if (kb == 16 && (r = prepare_kmap(ctx, c)) != TQ_OK) return r;
+
+    tq::PrefillParams p{};
+    p.k_codes = static_cast<const uint8_t*>(c->k_data);
+    p.k_norm = static_cast<const __half*>(c->k_norm);
+    p.v_codes = static_cast<const uint8_t*>(c->v_data);
+    p.v_norm = static_cast<const __half*>(c->v_norm);
+    p.lengths = c->lengths;
+    p.q = static_cast<const __half*>(q);
+    p.out = static_cast<__half*>(out);
+    p.status = ctx->d_words;
+    p.batch = c->batch;
+    p.hkv = c->num_kv_heads;
+    p.hq = num_q_heads;
+    p.group = group;
+    p.tq = tq_rows;
+    p.cap = c->capacity;
+    p.max_len = max_len_hint;
+    p.pos_per_tile = pos_per_tile;
+    p.mtiles = int(mtiles);
+    const float sc = (scale == 0.f) ? 1.0f / std::sqrt(float(kD)) : scale;
+    p.scale_log2e = sc * 1.4426950408889634f;
+    p.v_rescale = c->v_rescale;
+    if (kb != 16) std::memcpy(p.ktab, ctx->ktab.tab, sizeof(p.ktab));
+    std::memcpy(p.vtab, ctx->vtab.tab, sizeof(p.vtab));
+    std::memcpy(p.signs, ctx->signs, sizeof(p.signs));
+    CUtensorMap dummy;
+    std::memset(&dummy, 0, sizeof(dummy));
+    r = tq::launch_prefill(kb, vb, p, kb == 16 ? &ctx->kmap : &dummy, static_cast<cudaStream_t>(stream));
+    return r == 0 ? TQ_OK : TQ_ERR_CUDA;
+}
+
 void tq_free(tq_ctx* ctx) {
     if (ctx == nullptr) return;
     int prev = 0;

@@ -67,6 +67,24 @@ struct EncodeParams {
     float k_cb[8], v_cb[8];
 };
 
+// Chunked-prefill attention (tcgen05) parameters.  One CTA = one (query
+// tile of pos_per_tile positions x group heads, batch * kv head).
+struct PrefillParams {
+    const uint8_t* k_codes;   // packed K codes, or fp16 K rows (read through the tensor map)
+    const __half* k_norm;
+    const uint8_t* v_codes;
+    const __half* v_norm;
+    const int32_t* lengths;   // [B]
+    const __half* q;          // [B, Hq, Tq, 128]
+    __half* out;              // [B, Hq, Tq, 128]
+    uint32_t* status;
+    int32_t batch, hkv, hq, group, tq, cap, max_len;
+    int32_t pos_per_tile;     // query positions per 128-row tile (128 / group)
+    int32_t mtiles;           // tiles per kv head
+    float scale_log2e, v_rescale;
+    uint32_t ktab[4], vtab[4], signs[4];
+};
+
 // Launchers (return a cudaError_t value).
 // group_rows (p.group_rows) selects the 8- or 16-row variant.
 int launch_decode(int kbits, int vbits, const DecodeParams& p, const CUtensorMap* kmap,
@@ -76,6 +94,8 @@ int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stre
 
 // Resident CTAs per SM of a decode variant (for the host split planner).
 int decode_ctas_per_sm(int kbits, int vbits, int group_rows, bool table);
+int launch_prefill(int kbits, int vbits, const PrefillParams& p, const CUtensorMap* kmap,
+                   cudaStream_t stream);
 
 // Query rows per row group for `rows` query rows of one KV head.
 inline int group_rows_for(int rows) { return rows <= 8 ? 8 : 16; }

@@ -178,3 +178,28 @@ def assert_within_skip_bound(got, full, bound, what=""):
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     assert float(excess.max()) <= MAX_ABS_REL * rms, f"{what}: max excess {excess.max():.3e}"
     assert math.sqrt(float(np.mean(excess * excess))) <= RMS_REL * rms, f"{what}: rms excess"
+
+
+def assert_attention_close_rows(got, want, what=""):
+    """The attention bounds applied to each output row (last axis) against that
+    row's own RMS, plus the RMS-error bound over the whole tensor.  For a
+    causal prefill block, whose rows range from a single visible token (an
+    output about as large as one V vector) to the whole context (an average,
+    an order of magnitude smaller), so that one tensor-wide RMS would be set
+    by the small rows alone."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    g = got.reshape(-1, got.shape[-1])
+    w = want.reshape(-1, want.shape[-1])
+    rms_row = np.sqrt(np.mean(w * w, axis=1))
+    err = np.abs(g - w)
+    zero = rms_row == 0
+    assert np.all(g[zero] == 0), f"{what}: rows without visible tokens must be 0"
+    live = ~zero
+    mx = err[live].max(axis=1) / rms_row[live]
+    rm = np.sqrt(np.mean(err[live] ** 2, axis=1)) / rms_row[live]
+    assert mx.max() <= MAX_ABS_REL, f"{what}: row max-abs {mx.max():.3e} x its rms"
+    assert rm.max() <= RMS_REL, f"{what}: row rms err {rm.max():.3e} x its rms"
+    rms = math.sqrt(float(np.mean(w * w)))
+    assert math.sqrt(float(np.mean(err * err))) <= RMS_REL * rms, f"{what}: rms err over the tensor"
