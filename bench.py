@@ -41,11 +41,31 @@ if ROOT not in sys.path:
 from quantized_kv_cache_flash_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "quantized-KV decode attention: effective HBM GB/s (% of peak), tokens/s"
+PROMPT_METRIC = "chunked-prefill attention over the packed cache: TFLOP/s (causal FLOPs), tokens/s"
 # bytes per token per kv head (K, V): packed record + fp16 norm, or fp16 K, or
 # a table record (codes + centroid x norm table, no norm)
 REC = {"turbo4_asym": (256, 66), "turbo3": (50, 50), "turbo4": (66, 66),
        "turbo3_asym": (256, 50), "turbo4k_3v": (66, 50), "turbo3_table": (64, 64)}
 L2_BYTES = 129 * 1024 * 1024
+
+
+def prompt_flops(w: wl.Workload) -> float:
+    """Algorithmic FLOPs of the causal attention of a Tq-token prompt into an
+    empty cache: query j sees j + 1 tokens; QK^T and PV are 2 * 128 FLOPs per
+    (row, visible token) each."""
+    vis = w.tq * (w.tq + 1) / 2
+    return 4.0 * 128 * w.batch * w.num_q_heads * vis
+
+
+def load_tensor_peak():
+    """Dense fp16 tensor peak: the measured bf16 cuBLAS figure (burst) --
+    fp16 and bf16 share the same nominal dense rate on this part."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured bf16_tflops (cuBLAS, burst) x 1.0 fp16/bf16"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def load_peaks():
@@ -138,16 +158,51 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle sample (run in a child process with one BLAS thread)
 # ---------------------------------------------------------------------------
+def oracle_prompt_sample(w: wl.Workload, budget_s: float, seed: int = 0):
+    """The oracle on prompt prefixes of one kv head at a time until budget_s is
+    spent: encode a 256-token prefix of K and V, then the causal attention of
+    all its G * 256 query rows.  Returns (FLOPs, seconds, units, description)."""
+    from oracle import tq_oracle as o
+    kb, vb = o.MODES[w.mode]
+    cbk, cbv = (o.codebook(kb) if kb else None), o.codebook(vb)
+    s = o.sign_vector(w.rot_seed)
+    G, T = w.group, 256
+    flops, units, t_spent, u = 0.0, 0, 0.0, 0
+    while t_spent < budget_s:
+        h = (u * 3 + seed) % w.num_kv_heads
+        u += 1
+        kx = wl.keys(w, 0, h, 0, T)
+        vx = wl.values(w, 0, h, 0, T)
+        q = wl.random_fp16(95000 + h + seed, (G, T, 128))
+        t0 = time.perf_counter()
+        vi, vn, _, _ = o.encode(vx, cbv, s)
+        unit = {"v_idx": vi, "v_norm": vn}
+        if kb is None:
+            unit["k"] = kx
+        else:
+            unit["k_idx"], unit["k_norm"], _, _ = o.encode(kx, cbk, s)
+        o.decode_unit(w.mode, q, unit, T, T, G, cbk, cbv, s, 1 / math.sqrt(128), 1.0)
+        t_spent += time.perf_counter() - t0
+        flops += 4.0 * 128 * G * T * (T + 1) / 2
+        units += 1
+    desc = (f"{units} kv heads, each: encode of a {T}-token prompt prefix (K and V) + causal "
+            f"attention of its {G * T} query rows, fp64 NumPy, 1 BLAS thread")
+    return flops, t_spent, units, desc
+
+
 def oracle_sample(wnum: int, budget_s: float, seed: int = 0, mode=None):
     """Run the oracle on (b, kv-head) units of the workload until budget_s is
     spent: append of the step's new token (encode) + decode over the unit's
     visible context, on a packed cache of random records.  Returns
-    (bytes, seconds, units, description)."""
+    (bytes, seconds, units, description); for a prompt workload FLOPs in place
+    of bytes."""
     import dataclasses
     from oracle import tq_oracle as o
     w = wl.by_number(wnum)
     if mode:
         w = dataclasses.replace(w, mode=mode)
+    if w.prompt:
+        return oracle_prompt_sample(w, budget_s, seed)
     lens = wl.lengths(w)
     kb, vb = o.MODES[w.mode]
     table = w.mode in o.TABLE_MODES
@@ -208,6 +263,9 @@ def run_cpu_baseline(wnum: int, budget_s: float, mode=None):
         return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
                 "sample": "failed: " + r.stderr.strip().splitlines()[-1][:200]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
+    if wl.by_number(wnum).prompt:
+        return {"value": d["bytes"] / d["seconds"] / 1e12, "unit": "TFLOP/s", "cores": 1,
+                "kind": "oracle", "sample": d["desc"], "seconds": round(d["seconds"], 2)}
     return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": 1,
             "kind": "oracle", "sample": d["desc"], "seconds": round(d["seconds"], 2)}
 
@@ -215,6 +273,114 @@ def run_cpu_baseline(wnum: int, budget_s: float, mode=None):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+def prompt_arm(args, rank, world, device_index):
+    """One step = append a Tq-token prompt to an empty cache (encode) and run
+    the causal attention of its Tq queries over it (tcgen05 prefill kernel)."""
+    import torch
+    import quantized_kv_cache_flash_gb300 as tqf
+    from quantized_kv_cache_flash_gb300 import build as tqbuild
+
+    tqbuild.build()
+    dev = torch.device("cuda", device_index)
+    torch.cuda.set_device(dev)
+    w = workload(args)
+    B, Hq, Hkv, T = w.batch, w.num_q_heads, w.num_kv_heads, w.tq
+    cap = int(math.ceil(T / 16) * 16)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed * 1000 + rank)
+    ch = torch.tensor(wl.outlier_channels(w), device=dev, dtype=torch.long)
+
+    def randn(shape, outl=False):
+        x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+        if outl and ch.numel():
+            x[..., ch] *= 8.0
+        return x.to(torch.float16)
+
+    ctx = tqf.Context()
+    cache = tqf.Cache(tqf.MODES[w.mode], B, Hkv, cap, dev, rot_seed=w.rot_seed)
+    k, v, q = randn((B, Hkv, T, 128), True), randn((B, Hkv, T, 128)), randn((B, Hq, T, 128))
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tqf.tq_encode_append(ctx, cache, k, v, stream)
+        tqf.tq_prefill_attention(ctx, cache, q, out, T, 0.0, stream)
+
+    steps, warm = args.steps, args.warmup
+    for _ in range(warm):
+        cache.lengths.zero_()
+        step()
+    torch.cuda.synchronize()
+    if tqf.tq_get_status(ctx) != 0:
+        raise RuntimeError("device status after the warm-up")
+    barrier(world)
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    clocks = ClockSampler(device_index)
+    clocks.start()
+    tqf.tq_set_kernel_timing(ctx, True)
+    tqf.tq_get_kernel_time(ctx)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
+    evs = []
+    for i in range(steps):
+        cache.lengths.zero_()
+        scratch.fill_(float(i))          # L2 flush between steps, outside the timed intervals
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in evs)
+    kern_ms, kern_n = tqf.tq_get_kernel_time(ctx)
+    tqf.tq_set_kernel_timing(ctx, False)
+    if tqf.tq_get_status(ctx) != 0:
+        raise RuntimeError("device status after the timed steps")
+    ms_max = reduce_max(world, ms)
+    flops = prompt_flops(w)
+    value = flops * steps * world / (ms_max * 1e-3) / 1e12
+    peak, peak_kind = load_tensor_peak()
+    achieved = flops / (kern_ms / kern_n * 1e-3) / 1e12 if kern_n else None
+
+    # end to end with host buffers: prompt K/V and q in, the output back
+    kh, vh, qh = k.cpu().pin_memory(), v.cpu().pin_memory(), q.cpu().pin_memory()
+    kd, vd, qd = torch.empty_like(k), torch.empty_like(v), torch.empty_like(q)
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e = 0.0
+    for i in range(steps):
+        cache.lengths.zero_()
+        f0.record(stream)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        qd.copy_(qh, non_blocking=True)
+        tqf.tq_encode_append(ctx, cache, kd, vd, stream)
+        tqf.tq_prefill_attention(ctx, cache, qd, out, T, 0.0, stream)
+        oh.copy_(out, non_blocking=True)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        e2e += f0.elapsed_time(f1)
+    e2e_ms = reduce_max(world, e2e)
+    h2d = k.numel() * 2 * 2 + q.numel() * 2
+    return {
+        "w": w, "value": value, "unit": "TFLOP/s", "prefill_encode": None, "ms": ms_max,
+        "tokens_per_s": B * T * steps * world / (ms_max * 1e-3), "step_bytes": float(h2d),
+        "clocks": clk,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": (achieved / peak) if achieved else None, "traffic": None,
+                     "kernel": "tq_prefill_kernel (tcgen05)",
+                     "kernel_ms": kern_ms / kern_n if kern_n else None,
+                     "kernel_flops": flops, "peak_kind": peak_kind},
+        "e2e": {"value": flops * steps * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(out.numel() * 2),
+                "ms_per_step": e2e_ms / steps},
+        "launches": 2 * steps,
+    }
+
+
 def gpu_arm(args, rank, world, device_index):
     import torch
     import quantized_kv_cache_flash_gb300 as tqf
@@ -492,15 +658,17 @@ def main():
             b, s, u, desc = oracle_sample(args.workload, per_step, seed=1000 + i, mode=args.mode)
             tb += b
             ts += s
-        v = tb / ts / 1e9
-        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
+        v = tb / ts / (1e12 if w.prompt else 1e9)
+        unit = "TFLOP/s" if w.prompt else "GB/s"
+        line = {"impl": "reference", "metric": PROMPT_METRIC if w.prompt else METRIC, "value": v,
+                "unit": unit,
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": ts / args.steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": config_dict(w, 0),
-                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "cpu_baseline": {"value": v, "unit": unit, "cores": 1, "kind": "oracle",
                                  "sample": "per step: " + desc},
-                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -510,13 +678,14 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
-    r = gpu_arm(args, rank, world, local)
+    r = (prompt_arm if w.prompt else gpu_arm)(args, rank, world, local)
     cpu = (run_cpu_baseline(args.workload, args.cpu_budget, args.mode)
            if (rank == 0 and world == 1) else None)
     if rank == 0:
         rf = r["roofline"]
         line = {
-            "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": world,
+            "metric": PROMPT_METRIC if w.prompt else METRIC, "value": r["value"],
+            "unit": r.get("unit", "GB/s"), "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16xf16->f32 (mma), fp32 softmax", "data": "synthetic",

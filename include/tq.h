@@ -252,10 +252,11 @@ int tq_plan_splits(int32_t mode, int32_t batch, int32_t num_kv_heads,
                    int32_t rows_per_kv_head, int32_t max_len_hint,
                    int32_t *split_tokens, int32_t *num_splits);
 
-/* Benchmark hook: when enabled, tq_decode_attention records CUDA events around
- * its main (split-K) kernel; tq_get_kernel_time synchronizes on the last event
- * and returns the summed milliseconds and the number of timed launches since
- * the last read (and resets both). */
+/* Benchmark hook: when enabled, tq_decode_attention (and its sparse-V form)
+ * records CUDA events around its main (split-K) kernel and
+ * tq_prefill_attention around its kernel; tq_get_kernel_time synchronizes on
+ * the last event and returns the summed milliseconds and the number of timed
+ * launches since the last read (and resets both). */
 int tq_set_kernel_timing(tq_ctx *ctx, int32_t enable);
 int tq_get_kernel_time(tq_ctx *ctx, float *ms_total, int32_t *launches);
 

@@ -248,6 +248,22 @@ int plan_ctas(int kb, int vb, bool table, int group_rows, long long units, int m
     return int(std::max<long long>(ctas, 1));
 }
 
+// The event pair bracketing the next timed launch (none when timing is off).
+int timing_events(tq_ctx* ctx, cudaEvent_t* e0, cudaEvent_t* e1) {
+    *e0 = *e1 = nullptr;
+    if (!ctx->timing) return TQ_OK;
+    if (ctx->events_used == ctx->events.size()) {
+        EventPair ep;
+        if (cudaEventCreate(&ep.a) != cudaSuccess || cudaEventCreate(&ep.b) != cudaSuccess)
+            return TQ_ERR_CUDA;
+        ctx->events.push_back(ep);
+    }
+    *e0 = ctx->events[ctx->events_used].a;
+    *e1 = ctx->events[ctx->events_used].b;
+    ctx->events_used++;
+    return TQ_OK;
+}
+
 int ensure_work(tq_ctx* ctx, size_t bytes) {
     if (ctx->work_bytes >= bytes) return TQ_OK;
     if (ctx->d_work) cudaFree(ctx->d_work);
@@ -436,17 +452,7 @@ int decode_impl(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_h
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
-    if (ctx->timing) {
-        if (ctx->events_used == ctx->events.size()) {
-            EventPair ep;
-            if (cudaEventCreate(&ep.a) != cudaSuccess || cudaEventCreate(&ep.b) != cudaSuccess)
-                return TQ_ERR_CUDA;
-            ctx->events.push_back(ep);
-        }
-        e0 = ctx->events[ctx->events_used].a;
-        e1 = ctx->events[ctx->events_used].b;
-        ctx->events_used++;
-    }
+    if ((r = timing_events(ctx, &e0, &e1)) != TQ_OK) return r;
     CUtensorMap dummy;
     std::memset(&dummy, 0, sizeof(dummy));
     r = tq::launch_decode(kb, vb, p, kb == 16 ? &ctx->kmap : &dummy, s, e0, e1);
@@ -538,7 +544,12 @@ int tq_prefill_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_
     std::memcpy(p.signs, ctx->signs, sizeof(p.signs));
     CUtensorMap dummy;
     std::memset(&dummy, 0, sizeof(dummy));
-    r = tq::launch_prefill(kb, vb, p, kb == 16 ? &ctx->kmap : &dummy, static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if ((r = timing_events(ctx, &e0, &e1)) != TQ_OK) return r;
+    if (e0) cudaEventRecord(e0, s);
+    r = tq::launch_prefill(kb, vb, p, kb == 16 ? &ctx->kmap : &dummy, s);
+    if (e1) cudaEventRecord(e1, s);
     return r == 0 ? TQ_OK : TQ_ERR_CUDA;
 }
 

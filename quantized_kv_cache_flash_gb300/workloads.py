@@ -43,6 +43,7 @@ class Workload:
     outliers: bool = True  # K has 4 channels scaled x8
     append: int = 0        # tokens appended per sequence inside each step
     prefill_chunk: int = 0 # tokens encoded per sequence as a separately timed chunk
+    prompt: bool = False   # a prompt of `tq` tokens appended to an empty cache, then attended
     rot_seed: int = 42
 
     @property
@@ -67,6 +68,11 @@ WORKLOADS = [
              32, 32, 8, 32768, context_min=16384, append=1),
     Workload(5, "long_turbo3_b4_hq32_hkv8_l131072_tq4_prefill4096", "turbo3",
              4, 32, 8, 131072, tq=4, prefill_chunk=4096),
+    # the 8K prefill leg of the pages' sweep at Qwen2.5-7B attention shape: an
+    # 8192-token prompt appended to an empty cache, then causal attention of
+    # all its queries over it
+    Workload(6, "qwen25_7b_turbo3_prompt8192_prefill", "turbo3", 1, 28, 4, 8192, tq=8192,
+             prompt=True),
 ]
 
 
