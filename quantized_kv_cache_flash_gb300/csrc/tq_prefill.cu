@@ -14,10 +14,13 @@
 // [dim][token]); the norms are applied per token in fp32, n_k to the scores
 // and n_v folded into P, as in the decode kernels.
 //
-// CTA = 128 threads on one (batch, kv head, tile of 128 query rows); thread i
-// owns row i (tensor-memory lane i) for the softmax.  Packed records of the
-// next tiles stream into two staging slots by bulk copies (fp16 K by 2-D
-// tensor-map copies straight into the MMA layout); every wait is bounded.
+// CTA = 256 threads on one (batch, kv head, tile of 128 query rows); row i
+// (tensor-memory lane i) belongs to two threads, one per 64-column half, for
+// the softmax.  The MMAs of a tile overlap the CUDA-core work around them:
+// S(n) runs while V(n) is dequantised, P.V(n) while K(n+1) is.  Packed
+// records of the next tiles stream into two staging slots by bulk copies
+// (fp16 K by 2-D tensor-map copies straight into the MMA layout); every wait
+// is bounded.
 #include <float.h>
 
 #include "tq_device.cuh"
@@ -42,8 +45,8 @@ struct PreCfg {
     static constexpr int kSVn = kTile * 2;
     static constexpr int kSlotRaw = kSK + kSKn + kSV + kSVn;
     static constexpr int kSlot = (kSlotRaw + 1023) / 1024 * 1024;
-    static constexpr int kColOff = kStgOff + 2 * kSlot;         // fp32 n_k[128] * scale, n_v[128]
-    static constexpr int kBarOff = kColOff + 2 * kTile * 4;     // stg[2], S, O mbarriers + TMEM slot
+    static constexpr int kColOff = kStgOff + 2 * kSlot;         // fp32 n_k[128], n_v[128], row max[2][128], sum[128]
+    static constexpr int kBarOff = kColOff + 5 * kTile * 4;     // stg[2], S, O mbarriers + TMEM slot
     static constexpr int kSmem = kBarOff + 64;
     static constexpr int kSmemAlloc = kSmem + 1024;             // base alignment slack
     static constexpr uint32_t kIdesc = umma_idesc_f16_f32(128, 128);
@@ -74,14 +77,16 @@ __device__ __forceinline__ void wht128_thread(float (&x)[128]) {
 }
 
 template <int KB, int VB>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     tq_prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap kmap) {
     using C = PreCfg<KB, VB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x;
     const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
-    const int lane = tid & 31;
+    // thread = (row r = TMEM lane, column half ch): warps 0-3 hold columns
+    // 0..63 of rows 0..127, warps 4-7 columns 64..127 of the same rows
+    const int r = tid & 127, ch = tid >> 7;
 
     // heaviest (latest) query tiles first
     const int mt = p.mtiles - 1 - static_cast<int>(blockIdx.x);
@@ -90,12 +95,12 @@ __global__ void __launch_bounds__(128, 1)
     griddep_wait();  // cache, lengths and q come from earlier work on the stream
     const int L = p.lengths[b];
     const int t_lim = min(L, p.max_len);
-    // this thread's row: query position j, head hl of the group
-    const int jl = tid / p.group, hl = tid - jl * p.group;
+    // row r: query position j, head hl of the group
+    const int jl = r / p.group, hl = r - jl * p.group;
     const int j = mt * p.pos_per_tile + jl;
     const bool row_ok = jl < p.pos_per_tile && j < p.tq;
     const int lim = row_ok ? min(L - p.tq + j, t_lim - 1) : -1;  // last visible token
-    // tiles: up to the last token any row sees; rows below lim_lo see every token of a tile
+    // tiles: up to the last token any row sees; rows see every token below lim_lo
     const int j_hi = min(p.tq - 1, (mt + 1) * p.pos_per_tile - 1);
     const int last = min(L - p.tq + j_hi, t_lim - 1);
     const int lim_lo = min(L - p.tq + mt * p.pos_per_tile, t_lim - 1);
@@ -105,7 +110,11 @@ __global__ void __launch_bounds__(128, 1)
     uint8_t* sQ = smem + C::kQOff;
     uint8_t* sP = smem + C::kPOff;
     uint8_t* sVt = smem + C::kVtOff;
-    const uint32_t bar_stg = smem_u32(smem + C::kBarOff);     // 2 x 8 bytes
+    float* colK = reinterpret_cast<float*>(smem + C::kColOff);  // n_k per token (1 for fp16 K)
+    float* colV = colK + C::kTile;                              // n_v per token
+    float* xmax = colV + C::kTile;                              // [2][128] partial row maxima
+    float* xsum = xmax + 2 * C::kTile;                          // [128] partial row sums (half 1)
+    const uint32_t bar_stg = smem_u32(smem + C::kBarOff);       // 2 x 8 bytes
     const uint32_t bar_s = bar_stg + 16, bar_o = bar_stg + 24;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 32);
 
@@ -142,7 +151,7 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 0) tmem_alloc(smem_u32(tslot), 256);  // S: columns 0..127, O: 128..255
 
     // ---- Q' = Rot(q) * scale * log2(e) (symmetric modes) or q * scale * log2(e) ----
-    {
+    if (ch == 0) {
         float x[128];
         if (row_ok) {
             const __half* qp = p.q + ((static_cast<size_t>(b) * p.hq + h * p.group + hl) * p.tq + j) * kD;
@@ -172,7 +181,7 @@ __global__ void __launch_bounds__(128, 1)
         }
 #pragma unroll
         for (int k = 0; k < 128; k += 8)
-            *reinterpret_cast<uint4*>(sQ + sw128_offset(tid, k)) =
+            *reinterpret_cast<uint4*>(sQ + sw128_offset(r, k)) =
                 make_uint4(pack_half2(x[k], x[k + 1]), pack_half2(x[k + 2], x[k + 3]),
                            pack_half2(x[k + 4], x[k + 5]), pack_half2(x[k + 6], x[k + 7]));
     }
@@ -180,143 +189,147 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t t_s = tmem, t_o = tmem + 128;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + 64 * ch;          // this thread's 64 columns of S
+    const uint32_t t_o = tmem + 128 + lane_off + 64 * ch;    // and of O
 
     const Tables kt{p.ktab[0], p.ktab[1], p.ktab[2], p.ktab[3]};
     const Tables vt{p.vtab[0], p.vtab[1], p.vtab[2], p.vtab[3]};
-    float m_base = -INFINITY, l_sum = 0.f;
+    float m_base = -INFINITY, l_part = 0.f;
     bool stalled = false;
-    int issued_s = 0, issued_o = 0;  // MMA batches committed (for the drain on a stall)
+    int issued_o = 0;  // P.V batches committed
 
+    // Per tile n: K(n) dequant -> S(n) MMA, overlapped with the V(n) dequant;
+    // softmax(n) -> P.V(n) MMA, overlapped with the K(n+1) dequant.
     for (int n = 0; n < ntiles && !stalled; ++n) {
         const int tok0 = n * C::kTile;
         uint8_t* slot = smem + C::kStgOff + (n & 1) * C::kSlot;
         if (!mbar_wait_bounded(bar_stg + 8 * (n & 1), (n >> 1) & 1)) stalled = true;
         if (__syncthreads_or(stalled)) { stalled = true; break; }
-        const bool tok_ok = tok0 + tid < t_lim;
 
-        // ---- K tile: thread = token; fp16 n * c[idx] into the MMA layout ----
+        // ---- K(n): thread = (token, half of the dims) ----
         uint8_t* sK = (KB == 0) ? slot : smem + C::kKOff;
-        float* colK = reinterpret_cast<float*>(smem + C::kColOff);
-        float* colV = colK + C::kTile;
         {
-            // per-token multipliers: K norm (1 for fp16 K), V norm; 0 past the end
-            const __half* vnorm = reinterpret_cast<const __half*>(slot + C::kSK + C::kSKn + C::kSV);
-            float nk = 1.f;
-            if constexpr (KB != 0) nk = __half2float(reinterpret_cast<const __half*>(slot + C::kSK)[tid]);
-            colK[tid] = tok_ok ? nk : 0.f;
-            colV[tid] = tok_ok ? __half2float(vnorm[tid]) : 0.f;
-        }
-        if constexpr (KB != 0) {
-            const uint8_t* rec = slot + tid * C::kRbK;
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                uint32_t hh[16];
-                dequant_q32<KB>(rec + qq * (C::kRbK / 4), kt, hh);
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    *reinterpret_cast<uint4*>(sK + sw128_offset(tid, 32 * qq + 8 * m)) =
-                        make_uint4(hh[4 * m], hh[4 * m + 1], hh[4 * m + 2], hh[4 * m + 3]);
+            const int tk = tid >> 1, hf = tid & 1;
+            const bool ok = tok0 + tk < t_lim;
+            if (hf == 0) {
+                const __half* vnorm = reinterpret_cast<const __half*>(slot + C::kSK + C::kSKn + C::kSV);
+                float nk = 1.f;
+                if constexpr (KB != 0) nk = __half2float(reinterpret_cast<const __half*>(slot + C::kSK)[tk]);
+                colK[tk] = ok ? nk : 0.f;
+                colV[tk] = ok ? __half2float(vnorm[tk]) : 0.f;
             }
-        }
-
-        // ---- V^T tile: thread = (token pair, half of the dims) ----
-        // (P.V of the previous tile must be done reading sVt and sP)
-        if (n > 0 && !mbar_wait_bounded(bar_o, (n - 1) & 1)) stalled = true;
-        {
-            const int pr = tid >> 1, dh = tid & 1;
-            const int ta = 2 * pr, tb = 2 * pr + 1;
-            const uint8_t* vrec = slot + C::kSK + C::kSKn;
-            // tokens past the end: their stale records still decode to finite
-            // centroids, and their weights are 0
+            if constexpr (KB != 0) {
+                const uint8_t* rec = slot + tk * C::kRbK;
 #pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
-                const int quarter = 2 * dh + qq;
-                uint32_t ha[16], hb[16];
-                dequant_q32<VB>(vrec + ta * C::kRbV + quarter * (C::kRbV / 4), vt, ha);
-                dequant_q32<VB>(vrec + tb * C::kRbV + quarter * (C::kRbV / 4), vt, hb);
+                for (int qq = 0; qq < 2; ++qq) {
+                    const int quarter = 2 * hf + qq;
+                    uint32_t hh[16];
+                    dequant_q32<KB>(rec + quarter * (C::kRbK / 4), kt, hh);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const uint32_t au = ha[k], cu = hb[k];
-                    const int d = 32 * quarter + 2 * k;
-                    // (token a, token b) of dims d and d + 1
-                    *reinterpret_cast<uint32_t*>(sVt + sw128_offset(d, ta)) = prmt(au, cu, 0x5410u);
-                    *reinterpret_cast<uint32_t*>(sVt + sw128_offset(d + 1, ta)) = prmt(au, cu, 0x7632u);
+                    for (int m = 0; m < 4; ++m)
+                        *reinterpret_cast<uint4*>(sK + sw128_offset(tk, 32 * quarter + 8 * m)) =
+                            make_uint4(hh[4 * m], hh[4 * m + 1], hh[4 * m + 2], hh[4 * m + 3]);
                 }
             }
         }
         fence_proxy_async();
         tc_fence_before();
-        if (__syncthreads_or(stalled)) { stalled = true; break; }
+        __syncthreads();
         tc_fence_after();
-
-        // ---- S = Q' . K^T ----
-        if (tid == 0) {
+        if (tid == 0) {  // S(n) = Q' . K(n)^T
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_f16(t_s, umma_desc_sw128(smem_u32(sQ) + koff), umma_desc_sw128(smem_u32(sK) + koff),
+                umma_f16(tmem, umma_desc_sw128(smem_u32(sQ) + koff), umma_desc_sw128(smem_u32(sK) + koff),
                          C::kIdesc, kk > 0 ? 1u : 0u);
             }
             umma_commit(bar_s);
-            // quantized K: the staging slot is consumed; refill it with tile n + 2
-            if (KB != 0 && n + 2 < ntiles) issue(n + 2);
         }
-        ++issued_s;
+
+        // ---- V(n)^T while S(n) runs: thread = (token pair, quarter of the dims) ----
+        // A warp covers 32 token pairs of one quarter, so each of its stores
+        // fills one whole 128-byte row of V^T (no bank conflicts).
+        // (P.V(n-1) must be done reading sVt and sP)
+        if (n > 0 && !mbar_wait_bounded(bar_o, (n - 1) & 1)) stalled = true;
+        {
+            const int pr = tid & 63, quarter = tid >> 6;
+            const int ta = 2 * pr, tb = 2 * pr + 1;
+            const uint8_t* vrec = slot + C::kSK + C::kSKn;
+            // tokens past the end: stale records still decode to finite
+            // centroids, and their weights are 0
+            uint32_t ha[16], hb[16];
+            dequant_q32<VB>(vrec + ta * C::kRbV + quarter * (C::kRbV / 4), vt, ha);
+            dequant_q32<VB>(vrec + tb * C::kRbV + quarter * (C::kRbV / 4), vt, hb);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int d = 32 * quarter + 2 * k;
+                // (token a, token b) of dims d and d + 1
+                *reinterpret_cast<uint32_t*>(sVt + sw128_offset(d, ta)) = prmt(ha[k], hb[k], 0x5410u);
+                *reinterpret_cast<uint32_t*>(sVt + sw128_offset(d + 1, ta)) = prmt(ha[k], hb[k], 0x7632u);
+            }
+        }
+        fence_proxy_async();
+
+        // ---- softmax(n): this thread's 64 columns of row r (log2 domain) ----
         if (!mbar_wait_bounded(bar_s, n & 1)) stalled = true;
         tc_fence_after();
-        if (KB == 0 && tid == 0 && n + 2 < ntiles && !stalled) issue(n + 2);  // fp16 K read by the MMA
-
-        // ---- softmax of this thread's row (log2 domain, lazy base) ----
-        float x[128];
+        float x[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
-            tmem_ld32(t_s + lane_off + 32 * c, v);
+            tmem_ld32(t_s + 32 * c, v);
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(v[e]);
         }
-        const bool full = tok0 + C::kTile - 1 <= lim_lo;  // every row sees every token
-        float mx = -INFINITY;
+        const int col0 = tok0 + 64 * ch;
+        if constexpr (KB != 0) {
 #pragma unroll
-        for (int e = 0; e < 128; e += 4) {
-            const float4 nk = *reinterpret_cast<const float4*>(colK + e);
-            if constexpr (KB != 0) {
+            for (int e = 0; e < 64; e += 4) {
+                const float4 nk = *reinterpret_cast<const float4*>(colK + 64 * ch + e);
                 x[e] *= nk.x; x[e + 1] *= nk.y; x[e + 2] *= nk.z; x[e + 3] *= nk.w;
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (!full && tok0 + e + i > lim) x[e + i] = -INFINITY;
-                mx = fmaxf(mx, x[e + i]);
-            }
         }
+        if (tok0 + C::kTile - 1 > lim_lo) {  // a tile some row sees only in part (uniform)
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+                if (col0 + e > lim) x[e] = -INFINITY;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) mx = fmaxf(mx, fmaxf(x[e], x[e + 1]));
+        xmax[ch * C::kTile + r] = mx;
+        // every thread is past its V(n) reads: the staging slot is free once S(n)
+        // (which reads fp16 K from it) is done, i.e. now
+        if (__syncthreads_or(stalled)) { stalled = true; break; }
+        if (tid == 0 && n + 2 < ntiles) issue(n + 2);
+        mx = fmaxf(mx, xmax[(ch ^ 1) * C::kTile + r]);
         // the base moves only when a score passes it by more than 4 (so p <= 16
         // and p * n_v stays finite in fp16 for V norms below 4094)
         const bool grow = mx > m_base + 4.f;
-        if (__any_sync(0xffffffffu, grow)) {
+        if (__any_sync(0xffffffffu, grow)) {  // the same decision in both halves of a row
             const float nb_ = grow ? mx : m_base;
             const float alpha = (m_base == -INFINITY || !grow) ? (grow ? 0.f : 1.f) : fast_exp2(m_base - nb_);
-            l_sum *= alpha;
+            l_part *= alpha;
             m_base = nb_;
-            if (issued_o > 0) {  // rescale this row of O in tensor memory
+            if (issued_o > 0) {  // rescale this thread's half row of O in tensor memory
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t v[32];
-                    tmem_ld32(t_o + lane_off + 32 * c, v);
+                    tmem_ld32(t_o + 32 * c, v);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                    tmem_st32(t_o + lane_off + 32 * c, v);
+                    tmem_st32(t_o + 32 * c, v);
                 }
             }
         }
         const float base = (m_base == -INFINITY) ? 0.f : m_base;
         float s = 0.f;
 #pragma unroll
-        for (int k = 0; k < 128; k += 8) {
+        for (int k = 0; k < 64; k += 8) {
             float pv[8];
-            const float4 na = *reinterpret_cast<const float4*>(colV + k);
-            const float4 nb = *reinterpret_cast<const float4*>(colV + k + 4);
+            const float4 na = *reinterpret_cast<const float4*>(colV + 64 * ch + k);
+            const float4 nb = *reinterpret_cast<const float4*>(colV + 64 * ch + k + 4);
             const float nv[8] = {na.x, na.y, na.z, na.w, nb.x, nb.y, nb.z, nb.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -324,44 +337,42 @@ __global__ void __launch_bounds__(128, 1)
                 s += pe;
                 pv[e] = pe * nv[e];
             }
-            *reinterpret_cast<uint4*>(sP + sw128_offset(tid, k)) =
+            *reinterpret_cast<uint4*>(sP + sw128_offset(r, 64 * ch + k)) =
                 make_uint4(pack_half2(pv[0], pv[1]), pack_half2(pv[2], pv[3]),
                            pack_half2(pv[4], pv[5]), pack_half2(pv[6], pv[7]));
         }
-        l_sum += s;
+        l_part += s;
         fence_proxy_async();
         tc_fence_before();
         if (__syncthreads_or(stalled)) { stalled = true; break; }
         tc_fence_after();
-
-        // ---- O += P . V ----
-        if (tid == 0) {
+        if (tid == 0) {  // O += P(n) . V(n)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_f16(t_o, umma_desc_sw128(smem_u32(sP) + koff), umma_desc_sw128(smem_u32(sVt) + koff),
-                         C::kIdesc, (n > 0 || kk > 0) ? 1u : 0u);
+                umma_f16(tmem + 128, umma_desc_sw128(smem_u32(sP) + koff),
+                         umma_desc_sw128(smem_u32(sVt) + koff), C::kIdesc, (n > 0 || kk > 0) ? 1u : 0u);
             }
             umma_commit(bar_o);
         }
         ++issued_o;
     }
 
-    // ---- epilogue: O / l, v_rescale, inverse rotation, fp16 ----
+    // ---- epilogue: O / l, v_rescale, inverse rotation, fp16 (half 0 of each row) ----
+    if (ch == 1) xsum[r] = l_part;
     bool ok = !stalled;
     if (issued_o > 0 && !mbar_wait_bounded(bar_o, (issued_o - 1) & 1)) ok = false;
     ok = __syncthreads_and(ok) != 0;  // one decision for the whole CTA
     tc_fence_after();
     if (!ok) {
         if (tid == 0) atomicOr(p.status, kStatusPipelineStall);
-    } else {
-        // every lane of every warp takes part in the (warp-collective) loads
+    } else if (ch == 0) {  // warps 0-3, every lane: the loads are warp-collective
         float o[128];
         if (issued_o > 0) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
-                tmem_ld32(t_o + lane_off + 32 * c, v);
+                tmem_ld32(tmem + 128 + lane_off + 32 * c, v);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[32 * c + e] = __uint_as_float(v[e]);
             }
@@ -369,31 +380,32 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
             for (int e = 0; e < 128; ++e) o[e] = 0.f;
         }
-      if (row_ok) {
-        float inv = 0.f;
-        if (l_sum > 0.f) inv = p.v_rescale / l_sum;
-        else atomicOr(p.status, kStatusShortContext);
+        if (row_ok) {
+            const float l_sum = l_part + xsum[r];
+            float inv = 0.f;
+            if (l_sum > 0.f) inv = p.v_rescale / l_sum;
+            else atomicOr(p.status, kStatusShortContext);
 #pragma unroll
-        for (int e = 0; e < 128; ++e) o[e] *= inv;
-        wht128_thread(o);
-        __half* op = p.out + ((static_cast<size_t>(b) * p.hq + h * p.group + hl) * p.tq + j) * kD;
+            for (int e = 0; e < 128; ++e) o[e] *= inv;
+            wht128_thread(o);
+            __half* op = p.out + ((static_cast<size_t>(b) * p.hq + h * p.group + hl) * p.tq + j) * kD;
 #pragma unroll
-        for (int k = 0; k < 128; k += 8) {
-            float y[8];
+            for (int k = 0; k < 128; k += 8) {
+                float y[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float v = o[k + e] * 0.08838834764831845f;
-                y[e] = ((p.signs[(k + e) >> 5] >> ((k + e) & 31)) & 1u) ? -v : v;
+                for (int e = 0; e < 8; ++e) {
+                    const float v = o[k + e] * 0.08838834764831845f;
+                    y[e] = ((p.signs[(k + e) >> 5] >> ((k + e) & 31)) & 1u) ? -v : v;
+                }
+                *reinterpret_cast<uint4*>(op + k) = make_uint4(pack_half2(y[0], y[1]), pack_half2(y[2], y[3]),
+                                                               pack_half2(y[4], y[5]), pack_half2(y[6], y[7]));
             }
-            *reinterpret_cast<uint4*>(op + k) = make_uint4(pack_half2(y[0], y[1]), pack_half2(y[2], y[3]),
-                                                           pack_half2(y[4], y[5]), pack_half2(y[6], y[7]));
-        }
-      }  // padding rows of the tile write nothing
+        }  // padding rows of the tile write nothing
     }
     if (!ok) {
-        // let every copy still in flight land before the shared memory goes away
-        for (int n = issued_s; n < ntiles && n < issued_s + 2; ++n)
-            (void)mbar_wait_bounded(bar_stg + 8 * (n & 1), (n >> 1) & 1);
+        // let the copies still in flight land before the shared memory goes away
+        for (int n = 0; n < 2 && n < ntiles; ++n)
+            (void)mbar_wait_bounded(bar_stg + 8 * (n & 1), 0);
     }
     tc_fence_before();
     __syncthreads();
@@ -410,7 +422,7 @@ static int launch_prefill_t(const PrefillParams& p, const CUtensorMap* kmap, cud
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_pdl(tq_prefill_kernel<KB, VB>, dim3(p.mtiles, p.batch * p.hkv), dim3(128),
+    return launch_pdl(tq_prefill_kernel<KB, VB>, dim3(p.mtiles, p.batch * p.hkv), dim3(256),
                       C::kSmemAlloc, stream, p, *kmap);
 }
 
