@@ -14,13 +14,14 @@
 // [dim][token]); the norms are applied per token in fp32, n_k to the scores
 // and n_v folded into P, as in the decode kernels.
 //
-// CTA = 256 threads on one (batch, kv head, tile of 128 query rows); row i
-// (tensor-memory lane i) belongs to two threads, one per 64-column half, for
-// the softmax.  The MMAs of a tile overlap the CUDA-core work around them:
-// S(n) runs while V(n) is dequantised, P.V(n) while K(n+1) is.  Packed
-// records of the next tiles stream into two staging slots by bulk copies
-// (fp16 K by 2-D tensor-map copies straight into the MMA layout); every wait
-// is bounded.
+// CTA = 256 threads on one (batch, kv head, pair of 128-row query tiles):
+// thread = one query row (tensor-memory lane) of one tile, so each K/V tile is
+// dequantised once for 256 rows.  Tensor memory holds, per query tile, S (128
+// columns, whose first 64 take P back as fp16 pairs for the P.V MMA) and O
+// (128 columns): all 512.  The MMAs overlap the CUDA-core work: P.V(n-1)
+// runs while K(n) is dequantised, S(n) while V(n) is.  Packed records of the
+// next tiles stream into two staging slots by bulk copies (fp16 K by 2-D
+// tensor-map copies straight into the MMA layout); every wait is bounded.
 #include <float.h>
 
 #include "tq_device.cuh"
@@ -33,8 +34,7 @@ struct PreCfg {
     static constexpr int kTile = 128;                           // tokens per tile = rows per CTA
     static constexpr int kRbK = (KB == 0) ? 256 : KB * 16;
     static constexpr int kRbV = VB * 16;
-    static constexpr int kQOff = 0;                             // fp16 Q' (32 KB)
-    static constexpr int kPOff = 32768;                         // fp16 P [row][token] (32 KB)
+    static constexpr int kQOff = 0;                             // fp16 Q' of the two query tiles (64 KB)
     static constexpr int kVtOff = 65536;                        // fp16 V^T [dim][token] (32 KB)
     static constexpr int kKOff = 98304;                         // fp16 K [token][dim] (quantized K)
     static constexpr int kStgOff = kKOff + ((KB == 0) ? 0 : 32768);
@@ -45,8 +45,8 @@ struct PreCfg {
     static constexpr int kSVn = kTile * 2;
     static constexpr int kSlotRaw = kSK + kSKn + kSV + kSVn;
     static constexpr int kSlot = (kSlotRaw + 1023) / 1024 * 1024;
-    static constexpr int kColOff = kStgOff + 2 * kSlot;         // fp32 n_k[128], n_v[128], row max[2][128], sum[128]
-    static constexpr int kBarOff = kColOff + 5 * kTile * 4;     // stg[2], S, O mbarriers + TMEM slot
+    static constexpr int kColOff = kStgOff + 2 * kSlot;         // fp32 n_k[128], n_v[128]
+    static constexpr int kBarOff = kColOff + 2 * kTile * 4;     // stg[2], S, O mbarriers + TMEM slot
     static constexpr int kSmem = kBarOff + 64;
     static constexpr int kSmemAlloc = kSmem + 1024;             // base alignment slack
     static constexpr uint32_t kIdesc = umma_idesc_f16_f32(128, 128);
@@ -84,36 +84,35 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x;
     const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
-    // thread = (row r = TMEM lane, column half ch): warps 0-3 hold columns
-    // 0..63 of rows 0..127, warps 4-7 columns 64..127 of the same rows
-    const int r = tid & 127, ch = tid >> 7;
+    // thread = (query tile tl of the CTA's two, row r = TMEM lane): warps 0-3
+    // hold the rows of the first tile, warps 4-7 those of the second
+    const int tl = tid >> 7, r = tid & 127;
 
     // heaviest (latest) query tiles first
-    const int mt = p.mtiles - 1 - static_cast<int>(blockIdx.x);
+    const int npairs = (p.mtiles + 1) / 2;
+    const int pair = npairs - 1 - static_cast<int>(blockIdx.x);
+    const int mt = 2 * pair + tl;
     const int unit = blockIdx.y;  // b * hkv + h
     const int b = unit / p.hkv, h = unit - b * p.hkv;
     griddep_wait();  // cache, lengths and q come from earlier work on the stream
     const int L = p.lengths[b];
     const int t_lim = min(L, p.max_len);
-    // row r: query position j, head hl of the group
+    // row r of tile mt: query position j, head hl of the group
     const int jl = r / p.group, hl = r - jl * p.group;
     const int j = mt * p.pos_per_tile + jl;
-    const bool row_ok = jl < p.pos_per_tile && j < p.tq;
+    const bool row_ok = mt < p.mtiles && jl < p.pos_per_tile && j < p.tq;
     const int lim = row_ok ? min(L - p.tq + j, t_lim - 1) : -1;  // last visible token
-    // tiles: up to the last token any row sees; rows see every token below lim_lo
-    const int j_hi = min(p.tq - 1, (mt + 1) * p.pos_per_tile - 1);
+    // this tile's rows see every token up to lim_lo; the CTA's tiles end at `last`
+    const int lim_lo = mt < p.mtiles ? min(L - p.tq + mt * p.pos_per_tile, t_lim - 1) : -1;
+    const int j_hi = min(p.tq - 1, (2 * pair + 2) * p.pos_per_tile - 1);
     const int last = min(L - p.tq + j_hi, t_lim - 1);
-    const int lim_lo = min(L - p.tq + mt * p.pos_per_tile, t_lim - 1);
     const int ntiles = last >= 0 ? last / C::kTile + 1 : 0;
     const size_t row0 = static_cast<size_t>(unit) * p.cap;
 
-    uint8_t* sQ = smem + C::kQOff;
-    uint8_t* sP = smem + C::kPOff;
+    uint8_t* sQ = smem + C::kQOff;       // [2][128 x 128] fp16
     uint8_t* sVt = smem + C::kVtOff;
     float* colK = reinterpret_cast<float*>(smem + C::kColOff);  // n_k per token (1 for fp16 K)
     float* colV = colK + C::kTile;                              // n_v per token
-    float* xmax = colV + C::kTile;                              // [2][128] partial row maxima
-    float* xsum = xmax + 2 * C::kTile;                          // [128] partial row sums (half 1)
     const uint32_t bar_stg = smem_u32(smem + C::kBarOff);       // 2 x 8 bytes
     const uint32_t bar_s = bar_stg + 16, bar_o = bar_stg + 24;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 32);
@@ -148,10 +147,13 @@ __global__ void __launch_bounds__(256, 1)
         fence_barrier_init();
         for (int n = 0; n < 2 && n < ntiles; ++n) issue(n);
     }
-    if (warp == 0) tmem_alloc(smem_u32(tslot), 256);  // S: columns 0..127, O: 128..255
+    // tensor memory: tile t at columns 256 t: S (128, its first 64 reused for
+    // P as fp16 pairs), then O (128)
+    if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
 
     // ---- Q' = Rot(q) * scale * log2(e) (symmetric modes) or q * scale * log2(e) ----
-    if (ch == 0) {
+    uint8_t* sQt = sQ + tl * 32768;
+    {
         float x[128];
         if (row_ok) {
             const __half* qp = p.q + ((static_cast<size_t>(b) * p.hq + h * p.group + hl) * p.tq + j) * kD;
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(256, 1)
         }
 #pragma unroll
         for (int k = 0; k < 128; k += 8)
-            *reinterpret_cast<uint4*>(sQ + sw128_offset(r, k)) =
+            *reinterpret_cast<uint4*>(sQt + sw128_offset(r, k)) =
                 make_uint4(pack_half2(x[k], x[k + 1]), pack_half2(x[k + 2], x[k + 3]),
                            pack_half2(x[k + 4], x[k + 5]), pack_half2(x[k + 6], x[k + 7]));
     }
@@ -190,17 +192,18 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + 64 * ch;          // this thread's 64 columns of S
-    const uint32_t t_o = tmem + 128 + lane_off + 64 * ch;    // and of O
+    const uint32_t t_s = tmem + 256 * tl + lane_off;         // this row of S (and of P)
+    const uint32_t t_o = tmem + 256 * tl + 128 + lane_off;   // this row of O
 
     const Tables kt{p.ktab[0], p.ktab[1], p.ktab[2], p.ktab[3]};
     const Tables vt{p.vtab[0], p.vtab[1], p.vtab[2], p.vtab[3]};
-    float m_base = -INFINITY, l_part = 0.f;
+    float m_base = -INFINITY, l_sum = 0.f;
     bool stalled = false;
     int issued_o = 0;  // P.V batches committed
 
-    // Per tile n: K(n) dequant -> S(n) MMA, overlapped with the V(n) dequant;
-    // softmax(n) -> P.V(n) MMA, overlapped with the K(n+1) dequant.
+    // Per tile n: K(n) dequant (overlaps P.V(n-1)); S(n) for both query tiles
+    // (overlaps the V(n) dequant); softmax(n) writes P into tensor memory over
+    // S; P.V(n).
     for (int n = 0; n < ntiles && !stalled; ++n) {
         const int tok0 = n * C::kTile;
         uint8_t* slot = smem + C::kStgOff + (n & 1) * C::kSlot;
@@ -237,21 +240,24 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) {  // S(n) = Q' . K(n)^T
+        // P.V(n-1) reads P over the S columns and V^T: both reused from here on
+        if (n > 0 && !mbar_wait_bounded(bar_o, (n - 1) & 1)) stalled = true;
+        tc_fence_after();
+        if (tid == 0 && !stalled) {  // S_t(n) = Q'_t . K(n)^T for both tiles
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_f16(tmem, umma_desc_sw128(smem_u32(sQ) + koff), umma_desc_sw128(smem_u32(sK) + koff),
-                         C::kIdesc, kk > 0 ? 1u : 0u);
-            }
+            for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    umma_f16(tmem + 256 * t2, umma_desc_sw128(smem_u32(sQ) + t2 * 32768 + koff),
+                             umma_desc_sw128(smem_u32(sK) + koff), C::kIdesc, kk > 0 ? 1u : 0u);
+                }
             umma_commit(bar_s);
         }
 
-        // ---- V(n)^T while S(n) runs: thread = (token pair, quarter of the dims) ----
-        // A warp covers 32 token pairs of one quarter, so each of its stores
-        // fills one whole 128-byte row of V^T (no bank conflicts).
-        // (P.V(n-1) must be done reading sVt and sP)
-        if (n > 0 && !mbar_wait_bounded(bar_o, (n - 1) & 1)) stalled = true;
+        // ---- V(n)^T while S(n) runs: thread = (token pair, quarter of the dims);
+        // a warp covers 32 token pairs of one quarter: each store fills whole
+        // 128-byte rows of V^T ----
         {
             const int pr = tid & 63, quarter = tid >> 6;
             const int ta = 2 * pr, tb = 2 * pr + 1;
@@ -271,50 +277,43 @@ __global__ void __launch_bounds__(256, 1)
         }
         fence_proxy_async();
 
-        // ---- softmax(n): this thread's 64 columns of row r (log2 domain) ----
+        // ---- softmax(n): this thread's row of its tile (log2 domain) ----
         if (!mbar_wait_bounded(bar_s, n & 1)) stalled = true;
         tc_fence_after();
-        float x[64];
+        float x[128];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 4; ++c) {
             uint32_t v[32];
             tmem_ld32(t_s + 32 * c, v);
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(v[e]);
         }
-        const int col0 = tok0 + 64 * ch;
         if constexpr (KB != 0) {
 #pragma unroll
-            for (int e = 0; e < 64; e += 4) {
-                const float4 nk = *reinterpret_cast<const float4*>(colK + 64 * ch + e);
+            for (int e = 0; e < 128; e += 4) {
+                const float4 nk = *reinterpret_cast<const float4*>(colK + e);
                 x[e] *= nk.x; x[e + 1] *= nk.y; x[e + 2] *= nk.z; x[e + 3] *= nk.w;
             }
         }
-        if (tok0 + C::kTile - 1 > lim_lo) {  // a tile some row sees only in part (uniform)
+        if (tok0 + C::kTile - 1 > lim_lo) {  // a tile some row of this query tile sees in part
 #pragma unroll
-            for (int e = 0; e < 64; ++e)
-                if (col0 + e > lim) x[e] = -INFINITY;
+            for (int e = 0; e < 128; ++e)
+                if (tok0 + e > lim) x[e] = -INFINITY;
         }
         float mx = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) mx = fmaxf(mx, fmaxf(x[e], x[e + 1]));
-        xmax[ch * C::kTile + r] = mx;
-        // every thread is past its V(n) reads: the staging slot is free once S(n)
-        // (which reads fp16 K from it) is done, i.e. now
-        if (__syncthreads_or(stalled)) { stalled = true; break; }
-        if (tid == 0 && n + 2 < ntiles) issue(n + 2);
-        mx = fmaxf(mx, xmax[(ch ^ 1) * C::kTile + r]);
+        for (int e = 0; e < 128; e += 2) mx = fmaxf(mx, fmaxf(x[e], x[e + 1]));
         // the base moves only when a score passes it by more than 4 (so p <= 16
         // and p * n_v stays finite in fp16 for V norms below 4094)
         const bool grow = mx > m_base + 4.f;
-        if (__any_sync(0xffffffffu, grow)) {  // the same decision in both halves of a row
+        if (__any_sync(0xffffffffu, grow)) {
             const float nb_ = grow ? mx : m_base;
             const float alpha = (m_base == -INFINITY || !grow) ? (grow ? 0.f : 1.f) : fast_exp2(m_base - nb_);
-            l_part *= alpha;
+            l_sum *= alpha;
             m_base = nb_;
-            if (issued_o > 0) {  // rescale this thread's half row of O in tensor memory
+            if (issued_o > 0) {  // rescale this row of O in tensor memory (P.V(n-1) is done)
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t v[32];
                     tmem_ld32(t_o + 32 * c, v);
 #pragma unroll
@@ -326,53 +325,53 @@ __global__ void __launch_bounds__(256, 1)
         const float base = (m_base == -INFINITY) ? 0.f : m_base;
         float s = 0.f;
 #pragma unroll
-        for (int k = 0; k < 64; k += 8) {
-            float pv[8];
-            const float4 na = *reinterpret_cast<const float4*>(colV + 64 * ch + k);
-            const float4 nb = *reinterpret_cast<const float4*>(colV + 64 * ch + k + 4);
-            const float nv[8] = {na.x, na.y, na.z, na.w, nb.x, nb.y, nb.z, nb.w};
+        for (int c = 0; c < 2; ++c) {
+            uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float pe = fast_exp2(x[k + e] - base);
-                s += pe;
-                pv[e] = pe * nv[e];
+            for (int e = 0; e < 32; ++e) {
+                const int k = 64 * c + 2 * e;
+                const float2 nv = *reinterpret_cast<const float2*>(colV + k);
+                const float p0 = fast_exp2(x[k] - base), p1 = fast_exp2(x[k + 1] - base);
+                s += p0 + p1;
+                pk[e] = pack_half2(p0 * nv.x, p1 * nv.y);
             }
-            *reinterpret_cast<uint4*>(sP + sw128_offset(r, 64 * ch + k)) =
-                make_uint4(pack_half2(pv[0], pv[1]), pack_half2(pv[2], pv[3]),
-                           pack_half2(pv[4], pv[5]), pack_half2(pv[6], pv[7]));
+            tmem_st32(t_s + 32 * c, pk);  // P over S columns 0..63 (tokens 64c..64c+63)
         }
-        l_part += s;
-        fence_proxy_async();
+        l_sum += s;
         tc_fence_before();
         if (__syncthreads_or(stalled)) { stalled = true; break; }
         tc_fence_after();
-        if (tid == 0) {  // O += P(n) . V(n)
+        if (tid == 0) {  // O_t += P_t(n) . V(n) for both tiles; P from tensor memory
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                umma_f16(tmem + 128, umma_desc_sw128(smem_u32(sP) + koff),
-                         umma_desc_sw128(smem_u32(sVt) + koff), C::kIdesc, (n > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int t2 = 0; t2 < 2; ++t2)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    umma_f16_ts(tmem + 256 * t2 + 128, tmem + 256 * t2 + 8 * kk,
+                                umma_desc_sw128(smem_u32(sVt) + koff), C::kIdesc, (n > 0 || kk > 0) ? 1u : 0u);
+                }
             umma_commit(bar_o);
+            // every thread is past its reads of the staging slot (K, norms, V)
+            // and S(n) -- which reads fp16 K from it -- is done
+            if (n + 2 < ntiles) issue(n + 2);
         }
         ++issued_o;
     }
 
-    // ---- epilogue: O / l, v_rescale, inverse rotation, fp16 (half 0 of each row) ----
-    if (ch == 1) xsum[r] = l_part;
+    // ---- epilogue: O / l, v_rescale, inverse rotation, fp16 ----
     bool ok = !stalled;
     if (issued_o > 0 && !mbar_wait_bounded(bar_o, (issued_o - 1) & 1)) ok = false;
     ok = __syncthreads_and(ok) != 0;  // one decision for the whole CTA
     tc_fence_after();
     if (!ok) {
         if (tid == 0) atomicOr(p.status, kStatusPipelineStall);
-    } else if (ch == 0) {  // warps 0-3, every lane: the loads are warp-collective
+    } else {
         float o[128];
         if (issued_o > 0) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 4; ++c) {  // every lane: the loads are warp-collective
                 uint32_t v[32];
-                tmem_ld32(tmem + 128 + lane_off + 32 * c, v);
+                tmem_ld32(t_o + 32 * c, v);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) o[32 * c + e] = __uint_as_float(v[e]);
             }
@@ -381,7 +380,6 @@ __global__ void __launch_bounds__(256, 1)
             for (int e = 0; e < 128; ++e) o[e] = 0.f;
         }
         if (row_ok) {
-            const float l_sum = l_part + xsum[r];
             float inv = 0.f;
             if (l_sum > 0.f) inv = p.v_rescale / l_sum;
             else atomicOr(p.status, kStatusShortContext);
@@ -400,7 +398,7 @@ __global__ void __launch_bounds__(256, 1)
                 *reinterpret_cast<uint4*>(op + k) = make_uint4(pack_half2(y[0], y[1]), pack_half2(y[2], y[3]),
                                                                pack_half2(y[4], y[5]), pack_half2(y[6], y[7]));
             }
-        }  // padding rows of the tile write nothing
+        }  // padding rows write nothing
     }
     if (!ok) {
         // let the copies still in flight land before the shared memory goes away
@@ -409,7 +407,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 template <int KB, int VB>
@@ -422,7 +420,7 @@ static int launch_prefill_t(const PrefillParams& p, const CUtensorMap* kmap, cud
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_pdl(tq_prefill_kernel<KB, VB>, dim3(p.mtiles, p.batch * p.hkv), dim3(256),
+    return launch_pdl(tq_prefill_kernel<KB, VB>, dim3((p.mtiles + 1) / 2, p.batch * p.hkv), dim3(256),
                       C::kSmemAlloc, stream, p, *kmap);
 }
 
