@@ -288,12 +288,19 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(v[e]);
         }
-        if constexpr (KB != 0) {
+        // t = s * n_k - base in one FFMA per score; the base moves only when a
+        // score passes it by more than 4 (so p <= 16 and p * n_v stays finite
+        // in fp16 for V norms below 4094)
+        const bool fresh = (m_base == -INFINITY);
+        const float base0 = fresh ? 0.f : m_base;
 #pragma unroll
-            for (int e = 0; e < 128; e += 4) {
-                const float4 nk = *reinterpret_cast<const float4*>(colK + e);
-                x[e] *= nk.x; x[e + 1] *= nk.y; x[e + 2] *= nk.z; x[e + 3] *= nk.w;
-            }
+        for (int e = 0; e < 128; e += 4) {
+            float4 nk = make_float4(1.f, 1.f, 1.f, 1.f);
+            if constexpr (KB != 0) nk = *reinterpret_cast<const float4*>(colK + e);
+            x[e] = fmaf(x[e], nk.x, -base0);
+            x[e + 1] = fmaf(x[e + 1], nk.y, -base0);
+            x[e + 2] = fmaf(x[e + 2], nk.z, -base0);
+            x[e + 3] = fmaf(x[e + 3], nk.w, -base0);
         }
         if (tok0 + C::kTile - 1 > lim_lo) {  // a tile some row of this query tile sees in part
 #pragma unroll
@@ -303,14 +310,15 @@ __global__ void __launch_bounds__(256, 1)
         float mx = -INFINITY;
 #pragma unroll
         for (int e = 0; e < 128; e += 2) mx = fmaxf(mx, fmaxf(x[e], x[e + 1]));
-        // the base moves only when a score passes it by more than 4 (so p <= 16
-        // and p * n_v stays finite in fp16 for V norms below 4094)
-        const bool grow = mx > m_base + 4.f;
+        const bool grow = fresh ? (mx > -INFINITY) : (mx > 4.f);
         if (__any_sync(0xffffffffu, grow)) {
-            const float nb_ = grow ? mx : m_base;
-            const float alpha = (m_base == -INFINITY || !grow) ? (grow ? 0.f : 1.f) : fast_exp2(m_base - nb_);
+            // rows that grow move their base up by mx (t -= mx below); the others keep it
+            const float shift = grow ? mx : 0.f;
+            const float alpha = grow ? (fresh ? 0.f : fast_exp2(-mx)) : 1.f;
             l_sum *= alpha;
-            m_base = nb_;
+            if (grow) m_base = base0 + mx;  // a row that saw no token yet keeps no base
+#pragma unroll
+            for (int e = 0; e < 128; ++e) x[e] -= shift;
             if (issued_o > 0) {  // rescale this row of O in tensor memory (P.V(n-1) is done)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -322,7 +330,6 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
         }
-        const float base = (m_base == -INFINITY) ? 0.f : m_base;
         float s = 0.f;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -331,7 +338,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int e = 0; e < 32; ++e) {
                 const int k = 64 * c + 2 * e;
                 const float2 nv = *reinterpret_cast<const float2*>(colV + k);
-                const float p0 = fast_exp2(x[k] - base), p1 = fast_exp2(x[k + 1] - base);
+                const float p0 = fast_exp2(x[k]), p1 = fast_exp2(x[k + 1]);
                 s += p0 + p1;
                 pk[e] = pack_half2(p0 * nv.x, p1 * nv.y);
             }
