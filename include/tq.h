@@ -227,6 +227,13 @@ int tq_decode_attention_noalloc(const tq_cache *cache, const void *q, int32_t nu
                                 int32_t tq, int32_t max_len_hint, float scale, void *out,
                                 uint32_t *status, void *stream);
 
+/* Self-test of the failure path, for tests: launches one CTA that waits, with
+ * the kernels' own bounded wait and a limit of limit_us microseconds (1 ..
+ * 1000000), on an mbarrier nothing arrives on.  The wait gives up and the
+ * next tq_get_status reports TQ_STATUS_PIPELINE_STALL; the context stays
+ * usable (no fault, no trap).  Allocates the context on first use. */
+int tq_selftest_bounded_wait(tq_ctx **ctx, int32_t limit_us, void *stream);
+
 /* Release a context (device memory included).  tq_free(NULL) is a no-op. */
 void tq_free(tq_ctx *ctx);
 

@@ -60,6 +60,7 @@ _SIGS = {
     "tq_decode_attention_noalloc": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_int32, _c.c_int32,
                                                _c.c_int32, _c.c_float, _c.c_void_p, _c.c_void_p,
                                                _c.c_void_p]),
+    "tq_selftest_bounded_wait": (_c.c_int, [_c.POINTER(_c.c_void_p), _c.c_int32, _c.c_void_p]),
     "tq_free": (None, [_c.c_void_p]),
     "tq_get_status": (_c.c_int, [_c.c_void_p, _c.POINTER(_c.c_uint32)]),
     "tq_lloyd_max_codebook": (_c.c_int, [_c.c_int32, _c.POINTER(_c.c_float)]),
@@ -293,6 +294,12 @@ def tq_decode_attention_noalloc(cache: Cache, q, out, max_len_hint: int, scale: 
                                              int(q.shape[2]), int(max_len_hint), float(scale),
                                              _ptr(out), _ptr(status), _stream(stream)),
            "tq_decode_attention_noalloc")
+
+
+def tq_selftest_bounded_wait(ctx: Context, limit_us: int, stream=None) -> None:
+    """Make one bounded in-kernel wait run out (failure-path self-test)."""
+    _check(lib().tq_selftest_bounded_wait(ctypes.byref(ctx.ptr), int(limit_us), _stream(stream)),
+           "tq_selftest_bounded_wait")
 
 
 def tq_free(ctx: Context) -> None:

@@ -553,6 +553,15 @@ int tq_prefill_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_
     return r == 0 ? TQ_OK : TQ_ERR_CUDA;
 }
 
+int tq_selftest_bounded_wait(tq_ctx** pctx, int32_t limit_us, void* stream) {
+    if (pctx == nullptr || limit_us < 1 || limit_us > 1000000) return TQ_ERR_INVALID_ARG;
+    tq_ctx* ctx;
+    int r = get_ctx(pctx, &ctx);
+    if (r != TQ_OK) return r;
+    return cuda_err(static_cast<cudaError_t>(tq::launch_selftest_stall(
+        ctx->d_words, uint64_t(limit_us) * 1000ull, static_cast<cudaStream_t>(stream))));
+}
+
 void tq_free(tq_ctx* ctx) {
     if (ctx == nullptr) return;
     int prev = 0;

@@ -770,6 +770,26 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
     *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(row) * kD + lane * 4) = out;
 }
 
+// Self-test of the bounded waits: one CTA waits on an mbarrier nothing ever
+// arrives on, through the same wait the pipelines use, with a short limit; the
+// wait must give up and leave kStatusPipelineStall in the status word.
+__global__ void __launch_bounds__(32) tq_selftest_stall_kernel(uint32_t* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar_word;
+    const uint32_t bar = smem_u32(&bar_word);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_bounded(bar, 0, limit_ns);
+    if (!ok && threadIdx.x == 0) atomicOr(status, kStatusPipelineStall);
+}
+
+int launch_selftest_stall(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+    tq_selftest_stall_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
 template <int KB, int VB, int NT, bool TAB = false>
 static int launch_decode_t(const DecodeParams& p, const CUtensorMap* kmap, cudaStream_t stream,
                            cudaEvent_t ev0, cudaEvent_t ev1) {

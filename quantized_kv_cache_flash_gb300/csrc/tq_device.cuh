@@ -119,14 +119,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of the barrier, giving up after ~2 s of wall time.
-// Returns false on time-out (the caller raises kStatusPipelineStall).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of the barrier, giving up after limit_ns of wall
+// time (2 s by default).  Returns false on time-out (the caller raises
+// kStatusPipelineStall).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) return false;
+        if ((i & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -96,6 +96,7 @@ int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stre
 int decode_ctas_per_sm(int kbits, int vbits, int group_rows, bool table);
 int launch_prefill(int kbits, int vbits, const PrefillParams& p, const CUtensorMap* kmap,
                    cudaStream_t stream);
+int launch_selftest_stall(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
 // Query rows per row group for `rows` query rows of one KV head.
 inline int group_rows_for(int rows) { return rows <= 8 ? 8 : 16; }

@@ -182,3 +182,26 @@ def test_null_context_calls(lib):
     assert lib.tq_get_status(None, ctypes.byref(s)) == tqf.TQ_OK and s.value == 0
     assert lib.tq_set_kernel_timing(None, 1) == tqf.TQ_ERR_INVALID_ARG
     assert lib.tq_error_string(tqf.TQ_ERR_CUDA) == b"CUDA error"
+
+
+def test_binding_raises_on_injected_cuda_error(monkeypatch):
+    """A CUDA failure reported by the library surfaces as TqError with the
+    library's message (the error is injected on the host)."""
+    class FakeLib:
+        def tq_record_bytes(self, bits):
+            return tqf.TQ_ERR_CUDA
+
+        def tq_error_string(self, code):
+            return b"CUDA error"
+    monkeypatch.setattr(tqf, "lib", lambda: FakeLib())
+    with pytest.raises(tqf.TqError) as e:
+        tqf.tq_record_bytes(3)
+    assert e.value.code == tqf.TQ_ERR_CUDA
+
+
+def test_selftest_rejects_bad_limits(lib):
+    ctx = ctypes.c_void_p(None)
+    assert lib.tq_selftest_bounded_wait(ctypes.byref(ctx), 0, None) == tqf.TQ_ERR_INVALID_ARG
+    assert lib.tq_selftest_bounded_wait(ctypes.byref(ctx), 2000000, None) == tqf.TQ_ERR_INVALID_ARG
+    assert lib.tq_selftest_bounded_wait(None, 100, None) == tqf.TQ_ERR_INVALID_ARG
+    assert ctx.value is None
