@@ -320,18 +320,18 @@ __device__ __forceinline__ void encode_group(const __half* src, uint8_t* dst, __
     }
 }
 
-// Advance lengths[] after the last warp of the launch (every warp read
-// lengths[] before taking its ticket, so none sees an advanced length).
-__device__ __forceinline__ void finish_append(const EncodeParams& p, unsigned int total_warps,
-                                              int lane) {
-    __syncwarp();
-    unsigned int ticket = 0;
-    if (lane == 0) {
+// Advance lengths[] after the last CTA of the launch: one ticket per CTA
+// (every thread read lengths[] before its CTA takes the ticket, so none sees
+// an advanced length); the counter is back at zero for the next launch.
+__device__ __forceinline__ void finish_append(const EncodeParams& p, int lane) {
+    __shared__ unsigned int s_ticket;
+    __syncthreads();
+    if (threadIdx.x == 0) {
         __threadfence();
-        ticket = atomicAdd(p.counter, 1u);
+        s_ticket = atomicAdd(p.counter, 1u);
     }
-    ticket = __shfl_sync(0xffffffffu, ticket, 0);
-    if (ticket == total_warps - 1) {
+    __syncthreads();
+    if (s_ticket == gridDim.x - 1 && threadIdx.x < 32) {
         __threadfence();
         for (int bb = lane; bb < p.batch; bb += 32) {
             const int Lb = *((volatile int32_t*)p.lengths + bb);
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(32 * kEncWarps)
                          gmask);
     }
 
-    finish_append(p, gridDim.x * kEncWarps, lane);
+    finish_append(p, lane);
 }
 
 // Small appends (a few tokens per sequence): one warp per vector, lane l holds
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(128) tq_encode_small_kernel(const __grid_const
             }
         }
     }
-    finish_append(p, gridDim.x * 4, lane);
+    finish_append(p, lane);
 }
 
 int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stream) {
