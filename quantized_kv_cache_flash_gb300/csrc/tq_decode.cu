@@ -50,8 +50,11 @@ struct DecCfg {
     static constexpr int kStageAlign = (KB == 0) ? 1024 : 128;
     static constexpr int kStage = (kStageRaw + kStageAlign - 1) / kStageAlign * kStageAlign;
     static constexpr int kPipeBytes = kWarps * kStages * kStage;
-    static constexpr int kQOff = kPipeBytes;                 // fp32 [kRows][128] query rows
-    static constexpr int kBarOff = kQOff + kRows * kD * 4;
+    // fp16 query rows in MMA k order, [kRows][kQStride]: the 16-byte pad staggers
+    // the rows over the banks for ldmatrix
+    static constexpr int kQStride = kD + 8;
+    static constexpr int kQOff = kPipeBytes;
+    static constexpr int kBarOff = kQOff + kRows * kQStride * 2;
     static constexpr int kScanOff = (kBarOff + kWarps * kStages * 8 + 15) / 16 * 16;
     static constexpr int kSmem = kScanOff + kWarps * 4 * 32 * 4;  // per-warp batch scan
     static constexpr int kSmemAlloc = kSmem + 1024;          // base alignment slack
@@ -60,25 +63,43 @@ struct DecCfg {
     static_assert(kWarps * kRows * kOStride * 4 + kWarps * kRows * 8 <= kPipeBytes, "scratch");
 };
 
-template <int KB, int COL>
-__device__ __forceinline__ void dequant_quarter_q(const uint8_t* rec, const Tables& t,
-                                                  uint32_t (&q)[8][4]) {
-    if constexpr (KB == 3) {
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(rec);
-        dequant3_quarter_q<COL>(w[0], w[1], w[2], t, q);
-    } else {
-        dequant4_quarter_q<COL>(*reinterpret_cast<const uint4*>(rec), t, q);
-    }
-}
+// A thread's quarter of a record (32 dims): 16 bytes of 4-bit codes or 12
+// bytes of 3-bit codes (w[3] unused).
+struct QuarterWords {
+    uint32_t w[4];
+};
 
 template <int KB>
-__device__ __forceinline__ void dequant_quarter(const uint8_t* rec, const Tables& t,
-                                                uint32_t (&h)[16]) {
+__device__ __forceinline__ QuarterWords load_quarter(const uint8_t* rec) {
+    QuarterWords q;
     if constexpr (KB == 3) {
         const uint32_t* w = reinterpret_cast<const uint32_t*>(rec);
-        dequant3_quarter(w[0], w[1], w[2], t, h);
+        q.w[0] = w[0]; q.w[1] = w[1]; q.w[2] = w[2]; q.w[3] = 0u;
     } else {
-        dequant4_quarter(*reinterpret_cast<const uint4*>(rec), t, h);
+        const uint4 v = *reinterpret_cast<const uint4*>(rec);
+        q.w[0] = v.x; q.w[1] = v.y; q.w[2] = v.z; q.w[3] = v.w;
+    }
+    return q;
+}
+
+// Group J (0..3) of a quarter: dim pairs 4J..4J+3 as four half2, the pairs
+// the whole-quarter dequantisers put in h[4J..4J+3].  Decoding a group at a
+// time lets each group's MMAs follow it, so only one group is live.
+template <int KB, int J>
+__device__ __forceinline__ void dequant_group(const QuarterWords& q, const Tables& t,
+                                              uint32_t (&h)[4]) {
+    if constexpr (KB == 3) {
+        uint32_t m;
+        if constexpr (J < 3) {
+            m = q.w[J] & 0x77777777u;
+        } else {  // the spare bits: bit k of the codes of dims 24..31 (see dequant3_quarter)
+            m = (__umulhi(q.w[0], 1u << 29) & 0x11111111u) | (__umulhi(q.w[1], 1u << 30) & 0x22222222u) |
+                (__umulhi(q.w[2], 1u << 31) & 0x44444444u);
+        }
+        lut4(m, t, h[0], h[1]);
+        lut4(__umulhi(m, 1u << 16), t, h[2], h[3]);
+    } else {
+        dequant4_word(q.w[J], t, h[0], h[1], h[2], h[3]);
     }
 }
 
@@ -238,7 +259,8 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
         fence_barrier_init();
     }
     __syncwarp();
-    float* sQ = reinterpret_cast<float*>(smem + C::kQOff);
+    __half* sQ = reinterpret_cast<__half*>(smem + C::kQOff);
+    const uint32_t q_lds = smem_u32(sQ) + ((lane & 7) * C::kQStride + 8 * (lane >> 3)) * 2;
     const Tables kt{p.ktab[0], p.ktab[1], p.ktab[2], p.ktab[3]};
     const Tables vt{p.vtab[0], p.vtab[1], p.vtab[2], p.vtab[3]};
     const bool sparse = p.sparse_tau > 0.f;
@@ -321,26 +343,28 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
                     for (int i = 0; i < 4; ++i) v[i] *= inv;
                 }
             }
-            *reinterpret_cast<float4*>(sQ + r * kD + lane * 4) = make_float4(v[0], v[1], v[2], v[3]);
+            // Row r in the k order of the score MMA's B operand (k = head dims,
+            // n = query rows).  Quantized K: a thread's A operand is its tokens'
+            // quarter `t` in order, so k-index 16*kc + 8*hi + 2*t + e holds dim
+            // 32*t + 4*kc + 2*hi + e; this lane's dims 4*lane + 2*hi + e sit at
+            // k = 16*(lane & 7) + 8*hi + 2*(lane >> 3) + e.  fp16 K: k = dim.
+            __half* qrow = sQ + r * C::kQStride;
+            const uint32_t lo = pack_half2(v[0], v[1]), hi = pack_half2(v[2], v[3]);
+            if constexpr (KB != 0) {
+                const int k0 = 16 * (lane & 7) + 2 * (lane >> 3);
+                *reinterpret_cast<uint32_t*>(qrow + k0) = lo;
+                *reinterpret_cast<uint32_t*>(qrow + k0 + 8) = hi;
+            } else {
+                *reinterpret_cast<uint2*>(qrow + 4 * lane) = make_uint2(lo, hi);
+            }
         }
         __syncthreads();
 
-        // B fragments of the score MMA (k = head dims, n = query rows).  Quantized
-        // K: a thread's A operand is its tokens' quarter `t` in order, so logical
-        // k-index 16*kc + 2*t + e maps to dim 32*t + 4*kc + e (and +8 -> +2).
-        uint32_t qb[NT][8][2];
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            const float* qr = sQ + (8 * n + g) * kD;
-#pragma unroll
-            for (int kc = 0; kc < 8; ++kc) {
-                int d0, d1;
-                if constexpr (KB != 0) { d0 = 32 * t + 4 * kc; d1 = d0 + 2; }
-                else { d0 = 16 * kc + 2 * t; d1 = d0 + 8; }
-                qb[n][kc][0] = pack_half2(qr[d0], qr[d0 + 1]);
-                qb[n][kc][1] = pack_half2(qr[d1], qr[d1 + 1]);
-            }
-        }
+        // B fragments of k-steps 2*kc2 and 2*kc2 + 1 for row tile n (ldmatrix
+        // matrix j = lane >> 3 covers k in [32*kc2 + 8*j, +8) of rows 8n..8n+7)
+        auto load_qb = [&](int n, int kc2, uint32_t (&b)[4]) {
+            ldsm_x4(q_lds + (8 * n * C::kQStride + 32 * kc2) * 2, b[0], b[1], b[2], b[3]);
+        };
 
         // last visible token (inclusive) of the rows 8n + 2t + e this thread owns
         int lim[NT][2];
@@ -381,34 +405,50 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
                         const int mi = lane >> 3;
                         const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
         #pragma unroll
-                        for (int kc = 0; kc < 8; ++kc) {
-                            const int db = 2 * kc + (mi >> 1);  // 16-byte chunk 0..15 of the row
-                            const uint32_t addr = smem_u32(st) + (db >> 3) * 4096 + row * 128 +
-                                                  (((db & 7) ^ (row & 7)) << 4);
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4(addr, a0, a1, a2, a3);
+                        for (int kc2 = 0; kc2 < 4; ++kc2) {
+                            uint32_t qb[NT][4];
         #pragma unroll
-                            for (int n = 0; n < NT; ++n) mma_f16(x[tile][n], a0, a1, a2, a3, qb[n][kc][0], qb[n][kc][1]);
+                            for (int n = 0; n < NT; ++n) load_qb(n, kc2, qb[n]);
+        #pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const int db = 4 * kc2 + 2 * kk + (mi >> 1);  // 16-byte chunk 0..15 of the row
+                                const uint32_t addr = smem_u32(st) + (db >> 3) * 4096 + row * 128 +
+                                                      (((db & 7) ^ (row & 7)) << 4);
+                                uint32_t a0, a1, a2, a3;
+                                ldsm_x4(addr, a0, a1, a2, a3);
+        #pragma unroll
+                                for (int n = 0; n < NT; ++n)
+                                    mma_f16(x[tile][n], a0, a1, a2, a3, qb[n][2 * kk], qb[n][2 * kk + 1]);
+                            }
                         }
                     } else {
-                        // A quad of k-step kc: (token g, dims 2kc), (token g+8, 2kc),
-                        // (token g, 2kc+1), (token g+8, 2kc+1) in quarter-pair units
-                        uint32_t aq[8][4];
+                        // A quad of k-step kc: (token g, pair 2kc), (token g+8, pair 2kc),
+                        // (token g, pair 2kc+1), (token g+8, pair 2kc+1) of the quarters;
+                        // group J of both tokens feeds k-steps 2J and 2J+1
                         const uint8_t* ra = st + (tile * 16 + g) * C::kRbK;
                         const uint8_t* rb = st + (tile * 16 + g + 8) * C::kRbK;
-                        if constexpr (TAB) {
-                            dequant_quarter_q<KB, 0>(ra + t * C::kQuarterK, record_tables(ra + 48), aq);
-                            dequant_quarter_q<KB, 1>(rb + t * C::kQuarterK, record_tables(rb + 48), aq);
-                        } else {
-                            dequant_quarter_q<KB, 0>(ra + t * C::kQuarterK, kt, aq);
-                            dequant_quarter_q<KB, 1>(rb + t * C::kQuarterK, kt, aq);
-                        }
+                        const QuarterWords wa = load_quarter<KB>(ra + t * C::kQuarterK);
+                        const QuarterWords wb = load_quarter<KB>(rb + t * C::kQuarterK);
+                        const Tables ta = TAB ? record_tables(ra + 48) : kt;
+                        const Tables tb = TAB ? record_tables(rb + 48) : kt;
+                        auto kgroup = [&](auto jtag) {
+                            constexpr int J = decltype(jtag)::value;
+                            uint32_t ha[4], hb[4];
+                            dequant_group<KB, J>(wa, ta, ha);
+                            dequant_group<KB, J>(wb, tb, hb);
+                            uint32_t qb[NT][4];
         #pragma unroll
-                        for (int kc = 0; kc < 8; ++kc)
+                            for (int n = 0; n < NT; ++n) load_qb(n, J, qb[n]);
         #pragma unroll
-                            for (int n = 0; n < NT; ++n)
-                                mma_f16(x[tile][n], aq[kc][0], aq[kc][1], aq[kc][2], aq[kc][3],
-                                        qb[n][kc][0], qb[n][kc][1]);
+                            for (int n = 0; n < NT; ++n) {
+                                mma_f16(x[tile][n], ha[0], hb[0], ha[1], hb[1], qb[n][0], qb[n][1]);
+                                mma_f16(x[tile][n], ha[2], hb[2], ha[3], hb[3], qb[n][2], qb[n][3]);
+                            }
+                        };
+                        kgroup(std::integral_constant<int, 0>{});
+                        kgroup(std::integral_constant<int, 1>{});
+                        kgroup(std::integral_constant<int, 2>{});
+                        kgroup(std::integral_constant<int, 3>{});
                     }
                 }
 
@@ -528,33 +568,31 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
                         pb1[n] = movtrans(pack_half2(x[tile][n][2] * nv[tile][1], x[tile][n][3] * nv[tile][1]));
                     }
                     // A quad of dim tile mt: transposed pairs 2mt, 2mt+1 of token block 0
-                    // (tokens 0-7 of the tile) then of block 1 (tokens 8-15)
-                    uint32_t vq[8][4];
-                    {
-                        uint32_t hv[16];
-                        const uint8_t* rv = st + C::kVOff + (tile * 16 + g) * C::kRbV;
-                        dequant_quarter<VB>(rv + t * C::kQuarterV, TAB ? v_tables<FULL>(rv, tok0 + tile * 16 + g < t_end) : vt, hv);
+                    // (tokens 0-7 of the tile) then of block 1 (tokens 8-15); group J of
+                    // both tokens feeds dim tiles 2J and 2J+1
+                    const uint8_t* rva = st + C::kVOff + (tile * 16 + g) * C::kRbV;
+                    const uint8_t* rvb = st + C::kVOff + (tile * 16 + g + 8) * C::kRbV;
+                    const QuarterWords va = load_quarter<VB>(rva + t * C::kQuarterV);
+                    const QuarterWords vb = load_quarter<VB>(rvb + t * C::kQuarterV);
+                    const Tables tva = TAB ? v_tables<FULL>(rva, tok0 + tile * 16 + g < t_end) : vt;
+                    const Tables tvb = TAB ? v_tables<FULL>(rvb, tok0 + tile * 16 + g + 8 < t_end) : vt;
+                    auto vgroup = [&](auto jtag) {
+                        constexpr int J = decltype(jtag)::value;
+                        uint32_t ha[4], hb[4];
+                        dequant_group<VB, J>(va, tva, ha);
+                        dequant_group<VB, J>(vb, tvb, hb);
         #pragma unroll
-                        for (int mt = 0; mt < 8; ++mt) {
-                            vq[mt][0] = movtrans(hv[2 * mt]);
-                            vq[mt][1] = movtrans(hv[2 * mt + 1]);
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t v0 = movtrans(ha[2 * e]), v1 = movtrans(ha[2 * e + 1]);
+                            const uint32_t v2 = movtrans(hb[2 * e]), v3 = movtrans(hb[2 * e + 1]);
+        #pragma unroll
+                            for (int n = 0; n < NT; ++n) mma_f16(O[n][2 * J + e], v0, v1, v2, v3, pb0[n], pb1[n]);
                         }
-                    }
-                    {
-                        uint32_t hv[16];
-                        const uint8_t* rv = st + C::kVOff + (tile * 16 + g + 8) * C::kRbV;
-                        dequant_quarter<VB>(rv + t * C::kQuarterV, TAB ? v_tables<FULL>(rv, tok0 + tile * 16 + g + 8 < t_end) : vt, hv);
-        #pragma unroll
-                        for (int mt = 0; mt < 8; ++mt) {
-                            vq[mt][2] = movtrans(hv[2 * mt]);
-                            vq[mt][3] = movtrans(hv[2 * mt + 1]);
-                        }
-                    }
-        #pragma unroll
-                    for (int mt = 0; mt < 8; ++mt)
-        #pragma unroll
-                        for (int n = 0; n < NT; ++n)
-                            mma_f16(O[n][mt], vq[mt][0], vq[mt][1], vq[mt][2], vq[mt][3], pb0[n], pb1[n]);
+                    };
+                    vgroup(std::integral_constant<int, 0>{});
+                    vgroup(std::integral_constant<int, 1>{});
+                    vgroup(std::integral_constant<int, 2>{});
+                    vgroup(std::integral_constant<int, 3>{});
                 }
 
         };
@@ -836,21 +874,25 @@ int launch_combine(const CombineParams& p, cudaStream_t stream) {
     return launch_pdl(tq_combine_kernel, dim3((rows + 3) / 4), dim3(128), 0, stream, p);
 }
 
-template <int KB, int VB, bool TAB = false>
-static int smem_of(int nt) {
-    return nt == 1 ? DecCfg<KB, VB, 1, TAB>::kSmemAlloc : DecCfg<KB, VB, 2, TAB>::kSmemAlloc;
+// Resident CTAs per SM: the launch bounds' target, unless shared memory
+// (228 KB per SM, 1 KB of it reserved per CTA) allows fewer.
+template <int KB, int VB, int NT, bool TAB = false>
+static int ctas_of() {
+    using C = DecCfg<KB, VB, NT, TAB>;
+    const int by_smem = (228 * 1024) / (C::kSmemAlloc + 1024);
+    return by_smem < C::kMinCtas ? by_smem : C::kMinCtas;
+}
+
+template <int NT>
+static int ctas_nt(int kbits, int vbits, bool table) {
+    if (table) return ctas_of<3, 3, NT, true>();
+    if (kbits == 16) return vbits == 4 ? ctas_of<0, 4, NT>() : ctas_of<0, 3, NT>();
+    if (kbits == 3) return ctas_of<3, 3, NT>();
+    return vbits == 4 ? ctas_of<4, 4, NT>() : ctas_of<4, 3, NT>();
 }
 
 int decode_ctas_per_sm(int kbits, int vbits, int group_rows, bool table) {
-    const int nt = group_rows <= 8 ? 1 : 2;
-    int smem = 0;
-    if (table) smem = smem_of<3, 3, true>(nt);
-    else if (kbits == 16) smem = vbits == 4 ? smem_of<0, 4>(nt) : smem_of<0, 3>(nt);
-    else if (kbits == 3) smem = smem_of<3, 3>(nt);
-    else smem = vbits == 4 ? smem_of<4, 4>(nt) : smem_of<4, 3>(nt);
-    int by_smem = (228 * 1024) / (smem + 1024);  // 1 KB per CTA is reserved
-    const int by_regs = nt == 1 ? 4 : 3;         // the kernels' launch bounds
-    int c = by_smem < by_regs ? by_smem : by_regs;
+    const int c = group_rows <= 8 ? ctas_nt<1>(kbits, vbits, table) : ctas_nt<2>(kbits, vbits, table);
     return c < 1 ? 1 : c;
 }
 
