@@ -383,9 +383,14 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
         for (int n = 0; n < NT; ++n)
 #pragma unroll
             for (int i = 0; i < 8; ++i) O[n][i][0] = O[n][i][1] = O[n][i][2] = O[n][i][3] = 0.f;
-        float m[NT][2], l[NT][2];
+        // running max m, sum l, exp2 base bs (m, or 0 before the first score)
+        // and growth threshold thr of the rows this thread owns
+        constexpr float kSlack = 4.f;
+        float m[NT][2], l[NT][2], bs[NT][2], thr[NT][2];
 #pragma unroll
-        for (int n = 0; n < NT; ++n) m[n][0] = m[n][1] = -INFINITY, l[n][0] = l[n][1] = 0.f;
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) m[n][e] = thr[n][e] = -INFINITY, l[n][e] = bs[n][e] = 0.f;
         bool stalled = false;
 
         // One 32-token chunk of this warp.  FULL: all 32 tokens valid and visible
@@ -470,10 +475,13 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
                         nv[tile][0] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * ta));
                         nv[tile][1] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * tb));
                     }
+                    // scaled score minus the row's exp2 base, one FFMA each
         #pragma unroll
                     for (int n = 0; n < NT; ++n) {
-                        x[tile][n][0] *= ka; x[tile][n][1] *= ka;
-                        x[tile][n][2] *= kb2; x[tile][n][3] *= kb2;
+                        x[tile][n][0] = fmaf(x[tile][n][0], ka, -bs[n][0]);
+                        x[tile][n][1] = fmaf(x[tile][n][1], ka, -bs[n][1]);
+                        x[tile][n][2] = fmaf(x[tile][n][2], kb2, -bs[n][0]);
+                        x[tile][n][3] = fmaf(x[tile][n][3], kb2, -bs[n][1]);
                     }
                     if constexpr (!FULL) {
                         const int ga = tok0 + ta, gb = tok0 + tb;
@@ -492,16 +500,16 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
                 }
                 // The exp2 base of a row stays at its running max until a score exceeds
                 // it by more than kSlack (log2 units); only then (warp-uniform slow
-                // path) is the true max taken and O, l rescaled.  So p <= 2^kSlack.
-                constexpr float kSlack = 4.f;
+                // path) is the true max taken, O and l rescaled and the scores moved
+                // to the new base.  So p <= 2^kSlack.  A row with no score yet has
+                // base 0 and threshold -inf: its first finite score sets the max.
                 bool grow = false;
         #pragma unroll
                 for (int n = 0; n < NT; ++n)
         #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const float lim_x = m[n][e] + kSlack;
-                        grow |= x[0][n][e] > lim_x || x[0][n][e + 2] > lim_x ||
-                                x[1][n][e] > lim_x || x[1][n][e + 2] > lim_x;
+                        const float mx = fmaxf(fmaxf(x[0][n][e], x[0][n][e + 2]), fmaxf(x[1][n][e], x[1][n][e + 2]));
+                        grow |= mx > thr[n][e];
                     }
                 if (__any_sync(0xffffffffu, grow)) {
         #pragma unroll
@@ -512,9 +520,18 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                            const float mn = fmaxf(m[n][e], mx);
+                            const float mn = fmaxf(m[n][e], mx + bs[n][e]);
                             const float al = (m[n][e] == -INFINITY) ? 0.f : fast_exp2(m[n][e] - mn);
+                            const float nb = (mn == -INFINITY) ? 0.f : mn;
+                            const float shift = bs[n][e] - nb;
+        #pragma unroll
+                            for (int tile = 0; tile < 2; ++tile) {
+                                x[tile][n][e] += shift;
+                                x[tile][n][e + 2] += shift;
+                            }
                             m[n][e] = mn;
+                            bs[n][e] = nb;
+                            thr[n][e] = (mn == -INFINITY) ? -INFINITY : kSlack;
                             l[n][e] *= al;
         #pragma unroll
                             for (int i = 0; i < 8; ++i) {
@@ -527,12 +544,11 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
                 for (int n = 0; n < NT; ++n)
         #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const float base = (m[n][e] == -INFINITY) ? 0.f : m[n][e];
                         float s = 0.f;
         #pragma unroll
                         for (int tile = 0; tile < 2; ++tile) {
-                            x[tile][n][e] = fast_exp2(x[tile][n][e] - base);
-                            x[tile][n][e + 2] = fast_exp2(x[tile][n][e + 2] - base);
+                            x[tile][n][e] = fast_exp2(x[tile][n][e]);
+                            x[tile][n][e + 2] = fast_exp2(x[tile][n][e + 2]);
                             s += x[tile][n][e] + x[tile][n][e + 2];
                         }
                         l[n][e] += s;
