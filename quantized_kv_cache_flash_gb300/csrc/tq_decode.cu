@@ -721,18 +721,20 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
 }
 
 
-// One warp per output row (b, q head, query j): merge the partials of the
+// One CTA per output row (b, q head, query j): merge the partials of the
 // CTAs that covered the row's unit with their log-sum-exp weights, apply
 // v_rescale, leave the rotated basis (Rot^-1(y) = s * (H y) / sqrt(128)) and
-// store fp16.  The lanes first split the partials' (max, sum) pairs between
-// them; then every lane walks the partials for its 4 dims, 8 loads in flight,
-// taking each partial's weight from the lane that computed it.
+// store fp16.  The 4 warps split the partials (warp w takes i = w mod 4), so
+// a long unit's partials are read with four times the loads in flight: each
+// warp merges its share against its own max, lane l holding dims 4l..4l+3,
+// and warp 0 merges the four results.
 __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__ CombineParams p) {
+    __shared__ float4 s_acc[4][32];
+    __shared__ float s_m[4], s_den[4];
     griddep_wait();  // the decode kernel's partials
     const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int total = p.batch * p.hq * p.tq;
-    if (row >= total) return;
+    const int warp = threadIdx.x >> 5;
+    const int row = blockIdx.x;
     const int j = row % p.tq;
     const int hq = (row / p.tq) % p.hq;
     const int b = row / (p.tq * p.hq);
@@ -770,24 +772,31 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
         return i < n && (!some_empty || c * cq + (c * cr) / P < (c + 1) * cq + ((c + 1) * cr) / P);
     };
     const size_t row0 = (static_cast<size_t>(c0) + unit) * 16 + rl;  // partial of CTA c0
+    auto load_ml = [&](int i) {
+        return __ldcg(reinterpret_cast<const float2*>(p.part_ml) + row0 + 16 * static_cast<size_t>(i));
+    };
 
-    float M = -INFINITY;
-    for (int i = lane; i < n; i += 32)
-        if (used(i)) M = fmaxf(M, __ldcg(p.part_ml + (row0 + 16 * static_cast<size_t>(i)) * 2));
+    // this warp's partials: i = warp + 4k; lane l reads the (m, l) pair of k = l (+32 ...)
+    const int i_first = warp + 4 * lane;
+    const float2 ml_first = used(i_first) ? load_ml(i_first) : make_float2(-INFINITY, 0.f);
+    float M = ml_first.x;
+    for (int i = i_first + 128; i < n; i += 128)
+        if (used(i)) M = fmaxf(M, load_ml(i).x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
     float den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < n; i0 += 32) {
+    for (int i0 = 0; i0 < n; i0 += 128) {
+        const int i = i0 + i_first;
         float w = 0.f;
-        if (used(i0 + lane)) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + row0 +
-                                     16 * static_cast<size_t>(i0 + lane));
-            if (ml.x != -INFINITY) w = fast_exp2(ml.x - M);
+        const float2 ml = (i0 == 0) ? ml_first : (used(i) ? load_ml(i) : make_float2(-INFINITY, 0.f));
+        if (ml.x != -INFINITY) {
+            w = fast_exp2(ml.x - M);
             den += w * ml.y;
         }
-        const int nb = min(32, n - i0);
+        const int left = n - i0 - warp;                 // partials i0 + warp + 4k, k < nb
+        const int nb = left > 0 ? min(32, (left + 3) / 4) : 0;
         for (int k0 = 0; k0 < nb; k0 += 8) {
             float wk[8];
             float4 o[8];
@@ -796,7 +805,7 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
                 wk[k] = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
                 o[k] = (k0 + k < nb && wk[k] != 0.f)
                            ? __ldcg(reinterpret_cast<const float4*>(
-                                        p.part_o + (row0 + 16 * static_cast<size_t>(i0 + k0 + k)) * kD) +
+                                        p.part_o + (row0 + 16 * static_cast<size_t>(i0 + warp + 4 * (k0 + k))) * kD) +
                                     lane)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -809,10 +818,30 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    s_acc[warp][lane] = acc;
+    if (lane == 0) {
+        s_m[warp] = M;
+        s_den[warp] = den;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+
+    float Mall = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) Mall = fmaxf(Mall, s_m[w]);
+    float dsum = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const float sc = (s_m[w] == -INFINITY) ? 0.f : fast_exp2(s_m[w] - Mall);
+        const float4 x = s_acc[w][lane];
+        dsum += sc * s_den[w];
+        a.x += sc * x.x; a.y += sc * x.y; a.z += sc * x.z; a.w += sc * x.w;
+    }
     float inv = 0.f;
-    if (den > 0.f) inv = p.v_rescale / den;
+    if (dsum > 0.f) inv = p.v_rescale / dsum;
     else if (lane == 0) atomicOr(p.status, kStatusShortContext);
-    float v[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+    float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
     wht128_lane4(v, lane);
     const uint32_t sn = sign_nibble(p.signs, lane);
     const float nrm = 0.08838834764831845f;
@@ -887,7 +916,7 @@ int launch_decode(int kbits, int vbits, const DecodeParams& p, const CUtensorMap
 
 int launch_combine(const CombineParams& p, cudaStream_t stream) {
     const int rows = p.batch * p.hq * p.tq;
-    return launch_pdl(tq_combine_kernel, dim3((rows + 3) / 4), dim3(128), 0, stream, p);
+    return launch_pdl(tq_combine_kernel, dim3(rows), dim3(128), 0, stream, p);
 }
 
 // Resident CTAs per SM: the launch bounds' target, unless shared memory
