@@ -48,6 +48,7 @@ REC = {"turbo4_asym": (256, 66), "turbo3": (50, 50), "turbo4": (66, 66),
        "turbo3_asym": (256, 50), "turbo4k_3v": (66, 50), "turbo3_table": (64, 64)}
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SAMPLE = 10   # decode launches timed on their own: one timed step in this many
+PIPELINE_MIN_MS = 0.1   # e2e: device step time above which the host copies overlap compute
 
 
 def prompt_flops(w: wl.Workload) -> float:
@@ -505,13 +506,16 @@ def gpu_arm(args, rank, world, device_index):
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step copies its q (and new K/V) from pinned host memory and reads
-    # its output back.  The copies run on a second stream, double-buffered:
-    # step i+1's inputs go up while step i computes, and step i's output comes
-    # down while step i+1 computes, as a serving loop would overlap them.
+    # its output back.  Steps long enough to hide the extra host calls
+    # (> PIPELINE_MIN_MS on the device) run their copies on a second stream,
+    # double-buffered: step i+1's inputs go up while step i computes, and step
+    # i's output comes down while step i+1 computes.  Shorter steps are bound
+    # by the host's calls, so their copies stay on the compute stream.
     qh = [q.cpu().pin_memory() for q in qs]
     knh = [k.cpu().pin_memory() for k in kn]
     vnh = [v.cpu().pin_memory() for v in vn]
-    nbuf = 2
+    pipelined = ms_max / steps > PIPELINE_MIN_MS
+    nbuf = 2 if pipelined else 1
     q_dev = [torch.empty_like(qs[0]) for _ in range(nbuf)]
     k_dev = [torch.empty_like(kn[0]) for _ in range(nbuf)] if t_new else None
     v_dev = [torch.empty_like(vn[0]) for _ in range(nbuf)] if t_new else None
@@ -537,26 +541,36 @@ def gpu_arm(args, rank, world, device_index):
 
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    copy_stream.wait_event(f0)
     order = list(range(warm, nstep))
-    upload(order[0], 0)
-    for j, i in enumerate(order):
-        sl = j % nbuf
-        if j + 1 < len(order):
-            upload(order[j + 1], (j + 1) % nbuf)
-        stream.wait_event(h2d_ev[sl])
-        stream.wait_event(d2h_ev[sl])              # out_dev[sl] has been read back
-        if t_new:
-            tqf.tq_encode_append(ctx, cache, k_dev[sl], v_dev[sl], stream)
-        tqf.tq_decode_attention(ctx, cache, q_dev[sl], out_dev[sl], max_len_hint, 0.0, stream)
-        comp_ev[sl].record(stream)
-        copy_stream.wait_event(comp_ev[sl])
-        with torch.cuda.stream(copy_stream):
-            out_h.copy_(out_dev[sl], non_blocking=True)
-        d2h_ev[sl].record(copy_stream)
-    done = torch.cuda.Event()
-    done.record(copy_stream)
-    stream.wait_event(done)
+    if pipelined:
+        copy_stream.wait_event(f0)
+        upload(order[0], 0)
+        for j, i in enumerate(order):
+            sl = j % nbuf
+            if j + 1 < len(order):
+                upload(order[j + 1], (j + 1) % nbuf)
+            stream.wait_event(h2d_ev[sl])
+            stream.wait_event(d2h_ev[sl])              # out_dev[sl] has been read back
+            if t_new:
+                tqf.tq_encode_append(ctx, cache, k_dev[sl], v_dev[sl], stream)
+            tqf.tq_decode_attention(ctx, cache, q_dev[sl], out_dev[sl], max_len_hint, 0.0, stream)
+            comp_ev[sl].record(stream)
+            copy_stream.wait_event(comp_ev[sl])
+            with torch.cuda.stream(copy_stream):
+                out_h.copy_(out_dev[sl], non_blocking=True)
+            d2h_ev[sl].record(copy_stream)
+        done = torch.cuda.Event()
+        done.record(copy_stream)
+        stream.wait_event(done)
+    else:
+        for i in order:
+            q_dev[0].copy_(qh[i], non_blocking=True)
+            if t_new:
+                k_dev[0].copy_(knh[i], non_blocking=True)
+                v_dev[0].copy_(vnh[i], non_blocking=True)
+                tqf.tq_encode_append(ctx, cache, k_dev[0], v_dev[0], stream)
+            tqf.tq_decode_attention(ctx, cache, q_dev[0], out_dev[0], max_len_hint, 0.0, stream)
+            out_h.copy_(out_dev[0], non_blocking=True)
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(world, f0.elapsed_time(f1))
@@ -601,7 +615,8 @@ def gpu_arm(args, rank, world, device_index):
                      "peak_kind": f"{peak_kind} hbm_gbs (copy), kernel timed inside the step"},
         "e2e": {"value": total_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": e2e_ms / steps},
+                "ms_per_step": e2e_ms / steps,
+                "copies": "second stream, double-buffered" if pipelined else "compute stream"},
         "launches": (3 if t_new else 2) * steps,
     }
 

@@ -216,18 +216,46 @@ __device__ __forceinline__ void store_norm(__half* dst_norm, uint8_t* dst, const
     *reinterpret_cast<uint4*>(dst + 48) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// XOR masks that apply a lane's 32 signs to its dims as fp16 pairs: word k
+// flips dim 2k with bit 15 and dim 2k+1 with bit 31.
+__device__ __forceinline__ void sign_masks(uint32_t sg, uint32_t (&hm)[16]) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) hm[k] = (((sg >> (2 * k)) & 1u) << 15) | (((sg >> (2 * k + 1)) & 1u) << 31);
+}
+
+// Encode one vector per 4 lanes (8 per warp); lane quarter q holds dims
+// 32q .. 32q+31.  `valid` marks lanes whose vector exists.  The codes compare
+// the unnormalised rotated value y = H (s * x) / sqrt(128) ... scaled back:
+// u = y / n > tau_k  <=>  y > tau_k * sqrt(128) * n  for the fp32 norm n, so
+// the thresholds are scaled once per vector instead of every u divided.  The
+// fp32 rotation and scaling are within ~1e-7 (relative) of the exact u;
+// elements that close to a midpoint may round either way (a zero u is
+// negative: the tie goes to the lower index).
+// The lane's 32 fp16 inputs (64 bytes), or zeros for a lane without a vector.
+struct QuarterIn {
+    uint4 w[4];
+};
+
+__device__ __forceinline__ QuarterIn load_quarter_in(const __half* src, int q, bool valid) {
+    QuarterIn r;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + q * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r.w[i] = valid ? s4[i] : make_uint4(0u, 0u, 0u, 0u);
+    return r;
+}
+
 template <int BITS>
-__device__ __forceinline__ void encode_group(const __half* src, uint8_t* dst, __half* dst_norm,
-                                             const float* tcb, const uint32_t (&signs)[4],
-                                             const float* gt, const float* ge, bool valid,
+__device__ __forceinline__ void encode_group(const QuarterIn& in, const __half* src, uint8_t* dst,
+                                             __half* dst_norm, const float* tcb,
+                                             const uint32_t (&hm)[16], const float* gt, bool valid,
                                              uint32_t* status, int q, unsigned gmask) {
-    float x[32];
-    if (valid) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(src + q * 32);
+    float x[32];  // s * x for the lane's dims
+    {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint4 w = s4[i];
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+            const uint4 w = in.w[i];
+            const uint32_t ww[4] = {w.x ^ hm[4 * i], w.y ^ hm[4 * i + 1], w.z ^ hm[4 * i + 2],
+                                    w.w ^ hm[4 * i + 3]};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
@@ -235,12 +263,13 @@ __device__ __forceinline__ void encode_group(const __half* src, uint8_t* dst, __
                 x[8 * i + 2 * k + 1] = f.y;
             }
         }
-    } else {
+    }
+    if (!valid) {  // a lane without a vector takes part in the shuffles with zeros
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[i] = 0.f;
     }
 
-    // norm: squares of fp16 values are exact in fp32
+    // norm: squares of fp16 values are exact in fp32 (the signs do not matter)
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) ss = fmaf(x[i], x[i], ss);
@@ -254,9 +283,6 @@ __device__ __forceinline__ void encode_group(const __half* src, uint8_t* dst, __
     }
 
     // rotate: H (s * x), 5 in-lane stages + 2 across the group's lanes
-    const uint32_t sg = signs[q];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = ((sg >> i) & 1u) ? -x[i] : x[i];
 #pragma unroll
     for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
@@ -269,23 +295,19 @@ __device__ __forceinline__ void encode_group(const __half* src, uint8_t* dst, __
     }
 #pragma unroll
     for (int m = 1; m <= 2; m <<= 1) {
+        const float sgn = (q & m) ? -1.f : 1.f;   // upper half of the pair: o - x
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
-            x[i] = (q & m) ? (o - x[i]) : (x[i] + o);
+            x[i] = fmaf(sgn, x[i], o);
         }
     }
-    const float n = sqrtf(S32);
-    const float inv = (n > 0.f) ? 1.0f / (n * 11.313708498984761f) : 0.f;
 
     constexpr int H = 1 << (BITS - 1);
-    bool any_tie = false;
+    const float scale = sqrtf(S32) * 11.313708498984761f;   // sqrt(128) n
+    float T[H - 1];
 #pragma unroll
-    for (int k = 0; k < H - 1; ++k) any_tie |= ge[k] != gt[k];
-    uint32_t code[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) code[i] = quantize_code<BITS>(x[i] * inv, gt, ge, any_tie);
-
+    for (int k = 0; k < H - 1; ++k) T[k] = gt[k] * scale;
     if (!valid) return;
     if constexpr (BITS == 4) {
         // word k = dims 8k..8k+7: rank of dim 8k+j in bits 4j..4j+2; sign of dim
@@ -295,34 +317,64 @@ __device__ __forceinline__ void encode_group(const __half* src, uint8_t* dst, __
         for (int k = 0; k < 4; ++k) {
             uint32_t v = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v |= (code[8 * k + j] & 7u) << (4 * j);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v |= (code[8 * k + j] >> 3) << (8 * j + 7);
-                v |= (code[8 * k + 4 + j] >> 3) << (8 * j + 3);
+            for (int j = 0; j < 8; ++j) {
+                const float y = x[8 * k + j];
+                const float a = fabsf(y);
+                const bool b2 = a > T[3];
+                const bool b1 = a > (b2 ? T[5] : T[1]);
+                const float t0 = b2 ? (b1 ? T[6] : T[4]) : (b1 ? T[2] : T[0]);
+                const bool b0 = a > t0;
+                const uint32_t rank = (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u);
+                v |= rank << (4 * j);
+                if (!(y > 0.f)) v |= 1u << (j < 4 ? 8 * j + 7 : 8 * (j - 4) + 3);
             }
             w[k] = v;
         }
         *reinterpret_cast<uint4*>(dst + q * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     } else {
-        // quarter q: word k (k < 3): bits 4j..4j+2 = code(8k+j), bit 4j+3 = bit k of code(24+j)
-        uint32_t* d = reinterpret_cast<uint32_t*>(dst + q * 12);
+        // sign-magnitude code kappa = sign << 2 | rank; quarter q: word k (k < 3):
+        // bits 4j..4j+2 = code(8k+j), bit 4j+3 = bit k of code(24+j).  The
+        // comparisons give 0.0 / 1.0 and the words are summed in fp32 as two
+        // 16-bit halves (exact: every partial sum is an integer below 2^16).
+        float h[3][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                v |= (code[8 * k + j] & 7u) << (4 * j);
-                v |= ((code[24 + j] >> k) & 1u) << (4 * j + 3);
+        for (int i = 0; i < 32; ++i) {
+            const float y = x[i];
+            const float a = fabsf(y);
+            const bool b1 = a > T[1];
+            const float f1 = b1 ? 1.f : 0.f;
+            const float f0 = (a > (b1 ? T[2] : T[0])) ? 1.f : 0.f;
+            const float fn = (y > 0.f) ? 0.f : 1.f;
+            if (i < 24) {
+                const int j = i & 7;
+                const float unit = static_cast<float>(1u << (4 * (j & 3)));  // nibble j of the half
+                float& acc = h[i >> 3][j >> 2];
+                acc = fmaf(fn, 4.f * unit, acc);
+                acc = fmaf(f1, 2.f * unit, acc);
+                acc = fmaf(f0, unit, acc);
+            } else {
+                const int j = i - 24;
+                const float bit = static_cast<float>(1u << (4 * (j & 3) + 3));
+                h[0][j >> 2] = fmaf(f0, bit, h[0][j >> 2]);
+                h[1][j >> 2] = fmaf(f1, bit, h[1][j >> 2]);
+                h[2][j >> 2] = fmaf(fn, bit, h[2][j >> 2]);
             }
-            d[k] = v;
         }
+        uint32_t d[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k)
+            d[k] = static_cast<uint32_t>(h[k][0]) | (static_cast<uint32_t>(h[k][1]) << 16);
+        uint32_t* o = reinterpret_cast<uint32_t*>(dst + q * 12);
+        o[0] = d[0];
+        o[1] = d[1];
+        o[2] = d[2];
     }
 }
 
-// Advance lengths[] after the last CTA of the launch: one ticket per CTA
-// (every thread read lengths[] before its CTA takes the ticket, so none sees
-// an advanced length); the counter is back at zero for the next launch.
+// Advance lengths[] after the last CTA of the launch has read it: one ticket
+// per CTA, taken once every thread of the CTA has read lengths[] for the last
+// time (so none sees an advanced length); the counter is back at zero for the
+// next launch.
 __device__ __forceinline__ void finish_append(const EncodeParams& p, int lane) {
     __shared__ unsigned int s_ticket;
     __syncthreads();
@@ -342,60 +394,119 @@ __device__ __forceinline__ void finish_append(const EncodeParams& p, int lane) {
     }
 }
 
-// grid: [K blocks | V blocks]; a CTA of 2 warps encodes 16 vectors of one
-// stream (K or V), 8 per warp, 4 lanes per vector.  KB = 0 copies fp16 K rows.
-constexpr int kEncWarps = 2;
-constexpr int kEncVecs = 8 * kEncWarps;
+// grid: [K blocks | V blocks]; a CTA of 4 warps encodes 128 vectors of one
+// stream (K or V): each warp takes 8 vectors at a time, 4 lanes each, for 4
+// rounds, so a lane's sign masks (its quarter of s) serve 4 vectors.
+// KB = 0 copies fp16 K rows.
+constexpr int kEncWarps = 4;
+constexpr int kEncRounds = 4;
+constexpr int kEncVecs = 8 * kEncWarps * kEncRounds;
 
 template <int KB, int VB>
 __global__ void __launch_bounds__(32 * kEncWarps)
     tq_encode_kernel(const __grid_constant__ EncodeParams p, int k_blocks) {
+    __shared__ unsigned long long s_pos[kEncRounds][32 * kEncWarps];
     griddep_wait();                // inputs and lengths come from earlier work on the stream
     griddep_launch_dependents();   // the decode that follows may start launching
     const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int q = lane & 3;
     const unsigned gmask = 0xFu << (lane & ~3);
     const bool is_v = static_cast<int>(blockIdx.x) >= k_blocks;
-    const long long blk = is_v ? blockIdx.x - k_blocks : blockIdx.x;
-    const long long v = blk * kEncVecs + (threadIdx.x >> 2);  // vector index in the stream
-    const long long nvec = static_cast<long long>(p.batch) * p.hkv * p.t_new;
-    bool valid = v < nvec;
-    const long long vv = valid ? v : 0;
-    const int t = static_cast<int>(vv % p.t_new);
-    const long long bh = vv / p.t_new;
-    const int b = static_cast<int>(bh / p.hkv);
-    const __half* src = (is_v ? p.v_new : p.k_new) + vv * kD;
-    const int L = p.lengths[b];
-    if (valid && (L < 0 || L + p.t_new > p.cap)) {
-        if (q == 0 && !is_v && t == 0 && (bh % p.hkv) == 0) atomicOr(p.status, kStatusCapacity);
-        valid = false;
-    }
-    const size_t pos = valid ? static_cast<size_t>(bh) * p.cap + L + t : 0;
-    if (!is_v) {
-        if constexpr (KB == 0) {
-            if (valid) {
-                const uint4* s4 = reinterpret_cast<const uint4*>(src + q * 32);
-                uint4* d4 = reinterpret_cast<uint4*>(p.k_codes + pos * 256 + q * 64);
+    const int blk = is_v ? static_cast<int>(blockIdx.x) - k_blocks : static_cast<int>(blockIdx.x);
+    // vector counts stay below 2^31 (the host checks), so 32-bit index math
+    const int nvec = p.batch * p.hkv * p.t_new;
+    auto vec_of = [&](int round) { return blk * kEncVecs + (round * kEncWarps + warp) * 8 + (lane >> 2); };
+
+    // Every lane first reads the lengths its rounds write at and keeps the
+    // record positions (or ~0 for no vector); then the CTA takes its ticket,
+    // so the last CTA advances lengths[] while the others are still encoding
+    // (they no longer read it).
+    constexpr unsigned long long kNone = ~0ull;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) d4[i] = s4[i];
+    for (int r = 0; r < kEncRounds; ++r) {
+        const int v = vec_of(r);
+        unsigned long long pos = kNone;
+        if (v < nvec) {
+            const int bh = v / p.t_new;
+            const int t = v - bh * p.t_new;
+            const int L = p.lengths[bh / p.hkv];
+            if (L < 0 || L + p.t_new > p.cap) {
+                if (q == 0 && !is_v && t == 0 && (bh % p.hkv) == 0) atomicOr(p.status, kStatusCapacity);
+            } else {
+                pos = static_cast<unsigned long long>(bh) * p.cap + L + t;
+            }
+        }
+        s_pos[r][threadIdx.x] = pos;
+    }
+    finish_append(p, lane);
+
+    uint32_t hm[16];
+    sign_masks(p.signs[q], hm);
+
+    // round r's vector for this lane, whether it exists, and where it goes
+    struct Slot {
+        const __half* src;
+        size_t pos;
+        bool valid;
+    };
+    const __half* const in_base = is_v ? p.v_new : p.k_new;
+    auto slot = [&](int round) {
+        Slot sl;
+        const unsigned long long pos = s_pos[round][threadIdx.x];
+        sl.valid = pos != kNone;
+        sl.pos = sl.valid ? static_cast<size_t>(pos) : 0;
+        sl.src = in_base + static_cast<size_t>(sl.valid ? vec_of(round) : 0) * kD;
+        return sl;
+    };
+    // the stream this CTA encodes (one code path serves both when K and V have
+    // the same bits)
+    uint8_t* const codes = is_v ? p.v_codes : p.k_codes;
+    __half* const norms = is_v ? p.v_norm : p.k_norm;
+    const float* const tcb = p.table ? (is_v ? p.v_cb : p.k_cb) : nullptr;
+    const float* const gt = is_v ? p.v_gt : p.k_gt;
+    const int rec = is_v ? (p.table ? 64 : VB * 16) : (KB == 0 ? 256 : (p.table ? 64 : KB * 16));
+
+    // the next round's inputs are loaded before this round is encoded
+    Slot cur = slot(0);
+    QuarterIn in = load_quarter_in(cur.src, q, cur.valid);
+#pragma unroll 1
+    for (int round = 0; round < kEncRounds; ++round) {
+        Slot nxt = cur;
+        QuarterIn in_next = in;
+        if (round + 1 < kEncRounds) {
+            nxt = slot(round + 1);
+            in_next = load_quarter_in(nxt.src, q, nxt.valid);
+        }
+        uint8_t* const dst = codes + cur.pos * rec;
+        if constexpr (KB == VB) {
+            encode_group<KB>(in, cur.src, dst, norms + cur.pos, tcb, hm, gt, cur.valid, p.status, q,
+                             gmask);
+        } else if (!is_v) {
+            if constexpr (KB == 0) {
+                if (cur.valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + q * 64);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) d4[i] = in.w[i];
+                }
+            } else {
+                encode_group<KB>(in, cur.src, dst, norms + cur.pos, tcb, hm, gt, cur.valid,
+                                 p.status, q, gmask);
             }
         } else {
-            encode_group<KB>(src, p.k_codes + pos * (p.table ? 64 : KB * 16), p.k_norm + pos,
-                             p.table ? p.k_cb : nullptr, p.signs, p.k_gt, p.k_ge, valid, p.status,
+            encode_group<VB>(in, cur.src, dst, norms + cur.pos, tcb, hm, gt, cur.valid, p.status,
                              q, gmask);
         }
-    } else {
-        encode_group<VB>(src, p.v_codes + pos * (p.table ? 64 : VB * 16), p.v_norm + pos,
-                         p.table ? p.v_cb : nullptr, p.signs, p.v_gt, p.v_ge, valid, p.status, q,
-                         gmask);
+        cur = nxt;
+        in = in_next;
     }
-
-    finish_append(p, lane);
 }
 
 // Small appends (a few tokens per sequence): one warp per vector, lane l holds
 // dims 4l .. 4l+3, so every vector gets its own warp and the dependent chain
-// per lane is short.  Same arithmetic and output as encode_group.
+// per lane is short.  The same output as encode_group, except that elements
+// within ~1e-7 of a midpoint may round the other way: here u itself is formed
+// and compared exactly against the fp32 midpoints.
 template <int BITS>
 __device__ __forceinline__ void encode_vector_warp(const __half* src, uint8_t* dst,
                                                    __half* dst_norm, const float* tcb,
