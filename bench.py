@@ -102,13 +102,28 @@ def append_bytes(w: wl.Workload, t_new: int) -> int:
     return n * (2 * 128 * 2) + n * (rk + rv)
 
 
-def config_dict(w: wl.Workload, step_bytes: float):
+def nominal_step_bytes(w: wl.Workload) -> float:
+    """The bytes one step of the workload reads and writes, as the GPU arms
+    count them for the config's L2 note: the prompt's fp16 q, K and V for a
+    prompt workload, else the first timed step's decode and append bytes."""
+    if w.prompt:
+        return float(w.batch * w.tq * 128 * 2 * (w.num_q_heads + 2 * w.num_kv_heads))
+    lens0 = wl.lengths(w).astype(np.int64)[:w.batch]
+    return float(decode_bytes(w, lens0) + append_bytes(w, max(w.append, 0)))
+
+
+def config_dict(w: wl.Workload):
+    """The workload's config, the same for both arms.  The L2 note follows the
+    decode arm's rule: steps under 2 x L2 flush L2 between steps (the prompt
+    arm always does)."""
     ctx = (f"U[{w.context_min},{w.context}]" if w.ragged else str(w.context))
+    step_bytes = nominal_step_bytes(w)
     return {"workload": w.name, "mode": w.mode, "batch": w.batch, "num_q_heads": w.num_q_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": 128, "context": ctx, "tq": w.tq,
             "append_per_step": max(w.append, 0), "rot_seed": w.rot_seed,
-            "l2": ("inputs larger than L2 (%.0f MB per step > 129 MB)" % (step_bytes / 1e6)
-                   if step_bytes > L2_BYTES else "inputs fit in L2; L2 flushed between steps")}
+            "l2": ("inputs larger than L2 (%.0f MB per step > 2 x 129 MB), no flush" % (step_bytes / 1e6)
+                   if step_bytes >= 2 * L2_BYTES and not w.prompt
+                   else "L2 flushed between steps (%.0f MB per step)" % (step_bytes / 1e6))}
 
 
 # ---------------------------------------------------------------------------
@@ -725,7 +740,7 @@ def main():
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": ts / args.steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": config_dict(w, 0),
+                "config": config_dict(w),
                 "cpu_baseline": {"value": v, "unit": unit, "cores": 1, "kind": "oracle",
                                  "sample": "per step: " + desc},
                 "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0,
@@ -749,7 +764,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16xf16->f32 (mma), fp32 softmax", "data": "synthetic",
-            "config": config_dict(w, r["step_bytes"]),
+            "config": config_dict(w),
             "tokens_per_s": r["tokens_per_s"],
             "pct_of_peak": 100.0 * r["value"] / rf["peak"],
             "roofline": rf, "cpu_baseline": cpu, "e2e": r["e2e"], "clocks": r["clocks"],
