@@ -396,16 +396,16 @@ __device__ __forceinline__ void finish_append(const EncodeParams& p, int lane) {
 
 // grid: [K blocks | V blocks]; a CTA of 4 warps encodes 128 vectors of one
 // stream (K or V): each warp takes 8 vectors at a time, 4 lanes each, for 4
-// rounds, so a lane's sign masks (its quarter of s) serve 4 vectors.
+// passes, so a lane's sign masks (its quarter of s) serve 4 vectors.
 // KB = 0 copies fp16 K rows.
 constexpr int kEncWarps = 4;
-constexpr int kEncRounds = 4;
-constexpr int kEncVecs = 8 * kEncWarps * kEncRounds;
+constexpr int kEncPasses = 4;
+constexpr int kEncVecs = 8 * kEncWarps * kEncPasses;
 
 template <int KB, int VB>
 __global__ void __launch_bounds__(32 * kEncWarps)
     tq_encode_kernel(const __grid_constant__ EncodeParams p, int k_blocks) {
-    __shared__ unsigned long long s_pos[kEncRounds][32 * kEncWarps];
+    __shared__ unsigned long long s_pos[kEncPasses][32 * kEncWarps];
     griddep_wait();                // inputs and lengths come from earlier work on the stream
     griddep_launch_dependents();   // the decode that follows may start launching
     const int lane = threadIdx.x & 31;
@@ -416,15 +416,15 @@ __global__ void __launch_bounds__(32 * kEncWarps)
     const int blk = is_v ? static_cast<int>(blockIdx.x) - k_blocks : static_cast<int>(blockIdx.x);
     // vector counts stay below 2^31 (the host checks), so 32-bit index math
     const int nvec = p.batch * p.hkv * p.t_new;
-    auto vec_of = [&](int round) { return blk * kEncVecs + (round * kEncWarps + warp) * 8 + (lane >> 2); };
+    auto vec_of = [&](int pass) { return blk * kEncVecs + (pass * kEncWarps + warp) * 8 + (lane >> 2); };
 
-    // Every lane first reads the lengths its rounds write at and keeps the
+    // Every lane first reads the lengths its passes write at and keeps the
     // record positions (or ~0 for no vector); then the CTA takes its ticket,
     // so the last CTA advances lengths[] while the others are still encoding
     // (they no longer read it).
     constexpr unsigned long long kNone = ~0ull;
 #pragma unroll
-    for (int r = 0; r < kEncRounds; ++r) {
+    for (int r = 0; r < kEncPasses; ++r) {
         const int v = vec_of(r);
         unsigned long long pos = kNone;
         if (v < nvec) {
@@ -444,19 +444,19 @@ __global__ void __launch_bounds__(32 * kEncWarps)
     uint32_t hm[16];
     sign_masks(p.signs[q], hm);
 
-    // round r's vector for this lane, whether it exists, and where it goes
+    // pass r's vector for this lane, whether it exists, and where it goes
     struct Slot {
         const __half* src;
         size_t pos;
         bool valid;
     };
     const __half* const in_base = is_v ? p.v_new : p.k_new;
-    auto slot = [&](int round) {
+    auto slot = [&](int pass) {
         Slot sl;
-        const unsigned long long pos = s_pos[round][threadIdx.x];
+        const unsigned long long pos = s_pos[pass][threadIdx.x];
         sl.valid = pos != kNone;
         sl.pos = sl.valid ? static_cast<size_t>(pos) : 0;
-        sl.src = in_base + static_cast<size_t>(sl.valid ? vec_of(round) : 0) * kD;
+        sl.src = in_base + static_cast<size_t>(sl.valid ? vec_of(pass) : 0) * kD;
         return sl;
     };
     // the stream this CTA encodes (one code path serves both when K and V have
@@ -467,15 +467,15 @@ __global__ void __launch_bounds__(32 * kEncWarps)
     const float* const gt = is_v ? p.v_gt : p.k_gt;
     const int rec = is_v ? (p.table ? 64 : VB * 16) : (KB == 0 ? 256 : (p.table ? 64 : KB * 16));
 
-    // the next round's inputs are loaded before this round is encoded
+    // the next pass's inputs are loaded before this pass is encoded
     Slot cur = slot(0);
     QuarterIn in = load_quarter_in(cur.src, q, cur.valid);
 #pragma unroll 1
-    for (int round = 0; round < kEncRounds; ++round) {
+    for (int pass = 0; pass < kEncPasses; ++pass) {
         Slot nxt = cur;
         QuarterIn in_next = in;
-        if (round + 1 < kEncRounds) {
-            nxt = slot(round + 1);
+        if (pass + 1 < kEncPasses) {
+            nxt = slot(pass + 1);
             in_next = load_quarter_in(nxt.src, q, nxt.valid);
         }
         uint8_t* const dst = codes + cur.pos * rec;
