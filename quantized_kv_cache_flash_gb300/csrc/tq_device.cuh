@@ -245,35 +245,6 @@ __device__ __forceinline__ void dequant4_word(uint32_t w, const Tables& t, uint3
     }
 }
 
-// Quarter dequantisers that write pair i straight into slot q[i/2][COL + 2*(i%2)]
-// of an 8 x 4 array of MMA operand quads (no register copies to form quads).
-template <int COL>
-__device__ __forceinline__ void dequant3_quarter_q(uint32_t w0, uint32_t w1, uint32_t w2,
-                                                   const Tables& t, uint32_t (&q)[8][4]) {
-    const uint32_t m0 = w0 & 0x77777777u;
-    const uint32_t m1 = w1 & 0x77777777u;
-    const uint32_t m2 = w2 & 0x77777777u;
-    const uint32_t sp = (__umulhi(w0, 1u << 29) & 0x11111111u) |
-                        (__umulhi(w1, 1u << 30) & 0x22222222u) |
-                        (__umulhi(w2, 1u << 31) & 0x44444444u);
-    lut4(m0, t, q[0][COL], q[0][COL + 2]);
-    lut4(__umulhi(m0, 1u << 16), t, q[1][COL], q[1][COL + 2]);
-    lut4(m1, t, q[2][COL], q[2][COL + 2]);
-    lut4(__umulhi(m1, 1u << 16), t, q[3][COL], q[3][COL + 2]);
-    lut4(m2, t, q[4][COL], q[4][COL + 2]);
-    lut4(__umulhi(m2, 1u << 16), t, q[5][COL], q[5][COL + 2]);
-    lut4(sp, t, q[6][COL], q[6][COL + 2]);
-    lut4(__umulhi(sp, 1u << 16), t, q[7][COL], q[7][COL + 2]);
-}
-
-template <int COL>
-__device__ __forceinline__ void dequant4_quarter_q(uint4 w, const Tables& t, uint32_t (&q)[8][4]) {
-    dequant4_word(w.x, t, q[0][COL], q[0][COL + 2], q[1][COL], q[1][COL + 2]);
-    dequant4_word(w.y, t, q[2][COL], q[2][COL + 2], q[3][COL], q[3][COL + 2]);
-    dequant4_word(w.z, t, q[4][COL], q[4][COL + 2], q[5][COL], q[5][COL + 2]);
-    dequant4_word(w.w, t, q[6][COL], q[6][COL + 2], q[7][COL], q[7][COL + 2]);
-}
-
 __device__ __forceinline__ void dequant4_quarter(uint4 w, const Tables& t,
                                                  uint32_t (&h)[16]) {
     dequant4_word(w.x, t, h[0], h[1], h[2], h[3]);
