@@ -9,10 +9,10 @@
 //   S[128 rows x 128 tok]  = Q'[128 x 128] . K^T     (8 MMAs of K = 16, fp32 in TMEM)
 //   O[128 rows x 128 dim] += P[128 x 128 tok] . V    (8 MMAs, fp32 in TMEM)
 // Q' = Rot(q) * scale * log2(e) in fp16; K and V are dequantised once per
-// tile into shared memory as the fp16 centroids c[idx] (the 128-byte-swizzled
-// K-major layout the MMA descriptors read; V stored transposed,
-// [dim][token]); the norms are applied per token in fp32, n_k to the scores
-// and n_v folded into P, as in the decode kernels.
+// tile into shared memory (the 128-byte-swizzled K-major layout the MMA
+// descriptors read): K as the fp16 centroids c[idx], its norm applied to the
+// scores in fp32; V transposed, [dim][token], as fp16 c[idx] * n_v (a tile
+// has half as many V values as P values, so the norm goes there).
 //
 // CTA = 256 threads on one (batch, kv head, pair of 128-row query tiles):
 // thread = one query row (tensor-memory lane) of one tile, so each K/V tile is
@@ -267,12 +267,19 @@ __global__ void __launch_bounds__(256, 1)
             uint32_t ha[16], hb[16];
             dequant_q32<VB>(vrec + ta * C::kRbV + quarter * (C::kRbV / 4), vt, ha);
             dequant_q32<VB>(vrec + tb * C::kRbV + quarter * (C::kRbV / 4), vt, hb);
+            // n_v of both tokens (0 past the end) scales the stored values, so P
+            // itself goes to the MMA: 128 x 128 multiplies a tile instead of the
+            // 256 x 128 of scaling P
+            const __half2 nvab = __floats2half2_rn(colV[ta], colV[tb]);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const int d = 32 * quarter + 2 * k;
-                // (token a, token b) of dims d and d + 1
-                *reinterpret_cast<uint32_t*>(sVt + sw128_offset(d, ta)) = prmt(ha[k], hb[k], 0x5410u);
-                *reinterpret_cast<uint32_t*>(sVt + sw128_offset(d + 1, ta)) = prmt(ha[k], hb[k], 0x7632u);
+                // (token a, token b) of dims d and d + 1, times (n_v(a), n_v(b))
+                const uint32_t w0 = prmt(ha[k], hb[k], 0x5410u), w1 = prmt(ha[k], hb[k], 0x7632u);
+                const __half2 s0 = __hmul2(*reinterpret_cast<const __half2*>(&w0), nvab);
+                const __half2 s1 = __hmul2(*reinterpret_cast<const __half2*>(&w1), nvab);
+                *reinterpret_cast<__half2*>(sVt + sw128_offset(d, ta)) = s0;
+                *reinterpret_cast<__half2*>(sVt + sw128_offset(d + 1, ta)) = s1;
             }
         }
         fence_proxy_async();
@@ -289,8 +296,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(v[e]);
         }
         // t = s * n_k - base in one FFMA per score; the base moves only when a
-        // score passes it by more than 4 (so p <= 16 and p * n_v stays finite
-        // in fp16 for V norms below 4094)
+        // score passes it by more than 4 (so p <= 16 in fp16)
         const bool fresh = (m_base == -INFINITY);
         const float base0 = fresh ? 0.f : m_base;
 #pragma unroll
@@ -337,10 +343,9 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 const int k = 64 * c + 2 * e;
-                const float2 nv = *reinterpret_cast<const float2*>(colV + k);
                 const float p0 = fast_exp2(x[k]), p1 = fast_exp2(x[k + 1]);
                 s += p0 + p1;
-                pk[e] = pack_half2(p0 * nv.x, p1 * nv.y);
+                pk[e] = pack_half2(p0, p1);
             }
             tmem_st32(t_s + 32 * c, pk);  // P over S columns 0..63 (tokens 64c..64c+63)
         }
