@@ -62,6 +62,16 @@ __device__ __forceinline__ void dequant_q32(const uint8_t* rec, const Tables& t,
     }
 }
 
+// Four 8x8 b16 matrices stored transposed: register i of lane 4r + c holds
+// elements (r, 2c) and (r, 2c+1) of matrix i; matrix i's row k lands at the
+// address given by lane 8i + k as elements (0..7, k).
+__device__ __forceinline__ void stsm_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                              uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};\n" ::"r"(addr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
 // In-thread 128-point Walsh-Hadamard transform (unnormalised).
 __device__ __forceinline__ void wht128_thread(float (&x)[128]) {
 #pragma unroll
@@ -255,32 +265,46 @@ __global__ void __launch_bounds__(256, 1)
             umma_commit(bar_s);
         }
 
-        // ---- V(n)^T while S(n) runs: thread = (token pair, quarter of the dims);
-        // a warp covers 32 token pairs of one quarter: each store fills whole
-        // 128-byte rows of V^T ----
+        // ---- V(n)^T while S(n) runs: warp w takes tokens 16w..16w+15, thread
+        // (g, t) = lane 4g + t dequantises quarter t of tokens 16w+g and 16w+g+8
+        // (the MMA fragment layout, so stmatrix.trans writes [dim][token] rows);
+        // V^T rows are stored in the order pi(d) = d ^ 2(d >> 5), which puts the
+        // 8 rows of each stored 8x8 matrix in 8 different 16-byte bank groups
+        // (the epilogue reads O's columns back through the same pi) ----
         {
-            const int pr = tid & 63, quarter = tid >> 6;
-            const int ta = 2 * pr, tb = 2 * pr + 1;
+            const int lane = tid & 31, g = lane >> 2, tq4 = lane & 3;
+            const int ta = 16 * warp + g, tb = ta + 8;
             const uint8_t* vrec = slot + C::kSK + C::kSKn;
             // tokens past the end: stale records still decode to finite
-            // centroids, and their weights are 0
+            // centroids, and their norm (and weight) is 0
             uint32_t ha[16], hb[16];
-            dequant_q32<VB>(vrec + ta * C::kRbV + quarter * (C::kRbV / 4), vt, ha);
-            dequant_q32<VB>(vrec + tb * C::kRbV + quarter * (C::kRbV / 4), vt, hb);
-            // n_v of both tokens (0 past the end) scales the stored values, so P
-            // itself goes to the MMA: 128 x 128 multiplies a tile instead of the
-            // 256 x 128 of scaling P
-            const __half2 nvab = __floats2half2_rn(colV[ta], colV[tb]);
+            dequant_q32<VB>(vrec + ta * C::kRbV + tq4 * (C::kRbV / 4), vt, ha);
+            dequant_q32<VB>(vrec + tb * C::kRbV + tq4 * (C::kRbV / 4), vt, hb);
+            // n_v scales the stored values, so P itself goes to the MMA: 128 x
+            // 128 multiplies a tile instead of the 256 x 128 of scaling P
+            const __half2 na = __float2half2_rn(colV[ta]), nb = __float2half2_rn(colV[tb]);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const int d = 32 * quarter + 2 * k;
-                // (token a, token b) of dims d and d + 1, times (n_v(a), n_v(b))
-                const uint32_t w0 = prmt(ha[k], hb[k], 0x5410u), w1 = prmt(ha[k], hb[k], 0x7632u);
-                const __half2 s0 = __hmul2(*reinterpret_cast<const __half2*>(&w0), nvab);
-                const __half2 s1 = __hmul2(*reinterpret_cast<const __half2*>(&w1), nvab);
-                *reinterpret_cast<__half2*>(sVt + sw128_offset(d, ta)) = s0;
-                *reinterpret_cast<__half2*>(sVt + sw128_offset(d + 1, ta)) = s1;
+                const __half2 a = __hmul2(*reinterpret_cast<const __half2*>(&ha[k]), na);
+                const __half2 b = __hmul2(*reinterpret_cast<const __half2*>(&hb[k]), nb);
+                ha[k] = *reinterpret_cast<const uint32_t*>(&a);
+                hb[k] = *reinterpret_cast<const uint32_t*>(&b);
             }
+            // stmatrix k2 stores dim pairs 2k2 (matrices 0, 1: tokens A, B) and
+            // 2k2+1 (matrices 2, 3); lane 8j + c gives row c of matrix j: dim
+            // d = 32(c>>1) + 2(2k2 + (j>>1)) + (c&1), tokens 16w + 8(j&1) .. + 7
+            const int sj = lane >> 3, sc = lane & 7;
+            const int tokc = 2 * (warp & 3) + (sj & 1);  // 16-byte chunk of the tokens in their row
+            uint32_t vaddr[2];
+#pragma unroll
+            for (int par = 0; par < 2; ++par) {
+                const int row = 32 * (sc >> 1) + 2 * ((((par << 1) | (sj >> 1)) ^ (sc >> 1)) & 3) + (sc & 1);
+                vaddr[par] = smem_u32(sVt) + (warp >> 2) * 16384 + row * 128 + ((tokc ^ (row & 7)) << 4);
+            }
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2)
+                stsm_x4_trans(vaddr[k2 & 1] + 1024 * (k2 >> 1), ha[2 * k2], hb[2 * k2], ha[2 * k2 + 1],
+                              hb[2 * k2 + 1]);
         }
         fence_proxy_async();
 
@@ -397,6 +421,12 @@ __global__ void __launch_bounds__(256, 1)
             else atomicOr(p.status, kStatusShortContext);
 #pragma unroll
             for (int e = 0; e < 128; ++e) o[e] *= inv;
+            // O's column pi(d) holds dim d (V^T rows were stored in pi order)
+            float od[128];
+#pragma unroll
+            for (int d = 0; d < 128; ++d) od[d] = o[d ^ (2 * (d >> 5))];
+#pragma unroll
+            for (int d = 0; d < 128; ++d) o[d] = od[d];
             wht128_thread(o);
             __half* op = p.out + ((static_cast<size_t>(b) * p.hq + h * p.group + hl) * p.tq + j) * kD;
 #pragma unroll
