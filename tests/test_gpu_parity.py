@@ -67,6 +67,7 @@ DECODE_CASES = [
     ("turbo4", 40, 8, 2, [(37 * i) % 290 + 1 for i in range(40)], 1, 304, 0.0, 1.0),  # > 32 sequences
     ("turbo3_table", 2, 8, 2, [37, 1300], 1, 1312, 0.0, 1.0),  # centroid x norm table records
     ("turbo3_table", 1, 32, 8, [2049], 4, 2064, 0.0, 0.5),     # 16 rows, causal block
+    ("turbo4", 1, 4, 1, [40000], 1, 40000, 0.0, 1.0),          # > 128 partials for one row
 ]
 
 
