@@ -4,7 +4,6 @@ the same context keeps working (a decode right after matches the oracle)."""
 import math
 import time
 
-import numpy as np
 import pytest
 
 torch = pytest.importorskip("torch")

@@ -9,7 +9,6 @@ call reuses (and leaves behind) the same scratch.
 """
 import ctypes
 
-import numpy as np
 import pytest
 
 torch = pytest.importorskip("torch")
