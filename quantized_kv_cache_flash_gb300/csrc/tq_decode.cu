@@ -572,45 +572,74 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, NT, TAB>::kMinCtas)
                     }
                 }
 
-                // ---------------- O^T += C_v^T . (P n_v)^T (rotated basis) ----------------
-        #pragma unroll
-                for (int tile = 0; tile < 2; ++tile) {
-                    if (!FULL && tile == 1 && !two) break;
-                    if (!keep[tile]) continue;
-                    uint32_t pb0[NT], pb1[NT];
-        #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        pb0[n] = movtrans(pack_half2(x[tile][n][0] * nv[tile][0], x[tile][n][1] * nv[tile][0]));
-                        pb1[n] = movtrans(pack_half2(x[tile][n][2] * nv[tile][1], x[tile][n][3] * nv[tile][1]));
-                    }
-                    // A quad of dim tile mt: transposed pairs 2mt, 2mt+1 of token block 0
-                    // (tokens 0-7 of the tile) then of block 1 (tokens 8-15); group J of
-                    // both tokens feeds dim tiles 2J and 2J+1
-                    const uint8_t* rva = st + C::kVOff + (tile * 16 + g) * C::kRbV;
-                    const uint8_t* rvb = st + C::kVOff + (tile * 16 + g + 8) * C::kRbV;
-                    const QuarterWords va = load_quarter<VB>(rva + t * C::kQuarterV);
-                    const QuarterWords vb = load_quarter<VB>(rvb + t * C::kQuarterV);
-                    const Tables tva = TAB ? v_tables<FULL>(rva, tok0 + tile * 16 + g < t_end) : vt;
-                    const Tables tvb = TAB ? v_tables<FULL>(rvb, tok0 + tile * 16 + g + 8 < t_end) : vt;
-                    auto vgroup = [&](auto jtag) {
-                        constexpr int J = decltype(jtag)::value;
-                        uint32_t ha[4], hb[4];
-                        dequant_group<VB, J>(va, tva, ha);
-                        dequant_group<VB, J>(vb, tvb, hb);
-        #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const uint32_t v0 = movtrans(ha[2 * e]), v1 = movtrans(ha[2 * e + 1]);
-                            const uint32_t v2 = movtrans(hb[2 * e]), v3 = movtrans(hb[2 * e + 1]);
-        #pragma unroll
-                            for (int n = 0; n < NT; ++n) mma_f16(O[n][2 * J + e], v0, v1, v2, v3, pb0[n], pb1[n]);
-                        }
-                    };
-                    vgroup(std::integral_constant<int, 0>{});
-                    vgroup(std::integral_constant<int, 1>{});
-                    vgroup(std::integral_constant<int, 2>{});
-                    vgroup(std::integral_constant<int, 3>{});
-                }
+                // p <= 2^kSlack = 16, so p * n_v fits fp16 for V norms up to 4094.
+                // A chunk holding a larger norm (warp-uniform, rare) scales the
+                // dequantised V values instead (|c| * n_v <= 0.25 * 65504) and
+                // sends p itself to the MMA.
+                bool bigv = false;
+                if constexpr (!TAB)
+                    bigv = __any_sync(0xffffffffu, fmaxf(fmaxf(nv[0][0], nv[0][1]), fmaxf(nv[1][0], nv[1][1])) > 2048.f);
+                (void)bigv;
 
+                // ---------------- O^T += C_v^T . (P n_v)^T (rotated basis) ----------------
+                auto vpass = [&](auto big_tag) {
+                    constexpr bool BIG = decltype(big_tag)::value;
+        #pragma unroll
+                    for (int tile = 0; tile < 2; ++tile) {
+                        if (!FULL && tile == 1 && !two) break;
+                        if (!keep[tile]) continue;
+                        const float pa = BIG ? 1.f : nv[tile][0], pbn = BIG ? 1.f : nv[tile][1];
+                        uint32_t pb0[NT], pb1[NT];
+        #pragma unroll
+                        for (int n = 0; n < NT; ++n) {
+                            pb0[n] = movtrans(pack_half2(x[tile][n][0] * pa, x[tile][n][1] * pa));
+                            pb1[n] = movtrans(pack_half2(x[tile][n][2] * pbn, x[tile][n][3] * pbn));
+                        }
+                        // A quad of dim tile mt: transposed pairs 2mt, 2mt+1 of token block 0
+                        // (tokens 0-7 of the tile) then of block 1 (tokens 8-15); group J of
+                        // both tokens feeds dim tiles 2J and 2J+1
+                        const uint8_t* rva = st + C::kVOff + (tile * 16 + g) * C::kRbV;
+                        const uint8_t* rvb = st + C::kVOff + (tile * 16 + g + 8) * C::kRbV;
+                        const QuarterWords va = load_quarter<VB>(rva + t * C::kQuarterV);
+                        const QuarterWords vb = load_quarter<VB>(rvb + t * C::kQuarterV);
+                        const Tables tva = TAB ? v_tables<FULL>(rva, tok0 + tile * 16 + g < t_end) : vt;
+                        const Tables tvb = TAB ? v_tables<FULL>(rvb, tok0 + tile * 16 + g + 8 < t_end) : vt;
+                        auto vgroup = [&](auto jtag) {
+                            constexpr int J = decltype(jtag)::value;
+                            uint32_t ha[4], hb[4];
+                            dequant_group<VB, J>(va, tva, ha);
+                            dequant_group<VB, J>(vb, tvb, hb);
+                            if constexpr (BIG) {  // c * n_v per token (tokens g and g + 8 of the tile)
+                                const __half2 sa = __float2half2_rn(nv[tile][0]);
+                                const __half2 sb = __float2half2_rn(nv[tile][1]);
+        #pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const __half2 ca = __hmul2(*reinterpret_cast<const __half2*>(&ha[i]), sa);
+                                    const __half2 cb = __hmul2(*reinterpret_cast<const __half2*>(&hb[i]), sb);
+                                    ha[i] = *reinterpret_cast<const uint32_t*>(&ca);
+                                    hb[i] = *reinterpret_cast<const uint32_t*>(&cb);
+                                }
+                            }
+        #pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const uint32_t v0 = movtrans(ha[2 * e]), v1 = movtrans(ha[2 * e + 1]);
+                                const uint32_t v2 = movtrans(hb[2 * e]), v3 = movtrans(hb[2 * e + 1]);
+        #pragma unroll
+                                for (int n = 0; n < NT; ++n) mma_f16(O[n][2 * J + e], v0, v1, v2, v3, pb0[n], pb1[n]);
+                            }
+                        };
+                        vgroup(std::integral_constant<int, 0>{});
+                        vgroup(std::integral_constant<int, 1>{});
+                        vgroup(std::integral_constant<int, 2>{});
+                        vgroup(std::integral_constant<int, 3>{});
+                    }
+                };
+                if constexpr (TAB) {
+                    vpass(std::false_type{});
+                } else {
+                    if (bigv) vpass(std::true_type{});
+                    else vpass(std::false_type{});
+                }
         };
 
         int c = warp;

@@ -87,6 +87,28 @@ def test_decode_same_cache(case):
     H.assert_attention_close(got, want, str(case))
 
 
+@pytest.mark.parametrize("mode,Hq,Tq,scale_v", [("turbo4", 8, 1, 1000.0), ("turbo3", 32, 1, 3000.0),
+                                               ("turbo4k_3v", 8, 2, 1000.0), ("turbo4_asym", 4, 1, 2000.0)])
+def test_decode_large_v_norms(mode, Hq, Tq, scale_v):
+    # V norms ~ 6e3..5e4: p * n_v would overflow fp16 for p up to 16, so these
+    # chunks scale the dequantised V values instead; chunk 0 of the second
+    # sequence keeps ordinary norms (both paths in one launch)
+    B, Hkv, cap = 2, 2, 3008
+    kd, kn, vd, vn = H.random_cache(mode, B, Hkv, cap, 321)
+    vn = (vn.astype(np.float32) * scale_v).astype(np.float16)
+    vn[1, :, :32] = (vn[1, :, :32].astype(np.float32) / scale_v).astype(np.float16)
+    assert np.isfinite(vn).all()
+    q = wl.random_fp16(322, (B, Hq, Tq, 128))
+    lengths = [3000, 1700]
+    cache = H.gpu_cache_from_records(mode, B, Hkv, cap, lengths, kd, kn, vd, vn, DEV)
+    got, status, _ = _run_decode(cache, q, Tq, 3000)
+    assert status == 0
+    units = {(b, h): H.oracle_unit_from_records(mode, kd, kn, vd, vn, b, h, lengths[b])
+             for b in range(B) for h in range(Hkv)}
+    want = H.oracle_decode(mode, q, units, lengths, Hkv, Tq, 1 / math.sqrt(128), 1.0)
+    H.assert_attention_close(got, want, mode)
+
+
 def test_decode_short_context_rows_are_zero_and_flagged():
     # lengths 2 with a 4-query block: rows j = 0, 1 see no token
     mode, B, Hq, Hkv, cap = "turbo3", 1, 2, 1, 16
