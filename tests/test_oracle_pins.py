@@ -224,6 +224,61 @@ def test_nearest_index_bruteforce_near_every_threshold(bits):
         assert int(g) == _argmin_exact(u, cb), u
 
 
+def _boundary_distance_exact(u: float, cb32: np.ndarray) -> Fraction:
+    """Distance from u to the nearest decision midpoint (c_j + c_{j+1}) / 2,
+    in exact rationals over the fp64 value of u and the fp32 levels."""
+    uf = Fraction(float(u))
+    cs = [Fraction(float(c)) for c in cb32]
+    return min(abs(uf - (cs[j] + cs[j + 1]) / 2) for j in range(len(cs) - 1))
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_boundary_distance_bruteforce_and_closed_forms(bits):
+    """The distance that exempts encode mismatches near a decision boundary.
+
+    Pinned by exact rational brute force over fp64 u values placed a few fp64
+    steps and a few fp32 steps around every midpoint (so taking the distance
+    from the fp32-rounded u, or from the levels instead of the midpoints,
+    fails), at every level and far outside the codebook."""
+    cb = o.codebook(bits)
+    c = [Fraction(float(x)) for x in cb]
+    us = []
+    for j in range(len(cb) - 1):
+        mid = float((c[j] + c[j + 1]) / 2)
+        assert Fraction(mid) == (c[j] + c[j + 1]) / 2     # fp64 holds the midpoint exactly
+        for k in (-3, -1, 0, 1, 2):
+            us.append(mid + k * 2.0 ** -52 * abs(mid))      # fp64 steps: far below fp32 resolution
+            us.append(float(np.float32(mid)) + k * float(np.spacing(np.float32(mid))))
+        us.append(mid + 3e-6)
+        us.append(mid - 7e-6)
+    us += [float(x) for x in cb] + [0.0, -0.0, 5.0, -5.0]
+    rng = np.random.default_rng(bits + 40)
+    us += list(rng.standard_normal(200) * 0.12)
+    u = np.array(us, np.float64)
+    got = o.boundary_distance(u, cb)
+    for ui, g in zip(us, got):
+        want = _boundary_distance_exact(ui, cb)
+        assert abs(Fraction(float(g)) - want) <= Fraction(2.0 ** -50) * (abs(Fraction(ui)) + 1), ui
+    # closed forms: a midpoint is at distance 0, a level at half the gap to its
+    # nearer neighbour, and a value beyond the codebook at its distance to the
+    # outermost midpoint
+    for j in range(len(cb) - 1):
+        mid = float((c[j] + c[j + 1]) / 2)
+        assert o.boundary_distance(np.array([mid]), cb)[0] == 0.0
+    for j in range(len(cb)):
+        gaps = [c[j] - c[j - 1]] if j > 0 else []
+        gaps += [c[j + 1] - c[j]] if j + 1 < len(cb) else []
+        assert math.isclose(o.boundary_distance(np.array([float(c[j])]), cb)[0],
+                            float(min(gaps) / 2), rel_tol=1e-14)
+    top_mid = (c[-2] + c[-1]) / 2
+    assert math.isclose(o.boundary_distance(np.array([5.0]), cb)[0], float(5 - top_mid),
+                        rel_tol=1e-14)
+    # an element 1e-12 past a midpoint (the same fp32 value as the midpoint)
+    # is 1e-12 from it, not 0
+    mid0 = float((c[0] + c[1]) / 2)
+    assert math.isclose(o.boundary_distance(np.array([mid0 + 1e-12]), cb)[0], 1e-12, rel_tol=1e-3)
+
+
 def test_zero_vector_encodes_to_lower_middle_index():
     for bits in (3, 4):
         idx, n16, _, ov = o.encode(np.zeros((2, 128), np.float16), o.codebook(bits),
