@@ -26,7 +26,7 @@
  *     are detected on the host before any launch; nothing is launched then.
  *   - Calls are asynchronous on the given stream (a cudaStream_t passed as
  *     void*, NULL = legacy default stream) and never synchronize, except
- *     tq_get_status and tq_get_kernel_time.
+ *     tq_get_status (its context's latest stream) and tq_get_kernel_time.
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     never frees them.  The library owns only the context (workspace, status
  *     word, cached tables), created lazily when *ctx == NULL and released by
@@ -170,7 +170,8 @@ int tq_decode_attention(tq_ctx **ctx, const tq_cache *cache, const void *q,
  * measurement sweep, advisor commit of pull request #369.)
  *   Arguments and layouts as tq_decode_attention; any tq >= 1 and any group
  *   size up to 128 (num_q_heads / num_kv_heads); batch * num_kv_heads at most
- *   65535.  TQ_TURBO3_TABLE is not supported (TQ_ERR_UNSUPPORTED).
+ *   65535.  TQ_TURBO3_TABLE, and a K codebook whose entries are not all fp16
+ *   values, are not supported (TQ_ERR_UNSUPPORTED).
  *   The call allocates nothing beyond the context created on first use.
  */
 int tq_prefill_attention(tq_ctx **ctx, const tq_cache *cache, const void *q,
@@ -237,13 +238,21 @@ int tq_selftest_bounded_wait(tq_ctx **ctx, int32_t limit_us, void *stream);
 /* Release a context (device memory included).  tq_free(NULL) is a no-op. */
 void tq_free(tq_ctx *ctx);
 
-/* Synchronize the device, return the device status bits in *status and clear
- * them.  Returns TQ_ERR_CUDA if the device reported an error. */
+/* Return the device status bits in *status and clear them.  The read is
+ * ordered on the stream of the context's most recent call and waits for that
+ * stream only (not the whole device); bits that work still running on other
+ * streams sets later show in a later read.  Returns TQ_ERR_CUDA if the stream
+ * reported an error. */
 int tq_get_status(tq_ctx *ctx, uint32_t *status);
 
-/* Host-only: the Lloyd-Max codebook of N(0, 1/128) with 2^bits levels
- * (bits in 1..4), iterated in double precision to a fixed point and rounded to
- * fp32, ascending, into out[0 .. 2^bits-1]. */
+/* Host-only: the standard codebook: the Lloyd-Max levels of N(0, 1/128) with
+ * 2^bits levels (bits in 1..4), iterated in double precision to a fixed point
+ * and rounded to the nearest fp16 value (the half-precision centroid tables of
+ * the smem-dequant experiment and of the mlxcel dequant), ascending, as fp32
+ * values into out[0 .. 2^bits-1].  Any other strictly ascending, exactly
+ * symmetric fp32 codebook is accepted by the calls too; one whose entries are
+ * not all fp16 values takes a slower decode path that adds the entries'
+ * fp16 rounding residuals to every score. */
 int tq_lloyd_max_codebook(int32_t bits, float *out);
 
 /* Host-only: bytes of one packed record: 48 (bits 3), 64 (bits 4), 256 (16 = fp16). */

@@ -16,8 +16,9 @@ What it computes (plain, slow, obviously correct; float64 unless stated):
   Walsh-Hadamard rotated basis of mlxcel PR #369 (Change), over the 128-element
   rotation group of turboquant_plus smem-dequant-experiment.md (Hypothesis 1).
 * Codebook: Lloyd-Max quantiser of N(0, 1/128) with 2^b levels, iterated in
-  fp64 to a fixed point and rounded to fp32; the fp32 values are the codebook
-  both sides use.  The 3-bit codebook is a sign and four magnitudes (the
+  fp64 to a fixed point and rounded to fp16 (the half-precision centroid
+  tables of the pages); those values, carried as fp32, are the standard
+  codebook both sides use (any symmetric fp32 codebook can be given instead).  The 3-bit codebook is a sign and four magnitudes (the
   four-magnitude lookup table of smem-dequant-experiment.md); the 4-bit one is
   the V codec of mlxcel PR #369 (Result).
 * Encode: n16 = fp16 round-to-nearest-even of the exact L2 norm of the fp16
@@ -134,9 +135,17 @@ def lloyd_max(levels: int, sigma: float = 1.0 / math.sqrt(D), tol: float = 1e-15
 
 
 def codebook(bits: int) -> np.ndarray:
-    """The fp32 codebook (2^bits entries, ascending) both sides quantise with."""
+    """The standard codebook (2^bits entries, ascending) both sides quantise
+    with: the Lloyd-Max levels rounded to the nearest fp16 value (ties to
+    even), carried as fp32 (every fp16 value is one).  The pages' centroid
+    lookup tables and dequantized caches are half precision (the turbo3
+    dequant into a half4 buffer and the fp16 centroid x norm table of the
+    smem-dequant experiment, the FP16 dequantized V of mlxcel PR #369), so
+    the levels are fp16 values; the rounding moves each level by at most
+    2^-12 of itself.  Any other symmetric fp32 codebook may be passed to
+    both sides instead."""
     c64, _, _ = lloyd_max(1 << bits)
-    return c64.astype(np.float32)
+    return c64.astype(np.float16).astype(np.float32)
 
 
 # --------------------------------------------------------------------------

@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtq.so")
 
-SOURCES = ["tq_api.cu", "tq_decode.cu", "tq_encode.cu", "tq_noalloc.cu", "tq_prefill.cu"]
+SOURCES = ["tq_api.cu", "tq_decode.cu", "tq_decode_f.cu", "tq_decode_q.cu", "tq_decode_r.cu",
+           "tq_encode.cu", "tq_noalloc.cu", "tq_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

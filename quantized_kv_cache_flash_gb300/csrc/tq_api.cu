@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/tq.h: argument checks, codebook
 // tables, sign vector, split planning, workspace, launches.
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
 #include <cmath>
@@ -15,43 +16,19 @@
 namespace {
 
 constexpr int kD = 128;
-constexpr int kSMs = 152;  // GB300 (only used to size the split grid)
 
 struct EventPair {
     cudaEvent_t a = nullptr, b = nullptr;
 };
 
-struct CodebookTables {
-    bool valid = false;
-    int bits = 0;
-    float cb[16] = {};
-    uint32_t tab[4] = {};  // prmt byte tables
-    float gt[7] = {}, ge[7] = {};
-};
+using tq::host::CodebookTables;
 
 }  // namespace
 
-struct tq_ctx {
-    int device = -1;
-    uint32_t* d_words = nullptr;  // [0] status, [1] encode ticket counter
-    float* d_work = nullptr;
-    size_t work_bytes = 0;
-    CodebookTables ktab, vtab;
-    bool signs_valid = false;
-    uint64_t seed = 0;
-    uint32_t signs[4] = {};
-    // tensor map of the fp16 K rows (rebuilt when the buffer or shape changes)
-    CUtensorMap kmap;
-    const void* kmap_ptr = nullptr;
-    uint64_t kmap_rows = 0;
-    bool timing = false;
-    std::vector<EventPair> events;
-    size_t events_used = 0;
-};
+namespace tq {
+namespace host {
 
-namespace {
-
-int cuda_err(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
+int cuda_err_code(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -126,6 +103,25 @@ int build_tables(const float* cb, int n, int bits, CodebookTables* t) {
     t->tab[1] = word(lo + 4);
     t->tab[2] = word(hi);
     t->tab[3] = word(hi + 4);
+    // the rounding residuals of the same 8 entries, exact in double, scaled
+    // by 2^a so the largest lands in [128, 256) (e4m3 holds up to 448)
+    double res[8];
+    double rmax = 0.0;
+    for (int k = 0; k < 8; ++k) {
+        const double v = (bits == 3) ? ((k & 4) ? -double(cb[h + (k & 3)]) : double(cb[h + (k & 3)]))
+                                     : double(cb[h + k]);
+        res[k] = v - double(__half2float(__float2half_rn(float(v))));
+        rmax = std::max(rmax, std::fabs(res[k]));
+    }
+    int e = 0;
+    if (rmax > 0.0) (void)std::frexp(rmax, &e);
+    t->res_shift = rmax > 0.0 ? 8 - e : 0;
+    uint8_t r8[8];
+    for (int k = 0; k < 8; ++k)
+        r8[k] = static_cast<uint8_t>(
+            __nv_cvt_double_to_fp8(std::ldexp(res[k], t->res_shift), __NV_SATFINITE, __NV_E4M3));
+    t->tab8[0] = word(r8);
+    t->tab8[1] = word(r8 + 4);
     // thresholds between positive neighbours: tau_k = (m[k] + m[k+1]) / 2 exactly
     for (int k = 0; k < 7; ++k) t->gt[k] = t->ge[k] = INFINITY;
     for (int k = 0; k + 1 < h; ++k) {
@@ -141,6 +137,195 @@ int build_tables(const float* cb, int n, int bits, CodebookTables* t) {
     t->valid = true;
     return TQ_OK;
 }
+
+int check_cache(const tq_cache* c, int* kb, int* vb) {
+    if (c == nullptr) return TQ_ERR_INVALID_ARG;
+    int r = tq::mode_bits(c->mode, kb, vb);
+    if (r != TQ_OK) return r;
+    if (c->head_dim != kD) return TQ_ERR_UNSUPPORTED;
+    if (c->batch <= 0 || c->num_kv_heads <= 0 || c->capacity <= 0 || (c->capacity % 16) != 0)
+        return TQ_ERR_INVALID_ARG;
+    const bool table = tq::mode_table(c->mode);  // table records: no norm arrays
+    if (c->k_data == nullptr || c->v_data == nullptr || c->lengths == nullptr)
+        return TQ_ERR_INVALID_ARG;
+    if (!table && (c->v_norm == nullptr || (*kb != 16 && c->k_norm == nullptr)))
+        return TQ_ERR_INVALID_ARG;
+    if (!aligned16(c->k_data) || !aligned16(c->v_data) || (c->v_norm && !aligned16(c->v_norm)) ||
+        (c->k_norm && !aligned16(c->k_norm)))
+        return TQ_ERR_INVALID_ARG;
+    const long long rows = 1ll * c->batch * c->num_kv_heads * c->capacity;
+    if (rows >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;
+    if (*kb != 16 && (r = check_codebook(c->codebook_k, c->codebook_k_size, *kb)) != TQ_OK) return r;
+    if ((r = check_codebook(c->codebook_v, c->codebook_v_size, *vb)) != TQ_OK) return r;
+    return TQ_OK;
+}
+
+// The driver's tensor-map encoder, looked up once per process.
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool codebook_is_fp16(const float* cb, int n) {
+    for (int j = 0; j < n; ++j)
+        if (__half2float(__float2half_rn(cb[j])) != cb[j]) return false;
+    return true;
+}
+
+// fp16 K rows [B*Hkv*cap, 128] as a 2-D tensor, boxes of 32 rows x 64 halves
+// (128 bytes, 128-byte swizzle).
+int encode_kmap(CUtensorMap* map, const tq_cache* c) {
+    const uint64_t rows = uint64_t(c->batch) * c->num_kv_heads * c->capacity;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_tiled();
+    if (enc == nullptr) return TQ_ERR_CUDA;
+    cuuint64_t dims[2] = {kD, rows};
+    cuuint64_t strides[1] = {kD * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c->k_data, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TQ_OK : TQ_ERR_CUDA;
+}
+
+constexpr int kSMs = 152;  // GB300 (only used to size the split grid)
+
+// Decode grid: two waves of resident CTAs (the second lets the block
+// scheduler even out SMs that run at different speeds), fewer when the
+// context (at the hint length) gives a CTA less than two 32-token chunks per
+// warp.
+int plan_ctas(int kb, int vb, bool table, bool res, int group_rows, long long units, int max_len) {
+    const long long slots = 2ll * kSMs * tq::decode_ctas_per_sm(kb, vb, group_rows, table, res);
+    const long long chunks = units * ((max_len + 31) / 32);
+    long long ctas = std::min(slots, (chunks + 7) / 8);
+    return int(std::max<long long>(ctas, 1));
+}
+
+int plan_decode(const tq_cache* c, const void* q, const void* out, int num_q_heads, int tq_rows,
+                int max_len_hint, float scale, DecodePlan* pl) {
+    int r = check_cache(c, &pl->kb, &pl->vb);
+    if (r != TQ_OK) return r;
+    if (q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+    if (tq_rows <= 0 || max_len_hint <= 0 || max_len_hint > c->capacity) return TQ_ERR_INVALID_ARG;
+    if (tq_rows > max_len_hint) return TQ_ERR_INVALID_ARG;
+    if (!(scale >= 0.f) || !std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
+    if (!std::isfinite(c->v_rescale)) return TQ_ERR_INVALID_ARG;
+    pl->group = num_q_heads / c->num_kv_heads;
+    pl->rows = pl->group * tq_rows;
+    if (pl->rows > 256) return TQ_ERR_UNSUPPORTED;
+    pl->group_rows = tq::group_rows_for(pl->rows, pl->kb);
+    pl->row_groups = (pl->rows + pl->group_rows - 1) / pl->group_rows;
+    pl->units = 1ll * c->batch * c->num_kv_heads * pl->row_groups;
+    pl->res = pl->kb != 16 && !tq::mode_table(c->mode) && !codebook_is_fp16(c->codebook_k, c->codebook_k_size);
+    pl->ctas = plan_ctas(pl->kb, pl->vb, tq::mode_table(c->mode), pl->res, pl->group_rows, pl->units,
+                         max_len_hint);
+    return TQ_OK;
+}
+
+int launch_decode_plan(const DecodePlan& pl, const tq_cache* c, const CodebookTables& kt,
+                       const CodebookTables& vt, const uint32_t signs[4], const CUtensorMap* kmap,
+                       const void* q, int num_q_heads, int tq_rows, int max_len_hint, float scale,
+                       float tau, void* out, float* part, uint32_t* status, cudaStream_t stream,
+                       cudaEvent_t ev0, cudaEvent_t ev1) {
+    const size_t slots = decode_slots(pl);
+    const float sc = (scale == 0.f) ? 1.0f / std::sqrt(float(kD)) : scale;
+    tq::DecodeParams p{};
+    p.k_codes = static_cast<const uint8_t*>(c->k_data);
+    p.k_norm = static_cast<const __half*>(c->k_norm);
+    p.v_codes = static_cast<const uint8_t*>(c->v_data);
+    p.v_norm = static_cast<const __half*>(c->v_norm);
+    p.lengths = c->lengths;
+    p.q = static_cast<const __half*>(q);
+    p.part_o = part;
+    p.part_ml = part + slots * kD;
+    p.status = status;
+    p.batch = c->batch;
+    p.hkv = c->num_kv_heads;
+    p.hq = num_q_heads;
+    p.group = pl.group;
+    p.tq = tq_rows;
+    p.rows = pl.rows;
+    p.row_groups = pl.row_groups;
+    p.group_rows = pl.group_rows;
+    p.cap = c->capacity;
+    p.max_len = max_len_hint;
+    p.num_ctas = pl.ctas;
+    p.scale_log2e = sc * 1.4426950408889634f;
+    p.sparse_tau = tau;
+    p.table = tq::mode_table(c->mode) ? 1 : 0;
+    if (pl.kb != 16) {
+        std::memcpy(p.ktab, kt.tab, sizeof(p.ktab));
+        std::memcpy(p.ktab8, kt.tab8, sizeof(p.ktab8));
+        p.res_shift = kt.res_shift;
+        p.k_res = pl.res ? 1 : 0;
+    }
+    std::memcpy(p.vtab, vt.tab, sizeof(p.vtab));
+    std::memcpy(p.signs, signs, sizeof(p.signs));
+    CUtensorMap dummy;
+    std::memset(&dummy, 0, sizeof(dummy));
+    if (tq::launch_decode(pl.kb, pl.vb, p, pl.kb == 16 ? kmap : &dummy, stream, ev0, ev1) != 0)
+        return TQ_ERR_CUDA;
+
+    tq::CombineParams cp{};
+    cp.part_o = p.part_o;
+    cp.part_ml = p.part_ml;
+    cp.lengths = c->lengths;
+    cp.out = static_cast<__half*>(out);
+    cp.status = status;
+    cp.batch = c->batch;
+    cp.hkv = c->num_kv_heads;
+    cp.hq = num_q_heads;
+    cp.group = pl.group;
+    cp.tq = tq_rows;
+    cp.row_groups = pl.row_groups;
+    cp.group_rows = pl.group_rows;
+    cp.max_len = max_len_hint;
+    cp.num_ctas = pl.ctas;
+    cp.v_rescale = c->v_rescale;
+    std::memcpy(cp.signs, signs, sizeof(cp.signs));
+    return cuda_err_code(static_cast<cudaError_t>(tq::launch_combine(cp, stream)));
+}
+
+}  // namespace host
+}  // namespace tq
+
+struct tq_ctx {
+    int device = -1;
+    uint32_t* d_words = nullptr;  // [0] status, [1] encode ticket counter
+    float* d_work = nullptr;
+    size_t work_bytes = 0;
+    CodebookTables ktab, vtab;
+    bool signs_valid = false;
+    uint64_t seed = 0;
+    uint32_t signs[4] = {};
+    // tensor map of the fp16 K rows (rebuilt when the buffer or shape changes)
+    CUtensorMap kmap;
+    const void* kmap_ptr = nullptr;
+    uint64_t kmap_rows = 0;
+    bool timing = false;
+    // stream of the most recent call that used this context (status reads
+    // are ordered after it)
+    cudaStream_t last_stream = nullptr;
+    std::vector<EventPair> events;
+    size_t events_used = 0;
+};
+
+namespace {
+
+int cuda_err(cudaError_t e) { return tq::host::cuda_err_code(e); }
+using tq::host::aligned16;
+using tq::host::build_tables;
+using tq::host::check_cache;
+using tq::host::make_signs;
 
 int get_ctx(tq_ctx** pctx, tq_ctx** out) {
     if (pctx == nullptr) return TQ_ERR_INVALID_ARG;
@@ -167,28 +352,6 @@ int get_ctx(tq_ctx** pctx, tq_ctx** out) {
     return TQ_OK;
 }
 
-int check_cache(const tq_cache* c, int* kb, int* vb) {
-    if (c == nullptr) return TQ_ERR_INVALID_ARG;
-    int r = tq::mode_bits(c->mode, kb, vb);
-    if (r != TQ_OK) return r;
-    if (c->head_dim != kD) return TQ_ERR_UNSUPPORTED;
-    if (c->batch <= 0 || c->num_kv_heads <= 0 || c->capacity <= 0 || (c->capacity % 16) != 0)
-        return TQ_ERR_INVALID_ARG;
-    const bool table = tq::mode_table(c->mode);  // table records: no norm arrays
-    if (c->k_data == nullptr || c->v_data == nullptr || c->lengths == nullptr)
-        return TQ_ERR_INVALID_ARG;
-    if (!table && (c->v_norm == nullptr || (*kb != 16 && c->k_norm == nullptr)))
-        return TQ_ERR_INVALID_ARG;
-    if (!aligned16(c->k_data) || !aligned16(c->v_data) || (c->v_norm && !aligned16(c->v_norm)) ||
-        (c->k_norm && !aligned16(c->k_norm)))
-        return TQ_ERR_INVALID_ARG;
-    const long long rows = 1ll * c->batch * c->num_kv_heads * c->capacity;
-    if (rows >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;
-    if (*kb != 16 && (r = check_codebook(c->codebook_k, c->codebook_k_size, *kb)) != TQ_OK) return r;
-    if ((r = check_codebook(c->codebook_v, c->codebook_v_size, *vb)) != TQ_OK) return r;
-    return TQ_OK;
-}
-
 int prepare_tables(tq_ctx* ctx, const tq_cache* c, int kb, int vb) {
     if (kb != 16) {
         int r = build_tables(c->codebook_k, c->codebook_k_size, kb, &ctx->ktab);
@@ -204,48 +367,15 @@ int prepare_tables(tq_ctx* ctx, const tq_cache* c, int kb, int vb) {
     return TQ_OK;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_tiled() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// fp16 K rows [B*Hkv*cap, 128] as a 2-D tensor, boxes of 32 rows x 64 halves
-// (128 bytes, 128-byte swizzle).
+// The fp16 K tensor map, re-encoded when the buffer or its shape changes.
 int prepare_kmap(tq_ctx* ctx, const tq_cache* c) {
     const uint64_t rows = uint64_t(c->batch) * c->num_kv_heads * c->capacity;
     if (ctx->kmap_ptr == c->k_data && ctx->kmap_rows == rows) return TQ_OK;
-    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_tiled();
-    if (enc == nullptr) return TQ_ERR_CUDA;
-    cuuint64_t dims[2] = {kD, rows};
-    cuuint64_t strides[1] = {kD * 2};
-    cuuint32_t box[2] = {64, 32};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&ctx->kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, c->k_data, dims, strides, box,
-                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return TQ_ERR_CUDA;
+    const int r = tq::host::encode_kmap(&ctx->kmap, c);
+    if (r != TQ_OK) return r;
     ctx->kmap_ptr = c->k_data;
     ctx->kmap_rows = rows;
     return TQ_OK;
-}
-
-// Decode grid: two waves of resident CTAs (the second lets the block
-// scheduler even out SMs that run at different speeds), fewer when the
-// context (at the hint length) gives a CTA less than two 32-token chunks per
-// warp.
-int plan_ctas(int kb, int vb, bool table, int group_rows, long long units, int max_len) {
-    const long long slots = 2ll * kSMs * tq::decode_ctas_per_sm(kb, vb, group_rows, table);
-    const long long chunks = units * ((max_len + 31) / 32);
-    long long ctas = std::min(slots, (chunks + 7) / 8);
-    return int(std::max<long long>(ctas, 1));
 }
 
 // The event pair bracketing the next timed launch (none when timing is off).
@@ -325,7 +455,29 @@ int tq_lloyd_max_codebook(int32_t bits, float* out) {
         }
         if (delta < 1e-15) break;
     }
-    for (int j = 0; j < n; ++j) out[j] = float(c[j]);
+    // each level rounded to the nearest fp16 value (ties to the even one):
+    // the candidates around the float-rounded value, compared exactly in double
+    for (int j = 0; j < n; ++j) {
+        const __half h0 = __float2half_rn(float(c[j]));
+        uint16_t b0;
+        std::memcpy(&b0, &h0, 2);
+        double best_v = 0.0, best_d = INFINITY;
+        uint16_t best_b = b0;
+        for (int k = -1; k <= 1; ++k) {
+            const uint16_t b = static_cast<uint16_t>(b0 + k);
+            __half h;
+            std::memcpy(&h, &b, 2);
+            const double v = double(__half2float(h));
+            if (!std::isfinite(v) || (v < 0) != (c[j] < 0)) continue;
+            const double d = std::fabs(v - c[j]);
+            if (d < best_d || (d == best_d && (b & 1u) == 0 && (best_b & 1u) != 0)) {
+                best_d = d;
+                best_v = v;
+                best_b = b;
+            }
+        }
+        out[j] = float(best_v);
+    }
     return TQ_OK;
 }
 
@@ -336,9 +488,9 @@ int tq_plan_splits(int32_t mode, int32_t batch, int32_t num_kv_heads, int32_t ro
     if (batch <= 0 || num_kv_heads <= 0 || rows_per_kv_head <= 0 || max_len_hint <= 0 ||
         split_tokens == nullptr || num_splits == nullptr)
         return TQ_ERR_INVALID_ARG;
-    const int gr = tq::group_rows_for(rows_per_kv_head);
+    const int gr = tq::group_rows_for(rows_per_kv_head, kb);
     const long long units = 1ll * batch * num_kv_heads * ((rows_per_kv_head + gr - 1) / gr);
-    const int ctas = plan_ctas(kb, vb, tq::mode_table(mode), gr, units, max_len_hint);
+    const int ctas = tq::host::plan_ctas(kb, vb, tq::mode_table(mode), false, gr, units, max_len_hint);
     const long long chunks = units * ((max_len_hint + 31) / 32);
     *num_splits = ctas;
     *split_tokens = int(std::min<long long>((chunks + ctas - 1) / ctas * 32, 1ll << 30));
@@ -384,6 +536,7 @@ int tq_encode_append(tq_ctx** pctx, const tq_cache* c, const void* k_new, const 
         std::memcpy(p.k_cb, c->codebook_k, sizeof(p.k_cb));
         std::memcpy(p.v_cb, c->codebook_v, sizeof(p.v_cb));
     }
+    ctx->last_stream = static_cast<cudaStream_t>(stream);
     return cuda_err(static_cast<cudaError_t>(
         tq::launch_encode(kb, vb, p, static_cast<cudaStream_t>(stream))));
 }
@@ -397,85 +550,22 @@ namespace {
 int decode_impl(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_heads,
                 int32_t tq_rows, int32_t max_len_hint, float scale, float tau, void* out,
                 void* stream) {
-    int kb, vb;
-    int r = check_cache(c, &kb, &vb);
+    tq::host::DecodePlan pl;
+    int r = tq::host::plan_decode(c, q, out, num_q_heads, tq_rows, max_len_hint, scale, &pl);
     if (r != TQ_OK) return r;
-    if (q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
-    if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
-    if (tq_rows <= 0 || max_len_hint <= 0 || max_len_hint > c->capacity) return TQ_ERR_INVALID_ARG;
-    if (tq_rows > max_len_hint) return TQ_ERR_INVALID_ARG;
-    if (!(scale >= 0.f) || !std::isfinite(scale)) return TQ_ERR_INVALID_ARG;
-    if (!std::isfinite(c->v_rescale)) return TQ_ERR_INVALID_ARG;
-    const int group = num_q_heads / c->num_kv_heads;
-    const int rows = group * tq_rows;
-    if (rows > 256) return TQ_ERR_UNSUPPORTED;
     tq_ctx* ctx;
     if ((r = get_ctx(pctx, &ctx)) != TQ_OK) return r;
-    if ((r = prepare_tables(ctx, c, kb, vb)) != TQ_OK) return r;
-    if (kb == 16 && (r = prepare_kmap(ctx, c)) != TQ_OK) return r;
-
-    const int group_rows = tq::group_rows_for(rows);
-    const int row_groups = (rows + group_rows - 1) / group_rows;
-    const long long units = 1ll * c->batch * c->num_kv_heads * row_groups;
-    const int ctas = plan_ctas(kb, vb, tq::mode_table(c->mode), group_rows, units, max_len_hint);
-    const size_t slots = size_t(ctas + units) * 16;
+    if ((r = prepare_tables(ctx, c, pl.kb, pl.vb)) != TQ_OK) return r;
+    if (pl.kb == 16 && (r = prepare_kmap(ctx, c)) != TQ_OK) return r;
+    const size_t slots = tq::host::decode_slots(pl);
     if ((r = ensure_work(ctx, slots * (kD + 2) * sizeof(float))) != TQ_OK) return r;
-
-    const float sc = (scale == 0.f) ? 1.0f / std::sqrt(float(kD)) : scale;
-    tq::DecodeParams p{};
-    p.k_codes = static_cast<const uint8_t*>(c->k_data);
-    p.k_norm = static_cast<const __half*>(c->k_norm);
-    p.v_codes = static_cast<const uint8_t*>(c->v_data);
-    p.v_norm = static_cast<const __half*>(c->v_norm);
-    p.lengths = c->lengths;
-    p.q = static_cast<const __half*>(q);
-    p.part_o = ctx->d_work;
-    p.part_ml = ctx->d_work + slots * kD;
-    p.status = ctx->d_words;
-    p.batch = c->batch;
-    p.hkv = c->num_kv_heads;
-    p.hq = num_q_heads;
-    p.group = group;
-    p.tq = tq_rows;
-    p.rows = rows;
-    p.row_groups = row_groups;
-    p.group_rows = group_rows;
-    p.cap = c->capacity;
-    p.max_len = max_len_hint;
-    p.num_ctas = ctas;
-    p.scale_log2e = sc * 1.4426950408889634f;
-    p.sparse_tau = tau;
-    p.table = tq::mode_table(c->mode) ? 1 : 0;
-    if (kb != 16) std::memcpy(p.ktab, ctx->ktab.tab, sizeof(p.ktab));
-    std::memcpy(p.vtab, ctx->vtab.tab, sizeof(p.vtab));
-    std::memcpy(p.signs, ctx->signs, sizeof(p.signs));
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if ((r = timing_events(ctx, &e0, &e1)) != TQ_OK) return r;
-    CUtensorMap dummy;
-    std::memset(&dummy, 0, sizeof(dummy));
-    r = tq::launch_decode(kb, vb, p, kb == 16 ? &ctx->kmap : &dummy, s, e0, e1);
-    if (r != 0) return TQ_ERR_CUDA;
-
-    tq::CombineParams cp{};
-    cp.part_o = p.part_o;
-    cp.part_ml = p.part_ml;
-    cp.lengths = c->lengths;
-    cp.out = static_cast<__half*>(out);
-    cp.status = ctx->d_words;
-    cp.batch = c->batch;
-    cp.hkv = c->num_kv_heads;
-    cp.hq = num_q_heads;
-    cp.group = group;
-    cp.tq = tq_rows;
-    cp.row_groups = row_groups;
-    cp.group_rows = group_rows;
-    cp.max_len = max_len_hint;
-    cp.num_ctas = ctas;
-    cp.v_rescale = c->v_rescale;
-    std::memcpy(cp.signs, ctx->signs, sizeof(cp.signs));
-    return cuda_err(static_cast<cudaError_t>(tq::launch_combine(cp, s)));
+    ctx->last_stream = static_cast<cudaStream_t>(stream);
+    return tq::host::launch_decode_plan(pl, c, ctx->ktab, ctx->vtab, ctx->signs, &ctx->kmap, q,
+                                        num_q_heads, tq_rows, max_len_hint, scale, tau, out,
+                                        ctx->d_work, ctx->d_words, static_cast<cudaStream_t>(stream),
+                                        e0, e1);
 }
 
 }  // namespace
@@ -501,6 +591,8 @@ int tq_prefill_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_
     int r = check_cache(c, &kb, &vb);
     if (r != TQ_OK) return r;
     if (tq::mode_table(c->mode)) return TQ_ERR_UNSUPPORTED;
+    // the prefill K tile holds fp16 centroids: exact only for fp16 levels
+    if (kb != 16 && !tq::host::codebook_is_fp16(c->codebook_k, c->codebook_k_size)) return TQ_ERR_UNSUPPORTED;
     if (q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
     if (num_q_heads <= 0 || num_q_heads % c->num_kv_heads != 0) return TQ_ERR_INVALID_ARG;
     if (tq_rows <= 0 || max_len_hint <= 0 || max_len_hint > c->capacity) return TQ_ERR_INVALID_ARG;
@@ -545,6 +637,7 @@ int tq_prefill_attention(tq_ctx** pctx, const tq_cache* c, const void* q, int32_
     CUtensorMap dummy;
     std::memset(&dummy, 0, sizeof(dummy));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ctx->last_stream = s;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if ((r = timing_events(ctx, &e0, &e1)) != TQ_OK) return r;
     if (e0) cudaEventRecord(e0, s);
@@ -558,6 +651,7 @@ int tq_selftest_bounded_wait(tq_ctx** pctx, int32_t limit_us, void* stream) {
     tq_ctx* ctx;
     int r = get_ctx(pctx, &ctx);
     if (r != TQ_OK) return r;
+    ctx->last_stream = static_cast<cudaStream_t>(stream);
     return cuda_err(static_cast<cudaError_t>(tq::launch_selftest_stall(
         ctx->d_words, uint64_t(limit_us) * 1000ull, static_cast<cudaStream_t>(stream))));
 }
@@ -581,10 +675,13 @@ int tq_get_status(tq_ctx* ctx, uint32_t* status) {
     if (status == nullptr) return TQ_ERR_INVALID_ARG;
     *status = 0;
     if (ctx == nullptr) return TQ_OK;
-    if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
+    // read and clear the word on the stream of the context's latest call, and
+    // wait for that stream only (other streams and devices keep running)
+    const cudaStream_t s = ctx->last_stream;
     uint32_t v = 0;
-    if (cudaMemcpy(&v, ctx->d_words, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ERR_CUDA;
-    if (cudaMemset(ctx->d_words, 0, 4) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaMemcpyAsync(&v, ctx->d_words, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaMemsetAsync(ctx->d_words, 0, 4, s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TQ_ERR_CUDA;
     *status = v;
     return TQ_OK;
 }

@@ -43,6 +43,19 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A(16x32, row) * B(32x8, col), e4m3 inputs (four per register), fp32
+// accumulate.  A: a0 = row g, k 4t..4t+3; a1 = row g+8, same k; a2, a3 the same
+// rows at k 16+4t..16+4t+3.  B: b0 = column g, k 4t..4t+3; b1 = k 16+4t...
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1,
+                                         uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Transpose an 8x8 fp16 matrix held one row pair per lane (lane = 4*row + colpair).
 __device__ __forceinline__ uint32_t movtrans(uint32_t a) {
     uint32_t d;
@@ -57,6 +70,12 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                  : "r"(addr));
 }
 
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(addr));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -64,6 +83,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two fp32 values as e4m3 (round to nearest even, saturating at +-448) in the
+// low 16 bits: lo in byte 0, hi in byte 1.
+__device__ __forceinline__ uint32_t fp8x2_e4m3(float lo, float hi) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -242,6 +269,33 @@ __device__ __forceinline__ void dequant4_word(uint32_t w, const Tables& t, uint3
         const uint32_t H = prmt(t.hi0, t.hi1, r2) | (w4 & 0x80808080u);
         h2 = prmt(L, H, 0x5140);
         h3 = prmt(L, H, 0x7362);
+    }
+}
+
+// dequant4_word plus the centroids' fp8 residuals (e4m3 bytes of
+// (c - fp16(c)) * 2^a looked up from the 8-byte table r8lo:r8hi by rank, the
+// element's sign XORed into bit 7): q0 = dims 0..3, q1 = dims 4..7.
+__device__ __forceinline__ void dequant4_word_res(uint32_t w, const Tables& t, uint32_t r8lo,
+                                                  uint32_t r8hi, uint32_t& h0, uint32_t& h1,
+                                                  uint32_t& h2, uint32_t& h3, uint32_t& q0,
+                                                  uint32_t& q1) {
+    const uint32_t rk = w & 0x77777777u;
+    const uint32_t s0 = w & 0x80808080u;
+    {
+        const uint32_t L = prmt(t.lo0, t.lo1, rk);
+        const uint32_t H = prmt(t.hi0, t.hi1, rk) | s0;
+        h0 = prmt(L, H, 0x5140);
+        h1 = prmt(L, H, 0x7362);
+        q0 = prmt(r8lo, r8hi, rk) ^ s0;
+    }
+    {
+        const uint32_t r2 = __umulhi(rk, 1u << 16);  // rk >> 16, on the FMA pipe
+        const uint32_t s1 = (w << 4) & 0x80808080u;
+        const uint32_t L = prmt(t.lo0, t.lo1, r2);
+        const uint32_t H = prmt(t.hi0, t.hi1, r2) | s1;
+        h2 = prmt(L, H, 0x5140);
+        h3 = prmt(L, H, 0x7362);
+        q1 = prmt(r8lo, r8hi, r2) ^ s1;
     }
 }
 

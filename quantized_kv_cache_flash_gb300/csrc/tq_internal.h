@@ -12,10 +12,10 @@
 
 namespace tq {
 
-// Decode (split-K) kernel parameters.  One CTA = one (split, batch*kv-head,
-// row group); a row group is up to group_rows (8 or 16) query rows (GQA heads
-// x Tq) of one KV head: the N dimension of the warp-level MMAs, whose M
-// dimension is 16 tokens.
+// Decode (split-K) kernel parameters.  A row group is up to group_rows (4, 8
+// or 16) query rows (GQA heads x Tq) of one KV head: the N dimension of the
+// warp-level MMAs, whose M dimension is 16 tokens.  The CTAs split the
+// context's 32-token chunks of all (batch, kv head, row group) units evenly.
 struct DecodeParams {
     const uint8_t* k_codes;   // packed K codes (unused for fp16 K)
     const __half* k_norm;     // fp16 K norms (unused for fp16 K)
@@ -34,6 +34,11 @@ struct DecodeParams {
     uint32_t ktab[4];         // prmt byte tables of the K codebook (lo0, lo1, hi0, hi1)
     uint32_t vtab[4];
     uint32_t signs[4];        // bit d set <=> s_d = -1
+    // K centroids' rounding residuals c - fp16(c), scaled by 2^res_shift, as
+    // e4m3 bytes (3-bit: indexed by the signed code; 4-bit: by magnitude rank)
+    uint32_t ktab8[2];
+    int32_t res_shift;
+    int32_t k_res;            // 1: the K codebook has entries that are not fp16 values
 };
 
 struct CombineParams {
@@ -86,20 +91,25 @@ struct PrefillParams {
 };
 
 // Launchers (return a cudaError_t value).
-// group_rows (p.group_rows) selects the 8- or 16-row variant.
+// group_rows (p.group_rows) selects the 4-, 8- or 16-row variant.
 int launch_decode(int kbits, int vbits, const DecodeParams& p, const CUtensorMap* kmap,
                   cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end);
 int launch_combine(const CombineParams& p, cudaStream_t stream);
 int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stream);
 
-// Resident CTAs per SM of a decode variant (for the host split planner).
-int decode_ctas_per_sm(int kbits, int vbits, int group_rows, bool table);
+// Resident CTAs per SM of a decode variant (for the host split planner);
+// res: the variant with the centroid residual product.
+int decode_ctas_per_sm(int kbits, int vbits, int group_rows, bool table, bool res);
 int launch_prefill(int kbits, int vbits, const PrefillParams& p, const CUtensorMap* kmap,
                    cudaStream_t stream);
 int launch_selftest_stall(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 
-// Query rows per row group for `rows` query rows of one KV head.
-inline int group_rows_for(int rows) { return rows <= 8 ? 8 : 16; }
+// Query rows per row group for `rows` query rows of one KV head: 4 when K is
+// quantized and at most 4 rows share a KV head (the low halves of the rotated
+// query then ride in the score MMA's spare columns), else 8, or 16 per group.
+inline int group_rows_for(int rows, int kbits) {
+    return (rows <= 4 && kbits != 16) ? 4 : rows <= 8 ? 8 : 16;
+}
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while its predecessor in the stream finishes (every kernel of this library
@@ -135,5 +145,60 @@ inline int mode_bits(int mode, int* kb, int* vb) {
         default: return TQ_ERR_UNSUPPORTED;
     }
 }
+
+// ---------------------------------------------------------------------------
+// Host helpers shared by the entry points (defined in tq_api.cu)
+// ---------------------------------------------------------------------------
+namespace host {
+
+// Kernel-side forms of a checked codebook.
+struct CodebookTables {
+    bool valid = false;
+    int bits = 0;
+    float cb[16] = {};
+    uint32_t tab[4] = {};  // prmt byte tables of the fp16 centroids (lo0, lo1, hi0, hi1)
+    float gt[7] = {}, ge[7] = {};  // encode decision thresholds (see EncodeParams)
+    // e4m3 bytes of (c - fp16(c)) * 2^res_shift (3-bit: by signed code; 4-bit:
+    // by magnitude rank), for the score's fp8 residual product
+    uint32_t tab8[2] = {};
+    int res_shift = 0;
+};
+
+int cuda_err_code(cudaError_t e);
+bool aligned16(const void* p);
+// Mode, shape, pointers and codebooks of a cache; *kb, *vb = its bits (16 = fp16 K).
+int check_cache(const tq_cache* c, int* kb, int* vb);
+// (Re)builds *t unless it already holds this codebook.
+int build_tables(const float* cb, int n, int bits, CodebookTables* t);
+// s_d = -1 <=> bit d of out (splitmix64 of the rotation seed).
+void make_signs(uint64_t seed, uint32_t out[4]);
+// Tensor map of the fp16 K rows of a cache (driver entry point looked up once).
+int encode_kmap(CUtensorMap* map, const tq_cache* c);
+// Whether every entry of a codebook is an fp16 value (no rounding residual).
+bool codebook_is_fp16(const float* cb, int n);
+
+// One decode call's checked arguments and the row grouping and grid derived
+// from them.
+struct DecodePlan {
+    int kb, vb;
+    bool res;          // quantized K whose codebook is not all fp16 values
+    int group, rows, group_rows, row_groups;
+    long long units;   // (batch, kv head, row group) units
+    int ctas;          // decode grid
+};
+int plan_decode(const tq_cache* c, const void* q, const void* out, int num_q_heads, int tq_rows,
+                int max_len_hint, float scale, DecodePlan* pl);
+// Split-K scratch of a plan: (ctas + units) slots of 16 rows x (128 + 2) floats.
+inline size_t decode_slots(const DecodePlan& pl) { return size_t(pl.ctas + pl.units) * 16; }
+// Launch the decode and combine kernels of a plan on `stream`, the partials
+// in `part` (decode_slots(pl) * 130 floats), device status bits ORed into
+// `status`; ev0/ev1 (optional) bracket the decode kernel.
+int launch_decode_plan(const DecodePlan& pl, const tq_cache* c, const CodebookTables& kt,
+                       const CodebookTables& vt, const uint32_t signs[4], const CUtensorMap* kmap,
+                       const void* q, int num_q_heads, int tq_rows, int max_len_hint, float scale,
+                       float tau, void* out, float* part, uint32_t* status, cudaStream_t stream,
+                       cudaEvent_t ev0, cudaEvent_t ev1);
+
+}  // namespace host
 
 }  // namespace tq

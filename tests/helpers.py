@@ -79,11 +79,14 @@ def upload(x, device):
 
 
 def gpu_cache_from_records(mode, B, Hkv, cap, lengths, kdata, knorm, vdata, vnorm, device,
-                           v_rescale=1.0, rot_seed=42):
-    """A library Cache whose buffers hold the given records (numpy, [B,Hkv,cap,...])."""
+                           v_rescale=1.0, rot_seed=42, codebook_k=None, codebook_v=None):
+    """A library Cache whose buffers hold the given records (numpy, [B,Hkv,cap,...]);
+    the standard codebooks unless others are given."""
     import torch
     import quantized_kv_cache_flash_gb300 as tqf
-    c = tqf.Cache(tqf.MODES[mode], B, Hkv, cap, device, rot_seed=rot_seed, v_rescale=v_rescale)
+    c = tqf.Cache(tqf.MODES[mode], B, Hkv, cap, device, rot_seed=rot_seed, v_rescale=v_rescale,
+                  codebook_k=None if codebook_k is None else [float(x) for x in codebook_k],
+                  codebook_v=None if codebook_v is None else [float(x) for x in codebook_v])
     c.k_data.copy_(upload(kdata, device))
     if c.k_norm is not None:
         c.k_norm.copy_(upload(knorm, device))
@@ -136,11 +139,20 @@ def oracle_unit_from_records(mode, kdata, knorm, vdata, vnorm, b, h, L):
     return unit
 
 
-def oracle_decode(mode, q, units, lengths, Hkv, tq, scale, v_rescale, rot_seed=42):
-    """Oracle output [B, Hq, Tq, 128] (fp64) from per-unit dicts units[(b, h)]."""
+def exact_lloyd_max(bits):
+    """The Lloyd-Max levels rounded to fp32 instead of fp16: a codebook whose
+    entries are not fp16 values (the decode path with the residual product)."""
+    return o.lloyd_max(1 << bits)[0].astype(np.float32)
+
+
+def oracle_decode(mode, q, units, lengths, Hkv, tq, scale, v_rescale, rot_seed=42, cbk=None, cbv=None):
+    """Oracle output [B, Hq, Tq, 128] (fp64) from per-unit dicts units[(b, h)]
+    (the standard codebooks unless others are given)."""
     kb, vb = MODE_BITS[mode]
-    cbk = o.codebook(kb) if kb != 16 else None
-    cbv = o.codebook(vb)
+    if cbk is None:
+        cbk = o.codebook(kb) if kb != 16 else None
+    if cbv is None:
+        cbv = o.codebook(vb)
     s = o.sign_vector(rot_seed)
     B, Hq = q.shape[0], q.shape[1]
     G = Hq // Hkv

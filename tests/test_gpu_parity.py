@@ -87,6 +87,75 @@ def test_decode_same_cache(case):
     H.assert_attention_close(got, want, str(case))
 
 
+# Peaked softmax: q scaled by 8 .. 32 puts the leading scores at 20 .. 100
+# (natural log units), where a relative score error of 2^-11 (one fp16
+# rounding of the rotated query or of a centroid) would already move the
+# dominant weights by a per cent.  Every row-group size (4, 8 and 16 rows per
+# KV head) and every mode, against the oracle.
+SHARP_CASES = [
+    # mode, B, Hq, Hkv, lengths, Tq, cap, q scale
+    ("turbo4", 2, 32, 8, [3000, 1777], 1, 3008, 8.0),            # 4 rows: q_lo in the pair columns
+    ("turbo4", 2, 32, 8, [3000, 1777], 1, 3008, 32.0),
+    ("turbo4", 1, 8, 4, [2000], 1, 2000, 16.0),                  # 2 rows
+    ("turbo3", 1, 32, 8, [2600], 4, 2608, 8.0),                  # 16 rows, causal block
+    ("turbo3", 1, 32, 8, [2600], 4, 2608, 32.0),
+    ("turbo3", 1, 28, 4, [4100], 1, 4112, 32.0),                 # 7 rows (8-row group)
+    ("turbo4k_3v", 2, 12, 4, [700, 1500], 2, 1504, 32.0),        # 6 rows
+    ("turbo4k_3v", 1, 16, 4, [1100], 1, 1104, 24.0),             # 4 rows, 3-bit V
+    ("turbo4_asym", 1, 28, 4, [4100], 1, 4112, 32.0),
+    ("turbo3_asym", 1, 8, 2, [900], 1, 912, 32.0),
+    ("turbo3_table", 1, 32, 8, [2049], 4, 2064, 32.0),
+    ("turbo3_table", 2, 8, 2, [1300, 37], 1, 1312, 16.0),
+]
+
+
+# Codebooks whose entries are not fp16 values (the Lloyd-Max levels rounded
+# to fp32) take the decode path that adds each score's centroid rounding
+# residual through an fp8 product: the same peaked cases with those.
+EXACT_CB_CASES = [c for c in SHARP_CASES if c[0] in ("turbo4", "turbo3", "turbo4k_3v")]
+
+
+def _peaked(case, exact_cb):
+    mode, B, Hq, Hkv, lengths, Tq, cap, qs = case
+    key = 8800 + sum(lengths) + Hq + int(qs)
+    kd, kn, vd, vn = H.random_cache(mode, B, Hkv, cap, key)
+    q = (wl.random_fp16(key + 3, (B, Hq, Tq, 128)).astype(np.float32) * qs).astype(np.float16)
+    kb, vb = H.MODE_BITS[mode]
+    cbk = H.exact_lloyd_max(kb) if exact_cb and kb != 16 else None
+    cbv = H.exact_lloyd_max(vb) if exact_cb else None
+    if exact_cb:
+        assert not np.array_equal(cbk, cbk.astype(np.float16).astype(np.float32))
+    cache = H.gpu_cache_from_records(mode, B, Hkv, cap, lengths, kd, kn, vd, vn, DEV, v_rescale=0.75,
+                                     codebook_k=cbk, codebook_v=cbv)
+    got, status, _ = _run_decode(cache, q, Tq, max(lengths))
+    assert status == 0
+    units = {(b, h): H.oracle_unit_from_records(mode, kd, kn, vd, vn, b, h, lengths[b])
+             for b in range(B) for h in range(Hkv)}
+    want = H.oracle_decode(mode, q, units, lengths, Hkv, Tq, 1 / math.sqrt(128), 0.75, cbk=cbk, cbv=cbv)
+    H.assert_attention_close(got, want, f"{case} exact codebook {exact_cb}")
+
+
+@pytest.mark.parametrize("case", SHARP_CASES, ids=lambda c: f"{c[0]}-Hq{c[2]}-Tq{c[5]}-q{c[7]:g}")
+def test_decode_peaked_softmax(case):
+    _peaked(case, False)
+
+
+@pytest.mark.parametrize("case", EXACT_CB_CASES, ids=lambda c: f"{c[0]}-Hq{c[2]}-Tq{c[5]}-q{c[7]:g}")
+def test_decode_peaked_softmax_fp32_codebook(case):
+    _peaked(case, True)
+
+
+@pytest.mark.parametrize("mode,B,Hq,Hkv,L,Tq,qs", [
+    ("turbo4", 2, 32, 8, 1500, 1, 8.0), ("turbo4", 2, 32, 8, 1500, 1, 32.0),
+    ("turbo3", 1, 32, 8, 1200, 4, 32.0), ("turbo3", 1, 28, 4, 2000, 1, 16.0),
+    ("turbo4_asym", 1, 28, 4, 2000, 1, 32.0),
+])
+def test_end_to_end_peaked_softmax(mode, B, Hq, Hkv, L, Tq, qs):
+    """Gaussian K with outlier channels and V, encoded by each side, queries
+    scaled up: the encoded-cache path of the same regime."""
+    _e2e(mode, B, Hq, Hkv, L, Tq, (L + 15) // 16 * 16, 600 + L + int(qs), q_scale=qs)
+
+
 @pytest.mark.parametrize("mode,Hq,Tq,scale_v", [("turbo4", 8, 1, 1000.0), ("turbo3", 32, 1, 3000.0),
                                                ("turbo4k_3v", 8, 2, 1000.0), ("turbo4_asym", 4, 1, 2000.0)])
 def test_decode_large_v_norms(mode, Hq, Tq, scale_v):
@@ -257,14 +326,14 @@ def test_encode_capacity_overflow_is_flagged_and_skipped():
 # ---------------------------------------------------------------------------
 # end to end: each side encodes on its own, then decodes
 # ---------------------------------------------------------------------------
-def _e2e(mode, B, Hq, Hkv, L, Tq, cap, outliers_key):
+def _e2e(mode, B, Hq, Hkv, L, Tq, cap, outliers_key, q_scale=1.0):
     w = wl.Workload(0, "test", mode, B, Hq, Hkv, L, tq=Tq)
     k = np.stack([np.stack([wl.random_fp16(outliers_key + 10 * b + h, (L, 128))
                             for h in range(Hkv)]) for b in range(B)])
     k[..., [3, 50, 77, 120]] = (k[..., [3, 50, 77, 120]].astype(np.float32) * 8).astype(np.float16)
     v = np.stack([np.stack([wl.random_fp16(outliers_key + 1000 + 10 * b + h, (L, 128))
                             for h in range(Hkv)]) for b in range(B)])
-    q = wl.random_fp16(outliers_key + 77, (B, Hq, Tq, 128))
+    q = wl.random_fp16(outliers_key + 77, (B, Hq, Tq, 128), scale=q_scale)
     ctx = tqf.Context()
     cache = tqf.Cache(tqf.MODES[mode], B, Hkv, cap, DEV)
     tqf.tq_encode_append(ctx, cache, H.upload(k, DEV), H.upload(v, DEV))

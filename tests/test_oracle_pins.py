@@ -98,7 +98,7 @@ def test_lloyd_max_fixed_point_and_symmetry(levels):
     assert np.all(np.diff(c) > 0)
     assert np.max(np.abs(c + c[::-1])) < 1e-15
     c32 = o.codebook(int(math.log2(levels)))
-    assert np.array_equal(c32, -c32[::-1])        # exactly symmetric in fp32
+    assert np.array_equal(c32, -c32[::-1])        # exactly symmetric after rounding
 
 
 @pytest.mark.parametrize("levels", [4, 8, 16])
@@ -132,8 +132,28 @@ def test_lloyd_max_matches_max_1960_table(golden_dir):
 def test_codebook_is_scaled_unit_gaussian_quantiser():
     for bits in (3, 4):
         c1, _, _ = o.lloyd_max(1 << bits, sigma=1.0)
-        c = o.codebook(bits).astype(np.float64)
-        assert np.max(np.abs(c * math.sqrt(128) - c1)) < 1e-6
+        c64, _, _ = o.lloyd_max(1 << bits)
+        assert np.max(np.abs(c64 * math.sqrt(128) - c1)) < 1e-12
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_codebook_levels_are_the_nearest_fp16_values(bits):
+    """Each standard level is the fp16 value nearest the fp64 Lloyd-Max level,
+    found by exact rational comparison against every finite fp16 value of the
+    same sign (ties would go to the even one: there are none here)."""
+    c64, _, _ = o.lloyd_max(1 << bits)
+    cb = o.codebook(bits)
+    assert cb.dtype == np.float32
+    allf = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    for x, got in zip(c64, cb):
+        a = Fraction(abs(float(x)))
+        near = [i for i in range(len(allf)) if a / 2 <= allf[i] <= 2 * a]
+        d = {i: abs(Fraction(allf[i]) - a) for i in near}
+        best = min(near, key=lambda i: (d[i], i % 2))   # bit pattern i: even = even mantissa
+        assert sorted(d.values())[0] < sorted(d.values())[1]   # no tie
+        assert float(got) == math.copysign(allf[best], x)
+    # the rounding moves each level by at most 2^-11 of itself (half an fp16 ulp)
+    assert np.all(np.abs(cb - c64) <= 2.0 ** -11 * np.abs(c64))
 
 
 # --------------------------------------------------------------------------
