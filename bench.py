@@ -13,9 +13,13 @@ between steps.
 Printed: one JSON line (rank 0) with value = effective GB/s over the
 algorithmic bytes of the step (packed K/V + norms over every visible token,
 q, o, and the append's fp16 inputs and packed outputs), tokens/s, the decode
-kernel's roofline, the oracle's CPU baseline, an end-to-end figure through the
-C ABI with host buffers, clocks sampled during the timed region, and the
-number of kernel launches.
+kernel's roofline (its own duration from 12 launches timed with the library's
+event pair right after the timed steps), the oracle's CPU baseline, an
+end-to-end figure through the C ABI with host buffers, clocks sampled during
+the timed region, and the number of kernel launches.  The default run (one
+GPU, workload 4) also times workloads 2, 3 and 5 (with the 4096-token
+prefill-chunk encode of workload 5) the same way and reports each under
+`other_workloads`.
 
 --impl reference times the fp64 CPU oracle (the correctness reference of this
 library; nothing else implements the pages' method here) on a bounded sample
@@ -47,7 +51,7 @@ PROMPT_METRIC = "chunked-prefill attention over the packed cache: TFLOP/s (causa
 REC = {"turbo4_asym": (256, 66), "turbo3": (50, 50), "turbo4": (66, 66),
        "turbo3_asym": (256, 50), "turbo4k_3v": (66, 50), "turbo3_table": (64, 64)}
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SAMPLE = 10   # decode launches timed on their own: one timed step in this many
+KERNEL_STEPS = 12   # decode launches timed on their own, after the timed steps
 PIPELINE_MIN_MS = 0.1   # e2e: device step time above which the host copies overlap compute
 
 
@@ -464,7 +468,8 @@ def gpu_arm(args, rank, world, device_index):
     lens0 = wl.lengths(wl.by_number(args.workload)).astype(np.int64)[:w.batch]
     t_new = max(w.append, 0)
     steps, warm = args.steps, args.warmup
-    grow = t_new * (steps + warm + 2)
+    kt = KERNEL_STEPS
+    grow = t_new * (steps + warm + kt + 2)
     cap = int(math.ceil((int(lens0.max()) + grow + 16) / 16) * 16)
     B, Hq, Hkv, Tq = w.batch, w.num_q_heads, w.num_kv_heads, w.tq
     mode = tqf.MODES[w.mode]
@@ -494,9 +499,9 @@ def gpu_arm(args, rank, world, device_index):
     assert tqf.tq_get_status(ctx) == 0
 
     nstep = steps + warm
-    qs = [randn((B, Hq, Tq, 128)) for _ in range(nstep)]
-    kn = [randn((B, Hkv, t_new, 128), True) for _ in range(nstep)] if t_new else []
-    vn = [randn((B, Hkv, t_new, 128)) for _ in range(nstep)] if t_new else []
+    qs = [randn((B, Hq, Tq, 128)) for _ in range(nstep + kt)]
+    kn = [randn((B, Hkv, t_new, 128), True) for _ in range(nstep + kt)] if t_new else []
+    vn = [randn((B, Hkv, t_new, 128)) for _ in range(nstep + kt)] if t_new else []
     out = torch.empty((B, Hq, Tq, 128), dtype=torch.float16, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -524,14 +529,11 @@ def gpu_arm(args, rank, world, device_index):
     tqf.tq_get_kernel_time(ctx)   # reset
     torch.cuda.synchronize()
 
-    # The decode launch of every KERNEL_SAMPLE-th timed step is bracketed by the
-    # library's event pair (the kernel's own duration); the other steps run
-    # without it, since an event between two launches stops programmatic
-    # dependent launch from overlapping them and would lengthen the step.
-    sampled = [i for i in range(warm, nstep) if (i - warm) % KERNEL_SAMPLE == 0]
-
+    # The timed steps carry no event between their launches (an event there
+    # stops programmatic dependent launch from overlapping them); the decode
+    # kernel's own duration comes from KERNEL_STEPS further steps right after
+    # them, each decode launch bracketed by the library's event pair.
     def timed_step(i):
-        tqf.tq_set_kernel_timing(ctx, (i - warm) % KERNEL_SAMPLE == 0)
         step(i, max_len_hint)
 
     torch.cuda.nvtx.range_push("timed")   # ncu --nvtx --nvtx-include timed/ selects these launches
@@ -557,6 +559,14 @@ def gpu_arm(args, rank, world, device_index):
         torch.cuda.synchronize()
         ms = sum(a.elapsed_time(b) for a, b in evs)
     torch.cuda.nvtx.range_pop()
+    # the decode kernel alone (same stream, inputs flushed from L2 when they fit)
+    sampled = list(range(nstep, nstep + kt))
+    tqf.tq_set_kernel_timing(ctx, True)
+    for i in sampled:
+        if flush:
+            scratch.fill_(float(i))
+        step(i, max_len_hint)
+    torch.cuda.synchronize()
     clk = clocks.stop()
     kern_ms, kern_n = tqf.tq_get_kernel_time(ctx)
     tqf.tq_set_kernel_timing(ctx, False)
@@ -688,6 +698,38 @@ def gpu_arm(args, rank, world, device_index):
         if tqf.tq_get_status(ctx) != 0:
             raise RuntimeError("device status after the prefill encode")
 
+    # sparse V (the V skip of tokens whose softmax weight is below tau) against
+    # the plain decode on the same cache, decode kernel alone, for the
+    # workload's own queries and for sharper ones (q x 8: most weights tiny)
+    sparse = None
+    if getattr(args, "sparse_leg", False):
+        sparse = []
+        L_now = int(cache.lengths.max().item())
+        for qscale in (1.0, 8.0):
+            q = (qs[0].float() * qscale).to(torch.float16)
+            res = {"q_scale": qscale, "tau": SPARSE_TAU}
+            for name, tau in (("plain", 0.0), ("sparse_v", SPARSE_TAU)):
+                tqf.tq_get_kernel_time(ctx)
+                tqf.tq_set_kernel_timing(ctx, True)
+                for rep in range(KERNEL_STEPS + 2):
+                    if rep == 2:  # two untimed warm-up launches
+                        torch.cuda.synchronize()
+                        tqf.tq_get_kernel_time(ctx)
+                    if tau > 0:
+                        tqf.tq_decode_attention_sparse_v(ctx, cache, q, out, L_now, tau, 0.0, stream)
+                    else:
+                        tqf.tq_decode_attention(ctx, cache, q, out, L_now, 0.0, stream)
+                torch.cuda.synchronize()
+                kms, kn_ = tqf.tq_get_kernel_time(ctx)
+                tqf.tq_set_kernel_timing(ctx, False)
+                res[name + "_kernel_us"] = kms / kn_ * 1e3
+            skipped, judged = tqf.tq_get_sparse_v_tiles(ctx)
+            res["tiles_skipped_fraction"] = skipped / max(judged, 1)
+            res["speedup"] = res["plain_kernel_us"] / res["sparse_v_kernel_us"]
+            sparse.append(res)
+        if tqf.tq_get_status(ctx) != 0:
+            raise RuntimeError("device status after the sparse-V leg")
+
     return {
         "w": w, "value": value, "prefill_encode": prefill, "ms": ms_max, "tokens_per_s": tokens / (ms_max * 1e-3),
         "step_bytes": sum(step_bytes) / steps, "clocks": clk,
@@ -705,7 +747,27 @@ def gpu_arm(args, rank, world, device_index):
                 "copies": "second stream, double-buffered" if pipelined else "compute stream"},
         "launches": (3 if t_new else 2) * steps,
         "hot_l2": hot,
+        "sparse_v": sparse,
     }
+
+
+EXTRA_WORKLOADS = (2, 3, 5)   # timed besides the headline (4) by the default run
+SPARSE_TAU = 1e-6             # the threshold the mlxcel ADR 0002 commit calls exact
+EXTRA_STEPS = 30
+
+
+def workload_summary(r, args):
+    """The JSON entry of one more workload: the headline's keys that describe it."""
+    d = {"value": r["value"], "unit": r.get("unit", "GB/s"), "steps": args.steps,
+         "ms_per_step": r["ms"] / args.steps, "tokens_per_s": r["tokens_per_s"],
+         "pct_of_peak": 100.0 * r["value"] / r["roofline"]["peak"], "roofline": r["roofline"],
+         "e2e": r["e2e"], "clocks": r["clocks"], "config": config_dict(r["w"]),
+         "gpu_launches": r["launches"]}
+    if r.get("hot_l2"):
+        d["hot_l2"] = r["hot_l2"]
+    if r.get("prefill_encode"):
+        d["prefill_encode"] = r["prefill_encode"]
+    return d
 
 
 def workload(args) -> wl.Workload:
@@ -779,6 +841,9 @@ def main():
                     help="override the workload's batch (small profiling cases only)")
     ap.add_argument("--mode", default=None, choices=sorted(REC),
                     help="run the workload's shapes in another cache mode (format and mode A/B)")
+    ap.add_argument("--no-extra", action="store_false", dest="extra",
+                    help="time only the chosen workload (the default run of workload 4 also "
+                         "times workloads 2, 3 and 5)")
     ap.add_argument("--_oracle-sample", type=int, default=None, dest="oracle_sample")
     ap.add_argument("--_budget", type=float, default=10.0, dest="budget")
     args = ap.parse_args()
@@ -831,7 +896,19 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
+    args.sparse_leg = (world == 1 and args.extra and args.workload == 4 and not args.batch
+                       and not args.mode)
     r = (prompt_arm if w.prompt else gpu_arm)(args, rank, world, local)
+    # the other decode configurations of the benchmark, each timed the same
+    # way (one GPU, the default run only)
+    extra = {}
+    if (world == 1 and args.extra and args.workload == 4 and not args.batch and not args.mode):
+        import copy
+        for n in EXTRA_WORKLOADS:
+            a2 = copy.copy(args)
+            a2.workload, a2.steps, a2.sparse_leg = n, min(args.steps, EXTRA_STEPS), False
+            x = gpu_arm(a2, rank, world, local)
+            extra[x["w"].name] = workload_summary(x, a2)
     cpu = (run_cpu_baseline(args.workload, args.cpu_budget, args.mode)
            if (rank == 0 and world == 1) else None)
     if rank == 0:
@@ -851,6 +928,10 @@ def main():
         }
         if r.get("hot_l2"):
             line["hot_l2"] = r["hot_l2"]
+        if extra:
+            line["other_workloads"] = extra
+        if r.get("sparse_v"):
+            line["sparse_v"] = r["sparse_v"]
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

@@ -268,6 +268,13 @@ int tq_plan_splits(int32_t mode, int32_t batch, int32_t num_kv_heads,
                    int32_t rows_per_kv_head, int32_t max_len_hint,
                    int32_t *split_tokens, int32_t *num_splits);
 
+/* The sparse-V decode's tile counts since the last read, then cleared:
+ * *skipped = 16-token tiles (of one row group) whose V work was skipped,
+ * *judged = tiles judged.  Ordered on the stream of the context's latest
+ * call; waits for that stream only.  (32-bit device counters: read them at
+ * least every 2^32 tiles.) */
+int tq_get_sparse_v_tiles(tq_ctx *ctx, uint64_t *skipped, uint64_t *judged);
+
 /* Benchmark hook: when enabled, tq_decode_attention (and its sparse-V form)
  * records CUDA events around its main (split-K) kernel and
  * tq_prefill_attention around its kernel; tq_get_kernel_time synchronizes on

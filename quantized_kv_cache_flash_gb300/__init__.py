@@ -67,6 +67,8 @@ _SIGS = {
     "tq_record_bytes": (_c.c_int, [_c.c_int32]),
     "tq_plan_splits": (_c.c_int, [_c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
                                   _c.POINTER(_c.c_int32), _c.POINTER(_c.c_int32)]),
+    "tq_get_sparse_v_tiles": (_c.c_int, [_c.c_void_p, _c.POINTER(_c.c_uint64),
+                                         _c.POINTER(_c.c_uint64)]),
     "tq_set_kernel_timing": (_c.c_int, [_c.c_void_p, _c.c_int32]),
     "tq_get_kernel_time": (_c.c_int, [_c.c_void_p, _c.POINTER(_c.c_float),
                                       _c.POINTER(_c.c_int32)]),
@@ -307,10 +309,18 @@ def tq_free(ctx: Context) -> None:
 
 
 def tq_get_status(ctx: Context) -> int:
-    """Synchronize, return and clear the device status bits."""
+    """Return and clear the device status bits (waits for the context's latest stream)."""
     s = ctypes.c_uint32()
     _check(lib().tq_get_status(ctx.ptr, ctypes.byref(s)), "tq_get_status")
     return s.value
+
+
+def tq_get_sparse_v_tiles(ctx: Context):
+    """(skipped, judged) 16-token tiles of the sparse-V decode since the last read."""
+    a, b = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(lib().tq_get_sparse_v_tiles(ctx.ptr, ctypes.byref(a), ctypes.byref(b)),
+           "tq_get_sparse_v_tiles")
+    return a.value, b.value
 
 
 def tq_set_kernel_timing(ctx: Context, enable: bool) -> None:

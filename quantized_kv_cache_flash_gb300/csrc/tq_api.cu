@@ -235,7 +235,8 @@ int launch_decode_plan(const DecodePlan& pl, const tq_cache* c, const CodebookTa
                        const CodebookTables& vt, const uint32_t signs[4], const CUtensorMap* kmap,
                        const void* q, int num_q_heads, int tq_rows, int max_len_hint, float scale,
                        float tau, void* out, float* part, uint32_t* status, cudaStream_t stream,
-                       cudaEvent_t ev0, cudaEvent_t ev1) {
+                       cudaEvent_t ev0, cudaEvent_t ev1, uint32_t* sparse_tiles) {
+    if (tau > 0.f && sparse_tiles == nullptr) return TQ_ERR_INVALID_ARG;
     const size_t slots = decode_slots(pl);
     const float sc = (scale == 0.f) ? 1.0f / std::sqrt(float(kD)) : scale;
     tq::DecodeParams p{};
@@ -261,6 +262,7 @@ int launch_decode_plan(const DecodePlan& pl, const tq_cache* c, const CodebookTa
     p.num_ctas = pl.ctas;
     p.scale_log2e = sc * 1.4426950408889634f;
     p.sparse_tau = tau;
+    p.sparse_tiles = sparse_tiles;
     p.table = tq::mode_table(c->mode) ? 1 : 0;
     if (pl.kb != 16) {
         std::memcpy(p.ktab, kt.tab, sizeof(p.ktab));
@@ -300,7 +302,7 @@ int launch_decode_plan(const DecodePlan& pl, const tq_cache* c, const CodebookTa
 
 struct tq_ctx {
     int device = -1;
-    uint32_t* d_words = nullptr;  // [0] status, [1] encode ticket counter
+    uint32_t* d_words = nullptr;  // [0] status, [1] encode ticket counter, [2..3] sparse-V tiles
     float* d_work = nullptr;
     size_t work_bytes = 0;
     CodebookTables ktab, vtab;
@@ -565,7 +567,7 @@ int decode_impl(tq_ctx** pctx, const tq_cache* c, const void* q, int32_t num_q_h
     return tq::host::launch_decode_plan(pl, c, ctx->ktab, ctx->vtab, ctx->signs, &ctx->kmap, q,
                                         num_q_heads, tq_rows, max_len_hint, scale, tau, out,
                                         ctx->d_work, ctx->d_words, static_cast<cudaStream_t>(stream),
-                                        e0, e1);
+                                        e0, e1, ctx->d_words + 2);
 }
 
 }  // namespace
@@ -683,6 +685,18 @@ int tq_get_status(tq_ctx* ctx, uint32_t* status) {
     if (cudaMemsetAsync(ctx->d_words, 0, 4, s) != cudaSuccess) return TQ_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return TQ_ERR_CUDA;
     *status = v;
+    return TQ_OK;
+}
+
+int tq_get_sparse_v_tiles(tq_ctx* ctx, uint64_t* skipped, uint64_t* judged) {
+    if (ctx == nullptr || skipped == nullptr || judged == nullptr) return TQ_ERR_INVALID_ARG;
+    const cudaStream_t s = ctx->last_stream;
+    uint32_t v[2] = {0, 0};
+    if (cudaMemcpyAsync(v, ctx->d_words + 2, 8, cudaMemcpyDeviceToHost, s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaMemsetAsync(ctx->d_words + 2, 0, 8, s) != cudaSuccess) return TQ_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TQ_ERR_CUDA;
+    *skipped = v[0];
+    *judged = v[1];
     return TQ_OK;
 }
 

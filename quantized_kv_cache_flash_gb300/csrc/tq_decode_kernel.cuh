@@ -507,6 +507,7 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, ROWS, TAB, RES>::kMinCtas)
 #pragma unroll
             for (int e = 0; e < NE; ++e) m[n][e] = -INFINITY, l[n][e] = bs[n][e] = 0.f;
         bool stalled = false;
+        uint32_t tiles_seen = 0, tiles_skipped = 0;  // sparse V: this warp's tile counts
 
         // TPC tiles (16 tokens each) of a 32-token chunk of this warp, from
         // tile0: both tiles in one call (their K dequant interleaves, one
@@ -729,6 +730,10 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, ROWS, TAB, RES>::kMinCtas)
                         for (int e = 0; e < NE; ++e)
                             if (row_ok(n, e)) mx = fmaxf(mx, fmaxf(x[tt][n][e], x[tt][n][e + 2]));
                     keep[tt] = __any_sync(0xffffffffu, mx >= p.sparse_tau);
+                    if (FULL || tt == 0 || two) {
+                        ++tiles_seen;
+                        tiles_skipped += keep[tt] ? 0u : 1u;
+                    }
                 }
             }
 
@@ -834,6 +839,10 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, ROWS, TAB, RES>::kMinCtas)
         }
 
         if (pos + nchunks >= hi) griddep_launch_dependents();  // last segment: let the merge launch
+        if (sparse && lane == 0 && tiles_seen) {
+            atomicAdd(p.sparse_tiles, tiles_skipped);
+            atomicAdd(p.sparse_tiles + 1, tiles_seen);
+        }
         if (stalled) {
             // Drain this warp's copies still in flight (bounded), flag, and stop.
             for (int k = 0; k < C::kStages; ++k) {

@@ -30,6 +30,7 @@ struct DecodeParams {
     int32_t num_ctas;         // decode grid (one wave of token-balanced CTAs)
     float scale_log2e;        // softmax scale * log2(e)
     float sparse_tau;         // sparse-V threshold on the softmax weight (0: off)
+    uint32_t* sparse_tiles;   // sparse V: [0] += 16-token tiles skipped, [1] += tiles judged
     int32_t table;            // 1: records carry their centroid x norm table (no norms)
     uint32_t ktab[4];         // prmt byte tables of the K codebook (lo0, lo1, hi0, hi1)
     uint32_t vtab[4];
@@ -197,7 +198,7 @@ int launch_decode_plan(const DecodePlan& pl, const tq_cache* c, const CodebookTa
                        const CodebookTables& vt, const uint32_t signs[4], const CUtensorMap* kmap,
                        const void* q, int num_q_heads, int tq_rows, int max_len_hint, float scale,
                        float tau, void* out, float* part, uint32_t* status, cudaStream_t stream,
-                       cudaEvent_t ev0, cudaEvent_t ev1);
+                       cudaEvent_t ev0, cudaEvent_t ev1, uint32_t* sparse_tiles = nullptr);
 
 }  // namespace host
 

@@ -6,13 +6,18 @@
 // only the output inverse-rotated (mlxcel pull request #369, Change) -- for
 // blocks of many queries (a prefill chunk), where every K/V tile serves 128
 // query rows and the two products are dense GEMMs:
-//   S[128 rows x 128 tok]  = Q'[128 x 128] . K^T     (8 MMAs of K = 16, fp32 in TMEM)
+//   S[128 rows x 128 tok]  = Q'[128 x 128] . K^T     (8 or 16 MMAs of K = 16, fp32 in TMEM)
 //   O[128 rows x 128 dim] += P[128 x 128 tok] . V    (8 MMAs, fp32 in TMEM)
-// Q' = Rot(q) * scale * log2(e) in fp16; K and V are dequantised once per
-// tile into shared memory (the 128-byte-swizzled K-major layout the MMA
-// descriptors read): K as the fp16 centroids c[idx], its norm applied to the
-// scores in fp32; V transposed, [dim][token], as fp16 c[idx] * n_v (a tile
-// has half as many V values as P values, so the norm goes there).
+// Q' = Rot(q) (quantized K) or q (fp16 K); the softmax scale * log2(e) and
+// the K norm are applied to the fp32 scores.  fp16 K: q and K are fp16
+// inputs, their products exact.  Quantized K: Rot(q) is not an fp16 value,
+// so it is split into q_hi = fp16(Rot q) and q_lo = fp16(Rot q - q_hi) and S
+// takes both products (16 MMAs of K = 16 per query tile instead of 8); the K
+// tile holds the fp16 centroids c[idx], exact for a codebook of fp16 values
+// (other codebooks are not taken by this kernel).  K and V are dequantised
+// once per tile into shared memory (the 128-byte-swizzled K-major layout the
+// MMA descriptors read); V transposed, [dim][token], as fp16 c[idx] * n_v (a
+// tile has half as many V values as P values, so the norm goes there).
 //
 // CTA = 256 threads on one (batch, kv head, pair of 128-row query tiles):
 // thread = one query row (tensor-memory lane) of one tile, so each K/V tile is
@@ -34,19 +39,22 @@ struct PreCfg {
     static constexpr int kTile = 128;                           // tokens per tile = rows per CTA
     static constexpr int kRbK = (KB == 0) ? 256 : KB * 16;
     static constexpr int kRbV = VB * 16;
-    static constexpr int kQOff = 0;                             // fp16 Q' of the two query tiles (64 KB)
+    static constexpr int kQOff = 0;                             // fp16 Q' (q_hi) of the two query tiles (64 KB)
     static constexpr int kVtOff = 65536;                        // fp16 V^T [dim][token] (32 KB)
     static constexpr int kKOff = 98304;                         // fp16 K [token][dim] (quantized K)
-    static constexpr int kStgOff = kKOff + ((KB == 0) ? 0 : 32768);
+    static constexpr int kQloOff = kKOff + 32768;               // fp16 q_lo of the two tiles (quantized K, 64 KB)
+    static constexpr int kStgOff = (KB == 0) ? kKOff : kQloOff + 65536;
     // staging slot: K (fp16 K: the MMA tile itself, 32 KB; else records), K norms, V records, V norms
     static constexpr int kSK = (KB == 0) ? 32768 : kTile * kRbK;
     static constexpr int kSKn = (KB == 0) ? 0 : kTile * 2;
     static constexpr int kSV = kTile * kRbV;
     static constexpr int kSVn = kTile * 2;
     static constexpr int kSlotRaw = kSK + kSKn + kSV + kSVn;
-    static constexpr int kSlot = (kSlotRaw + 1023) / 1024 * 1024;
-    static constexpr int kColOff = kStgOff + 2 * kSlot;         // fp32 n_k[128], n_v[128]
-    static constexpr int kBarOff = kColOff + 2 * kTile * 4;     // stg[2], S, O mbarriers + TMEM slot
+    // (fp16 K is read by the MMA straight from the slot: 1024-byte aligned)
+    static constexpr int kSlotAlign = (KB == 0) ? 1024 : 128;
+    static constexpr int kSlot = (kSlotRaw + kSlotAlign - 1) / kSlotAlign * kSlotAlign;
+    static constexpr int kColOff = kStgOff + 2 * kSlot;         // fp32 n_k * scale * log2(e) [128]
+    static constexpr int kBarOff = kColOff + kTile * 4;         // stg[2], S, O mbarriers + TMEM slot
     static constexpr int kSmem = kBarOff + 64;
     static constexpr int kSmemAlloc = kSmem + 1024;             // base alignment slack
     static constexpr uint32_t kIdesc = umma_idesc_f16_f32(128, 128);
@@ -121,8 +129,7 @@ __global__ void __launch_bounds__(256, 1)
 
     uint8_t* sQ = smem + C::kQOff;       // [2][128 x 128] fp16
     uint8_t* sVt = smem + C::kVtOff;
-    float* colK = reinterpret_cast<float*>(smem + C::kColOff);  // n_k per token (1 for fp16 K)
-    float* colV = colK + C::kTile;                              // n_v per token
+    float* colK = reinterpret_cast<float*>(smem + C::kColOff);  // n_k * scale * log2(e) per token (quantized K)
     const uint32_t bar_stg = smem_u32(smem + C::kBarOff);       // 2 x 8 bytes
     const uint32_t bar_s = bar_stg + 16, bar_o = bar_stg + 24;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 32);
@@ -161,8 +168,9 @@ __global__ void __launch_bounds__(256, 1)
     // P as fp16 pairs), then O (128)
     if (warp == 0) tmem_alloc(smem_u32(tslot), 512);
 
-    // ---- Q' = Rot(q) * scale * log2(e) (symmetric modes) or q * scale * log2(e) ----
+    // ---- Q' = Rot(q) as q_hi + q_lo (quantized K) or q (fp16 K) ----
     uint8_t* sQt = sQ + tl * 32768;
+    uint8_t* sQlt = smem + C::kQloOff + tl * 32768;
     {
         float x[128];
         if (row_ok) {
@@ -178,24 +186,33 @@ __global__ void __launch_bounds__(256, 1)
                     x[k + 2 * e + 1] = f.y;
                 }
             }
-            float f = p.scale_log2e;
             if constexpr (KB != 0) {
 #pragma unroll
                 for (int k = 0; k < 128; ++k) x[k] = ((p.signs[k >> 5] >> (k & 31)) & 1u) ? -x[k] : x[k];
                 wht128_thread(x);
-                f *= 0.08838834764831845f;  // 1/sqrt(128)
-            }
 #pragma unroll
-            for (int k = 0; k < 128; ++k) x[k] *= f;
+                for (int k = 0; k < 128; ++k) x[k] *= 0.08838834764831845f;  // 1/sqrt(128)
+            }
         } else {
 #pragma unroll
             for (int k = 0; k < 128; ++k) x[k] = 0.f;
         }
 #pragma unroll
-        for (int k = 0; k < 128; k += 8)
-            *reinterpret_cast<uint4*>(sQt + sw128_offset(r, k)) =
-                make_uint4(pack_half2(x[k], x[k + 1]), pack_half2(x[k + 2], x[k + 3]),
-                           pack_half2(x[k + 4], x[k + 5]), pack_half2(x[k + 6], x[k + 7]));
+        for (int k = 0; k < 128; k += 8) {
+            uint32_t hv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) hv[e] = pack_half2(x[k + 2 * e], x[k + 2 * e + 1]);
+            *reinterpret_cast<uint4*>(sQt + sw128_offset(r, k)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            if constexpr (KB != 0) {  // q_lo = Rot(q) - q_hi (exact in fp32), rounded once more
+                uint32_t lv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hv[e]));
+                    lv[e] = pack_half2(x[k + 2 * e] - hf.x, x[k + 2 * e + 1] - hf.y);
+                }
+                *reinterpret_cast<uint4*>(sQlt + sw128_offset(r, k)) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -225,12 +242,11 @@ __global__ void __launch_bounds__(256, 1)
         {
             const int tk = tid >> 1, hf = tid & 1;
             const bool ok = tok0 + tk < t_lim;
-            if (hf == 0) {
-                const __half* vnorm = reinterpret_cast<const __half*>(slot + C::kSK + C::kSKn + C::kSV);
-                float nk = 1.f;
-                if constexpr (KB != 0) nk = __half2float(reinterpret_cast<const __half*>(slot + C::kSK)[tk]);
-                colK[tk] = ok ? nk : 0.f;
-                colV[tk] = ok ? __half2float(vnorm[tk]) : 0.f;
+            if constexpr (KB != 0) {
+                if (hf == 0) {
+                    const float nk = __half2float(reinterpret_cast<const __half*>(slot + C::kSK)[tk]);
+                    colK[tk] = ok ? nk * p.scale_log2e : 0.f;
+                }
             }
             if constexpr (KB != 0) {
                 const uint8_t* rec = slot + tk * C::kRbK;
@@ -261,6 +277,10 @@ __global__ void __launch_bounds__(256, 1)
                     const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
                     umma_f16(tmem + 256 * t2, umma_desc_sw128(smem_u32(sQ) + t2 * 32768 + koff),
                              umma_desc_sw128(smem_u32(sK) + koff), C::kIdesc, kk > 0 ? 1u : 0u);
+                    if constexpr (KB != 0)  // + q_lo . K^T
+                        umma_f16(tmem + 256 * t2,
+                                 umma_desc_sw128(smem_u32(smem + C::kQloOff) + t2 * 32768 + koff),
+                                 umma_desc_sw128(smem_u32(sK) + koff), C::kIdesc, 1u);
                 }
             umma_commit(bar_s);
         }
@@ -275,6 +295,7 @@ __global__ void __launch_bounds__(256, 1)
             const int lane = tid & 31, g = lane >> 2, tq4 = lane & 3;
             const int ta = 16 * warp + g, tb = ta + 8;
             const uint8_t* vrec = slot + C::kSK + C::kSKn;
+            const __half* vnorm = reinterpret_cast<const __half*>(slot + C::kSK + C::kSKn + C::kSV);
             // tokens past the end: stale records still decode to finite
             // centroids, and their norm (and weight) is 0
             uint32_t ha[16], hb[16];
@@ -282,7 +303,8 @@ __global__ void __launch_bounds__(256, 1)
             dequant_q32<VB>(vrec + tb * C::kRbV + tq4 * (C::kRbV / 4), vt, hb);
             // n_v scales the stored values, so P itself goes to the MMA: 128 x
             // 128 multiplies a tile instead of the 256 x 128 of scaling P
-            const __half2 na = __float2half2_rn(colV[ta]), nb = __float2half2_rn(colV[tb]);
+            const __half2 na = tok0 + ta < t_lim ? __half2half2(vnorm[ta]) : __float2half2_rn(0.f);
+            const __half2 nb = tok0 + tb < t_lim ? __half2half2(vnorm[tb]) : __float2half2_rn(0.f);
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const __half2 a = __hmul2(*reinterpret_cast<const __half2*>(&ha[k]), na);
@@ -319,13 +341,14 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[32 * c + e] = __uint_as_float(v[e]);
         }
-        // t = s * n_k - base in one FFMA per score; the base moves only when a
+        // t = s * n_k * scale * log2(e) - base in one FFMA per score; the base moves only when a
         // score passes it by more than 4 (so p <= 16 in fp16)
         const bool fresh = (m_base == -INFINITY);
         const float base0 = fresh ? 0.f : m_base;
 #pragma unroll
         for (int e = 0; e < 128; e += 4) {
-            float4 nk = make_float4(1.f, 1.f, 1.f, 1.f);
+            const float sl = p.scale_log2e;
+            float4 nk = make_float4(sl, sl, sl, sl);
             if constexpr (KB != 0) nk = *reinterpret_cast<const float4*>(colK + e);
             x[e] = fmaf(x[e], nk.x, -base0);
             x[e + 1] = fmaf(x[e + 1], nk.y, -base0);

@@ -38,24 +38,32 @@ def _gpu():
 
 
 CASES = [
-    # mode, B, Hq, Hkv, lengths, Tq, cap, max_len hint (None = max length)
-    ("turbo4", 1, 8, 2, [300], 300, 304, None),            # prompt into an empty cache, G 4
-    ("turbo3", 2, 28, 4, [700, 450], 200, 704, None),      # chunk behind a context, G 7, ragged
-    ("turbo4_asym", 1, 4, 2, [513], 513, 528, None),       # fp16 K through the tensor map, G 2
-    ("turbo3_asym", 1, 8, 8, [260], 130, 272, None),       # G 1: 128 positions per tile
-    ("turbo4k_3v", 1, 16, 2, [1000], 64, 1008, None),      # G 8
-    ("turbo4", 2, 8, 2, [100, 37], 1, 112, None),          # Tq 1
-    ("turbo3", 1, 8, 2, [600], 300, 608, 450),             # hint below the length
+    # mode, B, Hq, Hkv, lengths, Tq, cap, max_len hint (None = max length), q scale
+    ("turbo4", 1, 8, 2, [300], 300, 304, None, 1.0),            # prompt into an empty cache, G 4
+    ("turbo3", 2, 28, 4, [700, 450], 200, 704, None, 1.0),      # chunk behind a context, G 7, ragged
+    ("turbo4_asym", 1, 4, 2, [513], 513, 528, None, 1.0),       # fp16 K through the tensor map, G 2
+    ("turbo3_asym", 1, 8, 8, [260], 130, 272, None, 1.0),       # G 1: 128 positions per tile
+    ("turbo4k_3v", 1, 16, 2, [1000], 64, 1008, None, 1.0),      # G 8
+    ("turbo4", 2, 8, 2, [100, 37], 1, 112, None, 1.0),          # Tq 1
+    ("turbo3", 1, 8, 2, [600], 300, 608, 450, 1.0),             # hint below the length
+    # peaked softmax: scores of 20 .. 100, where one fp16 rounding of the
+    # rotated query would move the dominant weights by a per cent
+    ("turbo4", 1, 8, 2, [300], 300, 304, None, 8.0),
+    ("turbo3", 2, 28, 4, [700, 450], 200, 704, None, 32.0),
+    ("turbo4_asym", 1, 4, 2, [513], 513, 528, None, 32.0),
+    ("turbo4k_3v", 1, 16, 2, [1000], 64, 1008, None, 16.0),
+    ("turbo3_asym", 1, 8, 8, [260], 130, 272, None, 32.0),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-Hq{c[2]}-Hkv{c[3]}-L{max(c[4])}-Tq{c[5]}")
+@pytest.mark.parametrize("case", CASES,
+                         ids=lambda c: f"{c[0]}-Hq{c[2]}-Hkv{c[3]}-L{max(c[4])}-Tq{c[5]}-q{c[8]:g}")
 def test_prefill_same_cache(case):
-    mode, B, Hq, Hkv, lengths, Tq, cap, hint = case
+    mode, B, Hq, Hkv, lengths, Tq, cap, hint, qs = case
     hint = hint or max(lengths)
     key = 12000 + sum(lengths) + Tq
     kd, kn, vd, vn = H.random_cache(mode, B, Hkv, cap, key)
-    q = wl.random_fp16(key + 5, (B, Hq, Tq, 128))
+    q = wl.random_fp16(key + 5, (B, Hq, Tq, 128), scale=qs)
     cache = H.gpu_cache_from_records(mode, B, Hkv, cap, lengths, kd, kn, vd, vn, DEV, v_rescale=0.5)
     ctx = tqf.Context()
     qd = H.upload(q, DEV)
@@ -95,6 +103,18 @@ def test_prefill_tq1_matches_decode_kernel():
     tqf.tq_decode_attention(ctx, cache, q, d, 2000)
     torch.cuda.synchronize()
     H.assert_attention_close(a.float().cpu().numpy(), d.float().cpu().numpy(), "prefill vs decode")
+
+
+def test_prefill_rejects_a_codebook_of_non_fp16_levels():
+    mode, B, Hq, Hkv, cap = "turbo4", 1, 8, 2, 64
+    kd, kn, vd, vn = H.random_cache(mode, B, Hkv, cap, 31)
+    cache = H.gpu_cache_from_records(mode, B, Hkv, cap, [40], kd, kn, vd, vn, DEV,
+                                     codebook_k=H.exact_lloyd_max(4))
+    q = H.upload(wl.random_fp16(32, (B, Hq, 8, 128)), DEV)
+    out = torch.empty_like(q)
+    with pytest.raises(tqf.TqError) as e:
+        tqf.tq_prefill_attention(tqf.Context(), cache, q, out, 40)
+    assert e.value.code == tqf.TQ_ERR_UNSUPPORTED
 
 
 def test_prefill_after_own_append_end_to_end():

@@ -99,7 +99,7 @@ def test_sparse_v_skips_tiles_after_a_dominant_token(mode, Tq):
     kb, _ = H.MODE_BITS[mode]
     for h in range(Hkv):
         d = q_np[0, h * G:(h + 1) * G].astype(np.float64).reshape(-1, 128).sum(0)
-        k_star = (0.1 * d).astype(np.float16)
+        k_star = (0.3 * d).astype(np.float16)   # a score some 50 above the others: every row
         if kb == 16:
             kd[0, h, 0:L:32] = k_star
         else:
@@ -113,6 +113,12 @@ def test_sparse_v_skips_tiles_after_a_dominant_token(mode, Tq):
     tqf.tq_decode_attention_sparse_v(ctx, cache, q, sparse, L, tau)
     tqf.tq_decode_attention(ctx, cache, q, full, L)
     torch.cuda.synchronize()
+    # the tile counters: every tile of every unit judged once, the second tile
+    # of (nearly) every chunk skipped; the plain decode counts nothing
+    skipped, judged = tqf.tq_get_sparse_v_tiles(ctx)
+    assert judged == Hkv * ((L + 15) // 16)     # one row group per kv head here
+    assert 0.3 * judged <= skipped < judged, (skipped, judged)
+    assert tqf.tq_get_sparse_v_tiles(ctx) == (0, 0)
     units = {(0, h): H.oracle_unit_from_records(mode, kd, kn, vd, vn, 0, h, L) for h in range(Hkv)}
     sc = 1 / math.sqrt(128)
     want_full = H.oracle_decode(mode, q_np, units, [L], Hkv, Tq, sc, 1.0)
