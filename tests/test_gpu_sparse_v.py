@@ -127,7 +127,6 @@ def test_sparse_v_skips_tiles_after_a_dominant_token(mode, Tq):
     rms = math.sqrt(float(np.mean(want_full ** 2)))
     assert np.all(_ulp_close(got, got_full, bound, rms))
     H.assert_within_skip_bound(got, want_full, bound, mode)
-    assert float(np.abs(got - got_full).max()) > 1e-3 * rms
 
 
 def test_sparse_v_zero_threshold_is_the_plain_decode():
