@@ -255,14 +255,16 @@ def _crafted_vectors():
     return np.stack(v)
 
 
-# T = 300 runs the warp-per-vector kernel (small appends), T = 700 the
-# four-lanes-per-vector kernel (more than 4096 vectors per stream)
-@pytest.mark.parametrize("T", [300, 700])
+# T = 300 runs the warp-per-vector kernel (small appends), T = 700 and 1029
+# the four-lanes-per-vector kernel (more than 4096 vectors per stream; 1029
+# leaves a ragged last CTA of vectors)
+@pytest.mark.parametrize("T", [300, 700, 1029])
 @pytest.mark.parametrize("mode", ["turbo3", "turbo4", "turbo4_asym", "turbo3_asym", "turbo4k_3v",
                                   "turbo3_table"])
 def test_encode_append_bit_exact(mode, T):
     kb, vb = H.MODE_BITS[mode]
-    B, Hkv, cap = 2, 3, 720
+    B, Hkv = 2, 3
+    cap = (T + 5 + 15) // 16 * 16
     rng = np.random.default_rng(3)
     k = wl.random_fp16(11, (B, Hkv, T, 128))
     v = wl.random_fp16(12, (B, Hkv, T, 128), scale=3.0)

@@ -33,10 +33,14 @@ CASES = [
     ("turbo4", 2, 8, 2, [3000, 777], 1, 3008),
     ("turbo4_asym", 1, 28, 4, [5000], 1, 5008),
     ("turbo3", 1, 32, 8, [4100], 4, 4112),
+    ("turbo3_table", 2, 16, 4, [2049, 300], 1, 2064),   # records carrying their centroid x norm tables
+    # 67 x 30 = 2010 (batch, kv head) units of a 2016-slot array: the decode
+    # grid is cut to the 6 slots left
+    ("turbo4k_3v", 67, 60, 30, [((37 * i) % 60) + 4 for i in range(67)], 1, 64),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: c[0])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-B{c[1]}")
 def test_noalloc_matches_regular_decode_on_two_calls(dev, case):
     mode, B, Hq, Hkv, lengths, Tq, cap = case
     key = 31000 + sum(lengths)
