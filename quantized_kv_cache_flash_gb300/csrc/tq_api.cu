@@ -196,6 +196,19 @@ int encode_kmap(CUtensorMap* map, const tq_cache* c) {
     return r == CUDA_SUCCESS ? TQ_OK : TQ_ERR_CUDA;
 }
 
+int encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_tiled();
+    if (enc == nullptr) return TQ_ERR_CUDA;
+    cuuint64_t dims[2] = {kD, rows};
+    cuuint64_t strides[1] = {kD * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TQ_OK : TQ_ERR_CUDA;
+}
+
 constexpr int kSMs = 152;  // GB300 (only used to size the split grid)
 
 // Decode grid: two waves of resident CTAs (the second lets the block
@@ -302,7 +315,7 @@ int launch_decode_plan(const DecodePlan& pl, const tq_cache* c, const CodebookTa
 
 struct tq_ctx {
     int device = -1;
-    uint32_t* d_words = nullptr;  // [0] status, [1] encode ticket counter, [2..3] sparse-V tiles
+    uint32_t* d_words = nullptr;  // [0] status, [1] encode ticket counter, [2..3] sparse-V tiles, [4] encode tile counter
     float* d_work = nullptr;
     size_t work_bytes = 0;
     CodebookTables ktab, vtab;
@@ -522,10 +535,13 @@ int tq_encode_append(tq_ctx** pctx, const tq_cache* c, const void* k_new, const 
     p.lengths = c->lengths;
     p.status = ctx->d_words;
     p.counter = ctx->d_words + 1;
+    p.tiles_next = ctx->d_words + 4;
     p.batch = c->batch;
     p.hkv = c->num_kv_heads;
     p.t_new = t_new;
     p.cap = c->capacity;
+    tq::div_magic(uint32_t(t_new), &p.div_t_m, &p.div_t_s);
+    tq::div_magic(uint32_t(c->num_kv_heads), &p.div_h_m, &p.div_h_s);
     std::memcpy(p.signs, ctx->signs, sizeof(p.signs));
     if (kb != 16) {
         std::memcpy(p.k_gt, ctx->ktab.gt, sizeof(p.k_gt));
@@ -538,9 +554,16 @@ int tq_encode_append(tq_ctx** pctx, const tq_cache* c, const void* k_new, const 
         std::memcpy(p.k_cb, c->codebook_k, sizeof(p.k_cb));
         std::memcpy(p.v_cb, c->codebook_v, sizeof(p.v_cb));
     }
+    CUtensorMap kmap, vmap;
+    const uint64_t nvec = uint64_t(c->batch) * c->num_kv_heads * t_new;
+    if (nvec > uint64_t(tq::kEncodeSmallMax)) {
+        if ((r = tq::host::encode_rows_map(&kmap, k_new, nvec)) != TQ_OK ||
+            (r = tq::host::encode_rows_map(&vmap, v_new, nvec)) != TQ_OK)
+            return r;
+    }
     ctx->last_stream = static_cast<cudaStream_t>(stream);
     return cuda_err(static_cast<cudaError_t>(
-        tq::launch_encode(kb, vb, p, static_cast<cudaStream_t>(stream))));
+        tq::launch_encode(kb, vb, p, &kmap, &vmap, static_cast<cudaStream_t>(stream))));
 }
 
 }  // extern "C"

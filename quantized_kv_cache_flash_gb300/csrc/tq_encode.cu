@@ -1,7 +1,7 @@
 // Encode/append: fp16 K/V vectors -> (fp16 norm, packed b-bit codes) written
 // at each sequence's current length, then lengths[b] += t_new.
 //
-// Per vector (four lanes of a warp, lane q holds dims 32q .. 32q+31):
+// Per vector:
 //   n16  = fp16 round-to-nearest-even of the exact L2 norm: fp32 sum of the
 //          exact squares, certified against the rounding midpoints; if it is
 //          too close to call, the sum of squares is formed exactly as a
@@ -11,10 +11,15 @@
 //   code = sign-magnitude index of the nearest codebook entry to u, decided
 //          with thresholds that make the fp32 comparison exact against the
 //          true midpoints of neighbouring centroids (ties to the lower index).
+// Large appends rotate 128 vectors at a time on the tensor cores (one thread
+// per vector afterwards); small appends (a decode step's tokens) give each
+// vector a warp and rotate with shuffles.
 // (The encode of mlxcel pull request #369, Change: seeded sign flip, Walsh-
 // Hadamard rotation, nearest codebook entry, bit packing; turboquant_plus
 // smem-dequant experiment, Hypothesis 1: a 128-element rotation group with
 // one norm per group.)
+#include <type_traits>
+
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
@@ -101,46 +106,28 @@ __device__ __forceinline__ unsigned short norm_to_half(U128 S) {
     return hb;
 }
 
-// Exact fp16 norm of one vector whose 4 lanes each hold 32 dims; reloads the
-// lane's 32 fp16 values from src (out of line: it is the rare path of
-// norm_fp16 below).  gmask = the group's lanes.
-__device__ __noinline__ unsigned short norm_exact_group(const __half* src, int q, bool valid,
-                                                        unsigned gmask) {
-    U128 S;
-    S.lo = 0;
-    S.hi = 0;
-    if (valid) {
-        const __half* x = src + q * 32;
-        for (int i = 0; i < 32; ++i) S = add128(S, sq_u128(fp16_scaled_int(__half2float(x[i]))));
-    }
-#pragma unroll
-    for (int m = 1; m <= 2; m <<= 1) {
-        U128 o;
-        o.lo = __shfl_xor_sync(gmask, S.lo, m);
-        o.hi = __shfl_xor_sync(gmask, S.hi, m);
-        S = add128(S, o);
-    }
-    return norm_to_half(S);
-}
 
 __device__ __forceinline__ float half_bits_to_float(unsigned short b) {
     return (b >= 0x7C00u) ? 65536.f : __half2float(__ushort_as_half(b));
 }
 
-// norm_fp16: fp16 round-to-nearest-even of the exact norm sqrt(sum x^2).  Fast path: the
-// fp32 sum of the (exact) squares is within 2^-17 (relative) of the exact sum,
-// so the candidate rounding of its square root is certain unless the sum lies
-// within 2^-16 of the square of a rounding midpoint (midpoints have 12
-// significant bits, so their squares are exact in fp32); then the exact
-// 128-bit integer path decides.
-// Candidate fp16 rounding of sqrt(S32) and whether it is certain (see norm_fp16).
+// The fp16 norm (round to nearest even of the exact sqrt(sum x^2)).  Fast
+// path: a fp32 sum S32 of the (exact) squares whose every term goes through
+// at most d roundings is within gamma_d = d u / (1 - d u) (u = 2^-24) of the
+// exact sum S, relative; so the candidate rounding of sqrt(S32) is certain
+// unless S32 lies within a margin above gamma_d of the square of a rounding
+// midpoint (midpoints have 12 significant bits, so their squares are exact in
+// fp32); then the exact 128-bit integer path decides.  MARGIN_LOG2: the
+// margin is S32 * 2^-MARGIN_LOG2 (2^-19 covers d = 18, 2^-20 covers d = 8).
+// Candidate fp16 rounding of sqrt(S32) and whether it is certain.
+template <int MARGIN_LOG2>
 __device__ __forceinline__ unsigned short norm_candidate(float S32, bool& certain) {
     certain = true;
     if (S32 == 0.f) return 0;
     const float n = sqrtf(S32);
     unsigned short hb = __half_as_ushort(__float2half_rn(n));
     if (hb > 0x7C00u) hb = 0x7C00u;
-    const float margin = S32 * (1.0f / 65536.0f);
+    const float margin = S32 * (1.0f / static_cast<float>(1u << MARGIN_LOG2));
     const float hf = half_bits_to_float(hb);
     if (hb < 0x7C00u) {
         const float up = 0.5f * (hf + half_bits_to_float(hb + 1));
@@ -154,13 +141,6 @@ __device__ __forceinline__ unsigned short norm_candidate(float S32, bool& certai
     return hb;
 }
 
-__device__ __forceinline__ unsigned short norm_fp16(const __half* src, int q, bool valid,
-                                                    float S32, unsigned gmask) {
-    bool ok;
-    const unsigned short hb = norm_candidate(S32, ok);
-    const bool all_ok = __all_sync(gmask, ok);   // the group decides together
-    return all_ok ? hb : norm_exact_group(src, q, valid, gmask);
-}
 
 // Sign-magnitude code of the centroid nearest to u: rank = #{tau_k < |u|} for
 // u > 0 and #{tau_k <= |u|} for u <= 0, with gt[k] / ge[k] the smallest fp32
@@ -193,8 +173,7 @@ __device__ __forceinline__ uint32_t quantize_code(float u, const float* gt, cons
     return (neg ? static_cast<uint32_t>(H) : 0u) | rank;
 }
 
-// Encode the vectors of one warp: 8 vectors, 4 lanes each; lane quarter q
-// holds dims 32q .. 32q+31.  `valid` marks lanes whose vector exists.
+
 // The record's norm (norm format) or, for table records (tcb != nullptr), the
 // eight fp16 values c_j * n16 after the 48 code bytes: c_j (fp32) times n16
 // (fp16) is exact in double, so each value is one rounding of the exact
@@ -216,164 +195,10 @@ __device__ __forceinline__ void store_norm(__half* dst_norm, uint8_t* dst, const
     *reinterpret_cast<uint4*>(dst + 48) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// XOR masks that apply a lane's 32 signs to its dims as fp16 pairs: word k
-// flips dim 2k with bit 15 and dim 2k+1 with bit 31.
-__device__ __forceinline__ void sign_masks(uint32_t sg, uint32_t (&hm)[16]) {
-#pragma unroll
-    for (int k = 0; k < 16; ++k) hm[k] = (((sg >> (2 * k)) & 1u) << 15) | (((sg >> (2 * k + 1)) & 1u) << 31);
-}
-
-// Encode one vector per 4 lanes (8 per warp); lane quarter q holds dims
-// 32q .. 32q+31.  `valid` marks lanes whose vector exists.  The codes compare
-// the unnormalised rotated value y = H (s * x) / sqrt(128) ... scaled back:
-// u = y / n > tau_k  <=>  y > tau_k * sqrt(128) * n  for the fp32 norm n, so
-// the thresholds are scaled once per vector instead of every u divided.  The
-// fp32 rotation and scaling are within ~1e-7 (relative) of the exact u;
-// elements that close to a midpoint may round either way (a zero u is
-// negative: the tie goes to the lower index).
-// The lane's 32 fp16 inputs (64 bytes), or zeros for a lane without a vector.
-struct QuarterIn {
-    uint4 w[4];
-};
-
-__device__ __forceinline__ QuarterIn load_quarter_in(const __half* src, int q, bool valid) {
-    QuarterIn r;
-    const uint4* s4 = reinterpret_cast<const uint4*>(src + q * 32);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) r.w[i] = valid ? s4[i] : make_uint4(0u, 0u, 0u, 0u);
-    return r;
-}
-
-template <int BITS>
-__device__ __forceinline__ void encode_group(const QuarterIn& in, const __half* src, uint8_t* dst,
-                                             __half* dst_norm, const float* tcb,
-                                             const uint32_t (&hm)[16], const float* gt, bool valid,
-                                             uint32_t* status, int q, unsigned gmask) {
-    float x[32];  // s * x for the lane's dims
-    {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint4 w = in.w[i];
-            const uint32_t ww[4] = {w.x ^ hm[4 * i], w.y ^ hm[4 * i + 1], w.z ^ hm[4 * i + 2],
-                                    w.w ^ hm[4 * i + 3]};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[k]));
-                x[8 * i + 2 * k] = f.x;
-                x[8 * i + 2 * k + 1] = f.y;
-            }
-        }
-    }
-    if (!valid) {  // a lane without a vector takes part in the shuffles with zeros
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = 0.f;
-    }
-
-    // norm: squares of fp16 values are exact in fp32 (the signs do not matter)
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) ss = fmaf(x[i], x[i], ss);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    const float S32 = __shfl_sync(0xffffffffu, ss, 0, 4);   // one rounding order per group
-    const unsigned short nb = norm_fp16(src, q, valid, S32, gmask);
-    if (valid && q == 0) {
-        store_norm(dst_norm, dst, tcb, nb);
-        if (nb >= 0x7C00u) atomicOr(status, kStatusNormOverflow);
-    }
-
-    // rotate: H (s * x), 5 in-lane stages + 2 across the group's lanes
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if (i & h) continue;
-            const float a = x[i], b = x[i + h];
-            x[i] = a + b;
-            x[i + h] = a - b;
-        }
-    }
-#pragma unroll
-    for (int m = 1; m <= 2; m <<= 1) {
-        const float sgn = (q & m) ? -1.f : 1.f;   // upper half of the pair: o - x
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
-            x[i] = fmaf(sgn, x[i], o);
-        }
-    }
-
-    constexpr int H = 1 << (BITS - 1);
-    const float scale = sqrtf(S32) * 11.313708498984761f;   // sqrt(128) n
-    float T[H - 1];
-#pragma unroll
-    for (int k = 0; k < H - 1; ++k) T[k] = gt[k] * scale;
-    if (!valid) return;
-    if constexpr (BITS == 4) {
-        // word k = dims 8k..8k+7: rank of dim 8k+j in bits 4j..4j+2; sign of dim
-        // 8k+j (j < 4) in bit 8j+7, of dim 8k+4+j in bit 8j+3
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float y = x[8 * k + j];
-                const float a = fabsf(y);
-                const bool b2 = a > T[3];
-                const bool b1 = a > (b2 ? T[5] : T[1]);
-                const float t0 = b2 ? (b1 ? T[6] : T[4]) : (b1 ? T[2] : T[0]);
-                const bool b0 = a > t0;
-                const uint32_t rank = (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u);
-                v |= rank << (4 * j);
-                if (!(y > 0.f)) v |= 1u << (j < 4 ? 8 * j + 7 : 8 * (j - 4) + 3);
-            }
-            w[k] = v;
-        }
-        *reinterpret_cast<uint4*>(dst + q * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-    } else {
-        // sign-magnitude code kappa = sign << 2 | rank; quarter q: word k (k < 3):
-        // bits 4j..4j+2 = code(8k+j), bit 4j+3 = bit k of code(24+j).  The
-        // comparisons give 0.0 / 1.0 and the words are summed in fp32 as two
-        // 16-bit halves (exact: every partial sum is an integer below 2^16).
-        float h[3][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float y = x[i];
-            const float a = fabsf(y);
-            const bool b1 = a > T[1];
-            const float f1 = b1 ? 1.f : 0.f;
-            const float f0 = (a > (b1 ? T[2] : T[0])) ? 1.f : 0.f;
-            const float fn = (y > 0.f) ? 0.f : 1.f;
-            if (i < 24) {
-                const int j = i & 7;
-                const float unit = static_cast<float>(1u << (4 * (j & 3)));  // nibble j of the half
-                float& acc = h[i >> 3][j >> 2];
-                acc = fmaf(fn, 4.f * unit, acc);
-                acc = fmaf(f1, 2.f * unit, acc);
-                acc = fmaf(f0, unit, acc);
-            } else {
-                const int j = i - 24;
-                const float bit = static_cast<float>(1u << (4 * (j & 3) + 3));
-                h[0][j >> 2] = fmaf(f0, bit, h[0][j >> 2]);
-                h[1][j >> 2] = fmaf(f1, bit, h[1][j >> 2]);
-                h[2][j >> 2] = fmaf(fn, bit, h[2][j >> 2]);
-            }
-        }
-        uint32_t d[3];
-#pragma unroll
-        for (int k = 0; k < 3; ++k)
-            d[k] = static_cast<uint32_t>(h[k][0]) | (static_cast<uint32_t>(h[k][1]) << 16);
-        uint32_t* o = reinterpret_cast<uint32_t*>(dst + q * 12);
-        o[0] = d[0];
-        o[1] = d[1];
-        o[2] = d[2];
-    }
-}
-
 // Advance lengths[] after the last CTA of the launch has read it: one ticket
 // per CTA, taken once every thread of the CTA has read lengths[] for the last
-// time (so none sees an advanced length); the counter is back at zero for the
+// time (so none sees an advanced length) and, for large appends, its
+// producer has stopped taking tiles; the counters are back at zero for the
 // next launch.
 __device__ __forceinline__ void finish_append(const EncodeParams& p, int lane) {
     __shared__ unsigned int s_ticket;
@@ -389,124 +214,462 @@ __device__ __forceinline__ void finish_append(const EncodeParams& p, int lane) {
             const int Lb = *((volatile int32_t*)p.lengths + bb);
             if (Lb >= 0 && Lb + p.t_new <= p.cap) p.lengths[bb] = Lb + p.t_new;
         }
-        if (lane == 0) *((volatile uint32_t*)p.counter) = 0u;
+        if (lane == 0) {
+            *((volatile uint32_t*)p.counter) = 0u;
+            if (p.tiles_next != nullptr) *((volatile uint32_t*)p.tiles_next) = 0u;
+        }
         __threadfence();
     }
 }
 
-// grid: [K blocks | V blocks]; a CTA of 4 warps encodes 128 vectors of one
-// stream (K or V): each warp takes 8 vectors at a time, 4 lanes each, for 4
-// passes, so a lane's sign masks (its quarter of s) serve 4 vectors.
-// KB = 0 copies fp16 K rows.
-constexpr int kEncWarps = 4;
-constexpr int kEncPasses = 4;
-constexpr int kEncVecs = 8 * kEncWarps * kEncPasses;
+// ---------------------------------------------------------------------------
+// Large appends on the 5th-generation tensor cores.
+//
+// A tile is 128 vectors of one stream (K or V).  Its rotation is one product
+// Y[128 x 128] = X[128 x 128] . B^T with B[n][k] = H[n][k] s_k: the entries
+// are +-1, so every product x_k B[n][k] is exact and only the fp32 sums round
+// (as in a butterfly transform, in another order).  It runs as 8 tcgen05 MMAs
+// of K = 16 into tensor memory; row i of Y (tensor-memory lane i) is vector
+// i's H (s * x), read back by two threads that each encode half of its dims,
+// having formed the vector's exact fp16 norm together (from the tile in
+// shared memory) and scaled the thresholds by sqrt(128) n.  X tiles arrive by
+// TMA in the MMA's K-major 128-byte-swizzled layout (rows past the end are
+// zero-filled).  Persistent CTAs, two per SM, each with B resident in shared
+// memory, two X stages and two tensor-memory accumulators: the copies and
+// MMAs of the next tiles run while a tile is encoded.
+// ---------------------------------------------------------------------------
+constexpr int kTcVecs = 128;                      // vectors per tile = tensor-memory lanes
+constexpr int kTcBOff = 0;                        // B: 128 x 128 fp16 (32 KB)
+constexpr int kTcXOff = 32768;                    // X stages: 2 x 32 KB
+constexpr int kTcBarOff = kTcXOff + 2 * 32768;    // full[2], done[2], xfree[2], afree[2] mbarriers, TMEM slot
+constexpr int kTcSmem = kTcBarOff + 128;
+constexpr int kTcSmemAlloc = kTcSmem + 1024;      // base alignment slack
+constexpr int kTcCtasPerSm = 2;
+constexpr uint32_t kTcIdesc = umma_idesc_f16_f32(128, 128);
+
+__device__ __forceinline__ uint32_t fbits(float f) { return __float_as_uint(f); }
+
+// x * x + acc for an fp16 x, one rounding (the square of an fp16 value is
+// exact in fp32, so this is fmaf(x, x, acc) on the converted value).
+__device__ __forceinline__ float fma_sq_f16(unsigned short x, float acc) {
+    float r;
+    asm("fma.rn.f32.f16 %0, %1, %1, %2;" : "=f"(r) : "h"(x), "f"(acc));
+    return r;
+}
+
+// Codes of the 32 dims of quarter q of a record from their rotated values
+// y = H (s * x) (unnormalised) and the thresholds T_k = gt_k sqrt(128) n, so
+// that |y| > T_k <=> |u| > tau_k for u = y / (sqrt(128) n).  Every decision is
+// a sign bit: c_k = sign(T_k - |y|) = [|y| > T_k] (the sign of a difference
+// is exact), the rank bits are XORs of the c_k (the rank counts the
+// thresholds below |y|), and p = sign(0 - y) = [y > 0] (a zero y is negative:
+// its tie goes to the lower index).  The bits are shifted into the words most
+// significant first (funnel shifts), the sign positions inverted at the end.
+//   3-bit: code = sign << 2 | rank; word k (k < 3): bits 4j..4j+2 = code of
+//          dim 8k+j, bit 4j+3 = bit k of the code of dim 24+j.
+//   4-bit: word k = dims 8k..8k+7: rank of dim 8k+j in bits 4j..4j+2, the
+//          sign of dim 8k+j (j < 4) in bit 8j+7, of dim 8k+4+j in bit 8j+3.
+template <int BITS>
+__device__ __forceinline__ void pack_quarter(const uint32_t (&r)[32],
+                                             const float (&T)[(1 << (BITS - 1)) - 1], uint32_t* w) {
+    auto shin = [](uint32_t acc, uint32_t v) { return __funnelshift_l(v, acc, 1); };  // acc << 1 | v >> 31
+    if constexpr (BITS == 3) {
+        struct Bits {
+            uint32_t b0, b1, p;
+        };
+        auto bits_of = [&](int i) {
+            const float y = __uint_as_float(r[i]);
+            const float a = fabsf(y);
+            const float d0 = T[0] - a, d1 = T[1] - a, d2 = T[2] - a;
+            Bits o;
+            o.b1 = fbits(d1);
+            o.b0 = fbits(d0) ^ fbits(d1) ^ fbits(d2);
+            o.p = fbits(__fsub_rn(0.f, y));
+            return o;
+        };
+        uint32_t a0 = 0, a1 = 0, a2 = 0;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+            const Bits e = bits_of(24 + j);
+            a0 = shin(a0, e.b0);
+            a1 = shin(a1, e.b1);
+            a2 = shin(a2, e.p);
+            const Bits x0 = bits_of(j), x1 = bits_of(8 + j), x2 = bits_of(16 + j);
+            a0 = shin(shin(shin(a0, x0.p), x0.b1), x0.b0);
+            a1 = shin(shin(shin(a1, x1.p), x1.b1), x1.b0);
+            a2 = shin(shin(shin(a2, x2.p), x2.b1), x2.b0);
+        }
+        w[0] = a0 ^ 0x44444444u;
+        w[1] = a1 ^ 0x44444444u;
+        w[2] = a2 ^ 0xCCCCCCCCu;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t b0[8], b1[8], b2[8], p[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float y = __uint_as_float(r[8 * k + j]);
+                const float a = fabsf(y);
+                uint32_t d[7];
+#pragma unroll
+                for (int t = 0; t < 7; ++t) d[t] = fbits(T[t] - a);
+                const uint32_t x135 = d[1] ^ d[3] ^ d[5];
+                b2[j] = d[3];
+                b1[j] = x135;
+                b0[j] = x135 ^ d[0] ^ d[2] ^ d[4] ^ d[6];
+                p[j] = fbits(__fsub_rn(0.f, y));
+            }
+            uint32_t acc = 0;
+#pragma unroll
+            for (int j = 7; j >= 0; --j) {
+                const int s = (j & 1) ? (j - 1) / 2 : 4 + j / 2;   // whose sign sits in bit 4j+3
+                acc = shin(shin(shin(shin(acc, p[s]), b2[j]), b1[j]), b0[j]);
+            }
+            w[k] = acc ^ 0x88888888u;
+        }
+    }
+}
+
+// Exact fp16 norm of row `row` of an X tile (the rare path of the norm): the
+// warp's lane l takes dims 4l..4l+3 and the 128-bit integer sums of their
+// exact squares are added across the warp.
+__device__ __noinline__ unsigned short norm_exact_row(const uint8_t* xs, int row, int lane) {
+    const int c = lane >> 1;  // 16-byte chunk of dims 8c..8c+7
+    const uint8_t* src = xs + (c >> 3) * 16384 + row * 128 + ((((c & 7) ^ (row & 7))) << 4) + (lane & 1) * 8;
+    const uint2 raw = *reinterpret_cast<const uint2*>(src);
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    U128 S = sq_u128(fp16_scaled_int(f0.x));
+    S = add128(S, sq_u128(fp16_scaled_int(f0.y)));
+    S = add128(S, sq_u128(fp16_scaled_int(f1.x)));
+    S = add128(S, sq_u128(fp16_scaled_int(f1.y)));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        U128 o;
+        o.lo = __shfl_xor_sync(0xffffffffu, S.lo, m);
+        o.hi = __shfl_xor_sync(0xffffffffu, S.hi, m);
+        S = add128(S, o);
+    }
+    return norm_to_half(S);
+}
+
+// B[n][k] = H[n][k] s_k as fp16 +-1 in the K-major swizzled layout; thread
+// i (< 256) writes half h = i >> 7 (dims 64h .. 64h+63) of row n = i & 127.
+__device__ __forceinline__ void build_rotation_b(uint8_t* sB, const uint32_t (&signs)[4], int i) {
+    const int n = i & 127, h0 = 8 * (i >> 7);
+#pragma unroll 4
+    for (int c = h0; c < h0 + 8; ++c) {
+        uint32_t hw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int k = 8 * c + 2 * e + h;
+                const uint32_t neg = (__popc(n & k) ^ (signs[k >> 5] >> (k & 31))) & 1u;
+                v |= (0x3C00u | (neg << 15)) << (16 * h);
+            }
+            hw[e] = v;
+        }
+        *reinterpret_cast<uint4*>(sB + sw128_offset(n, 8 * c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    }
+}
+
+// Warp roles: warps 0-7 encode in two groups of four (group g works through
+// X stage g and accumulator g; warp w reads tensor-memory lanes 32 (w & 3) ..
+// +31, one vector per thread), warp 8 hands out the tiles and issues the
+// copies and MMAs.  Tiles ([K tiles (quantized K only) | V tiles], 128
+// vectors each) are taken from one counter for the whole grid, a group's next
+// tile when it has released its stage, so groups on less loaded SMs take
+// more.  Hand-offs by mbarrier, per stage s: full[s] (copy landed, or the
+// end: tile id -1), done[s] (MMA committed), xfree[s] (the group has read X
+// stage s and seen its MMA complete), afree[s] (the group has read
+// accumulator s).  KB = 0 copies the fp16 K rows instead (plain coalesced
+// copies spread over the grid).
+constexpr int kTcEncWarps = 8;
+constexpr int kTcThreads = 32 * (kTcEncWarps + 1);
 
 template <int KB, int VB>
-__global__ void __launch_bounds__(32 * kEncWarps)
-    tq_encode_kernel(const __grid_constant__ EncodeParams p, int k_blocks) {
-    __shared__ unsigned long long s_pos[kEncPasses][32 * kEncWarps];
-    griddep_wait();                // inputs and lengths come from earlier work on the stream
-    griddep_launch_dependents();   // the decode that follows may start launching
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int q = lane & 3;
-    const unsigned gmask = 0xFu << (lane & ~3);
-    const bool is_v = static_cast<int>(blockIdx.x) >= k_blocks;
-    const int blk = is_v ? static_cast<int>(blockIdx.x) - k_blocks : static_cast<int>(blockIdx.x);
-    // vector counts stay below 2^31 (the host checks), so 32-bit index math
-    const int nvec = p.batch * p.hkv * p.t_new;
-    auto vec_of = [&](int pass) { return blk * kEncVecs + (pass * kEncWarps + warp) * 8 + (lane >> 2); };
+__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
+    tq_encode_tc_kernel(const __grid_constant__ EncodeParams p, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap) {
+    extern __shared__ __align__(1024) uint8_t esm_raw[];
+    uint8_t* smem = esm_raw + ((1024u - (smem_u32(esm_raw) & 1023u)) & 1023u);
+    __shared__ int s_tile[2];   // tile in stage s (-1: no more)
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
+    const int nvec = p.batch * p.hkv * p.t_new;   // below 2^31 (the host checks)
+    const int tiles_s = (nvec + kTcVecs - 1) / kTcVecs;
+    const int tiles_k = (KB == 0) ? 0 : tiles_s;
+    const int tiles = tiles_k + tiles_s;
+    const uint32_t bar_full = smem_u32(smem + kTcBarOff);   // + 8 s
+    const uint32_t bar_done = bar_full + 16;                 // + 8 s
+    const uint32_t bar_xfree = bar_full + 32;                // + 8 s
+    const uint32_t bar_afree = bar_full + 48;                // + 8 s
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kTcBarOff + 64);
+    uint8_t* sB = smem + kTcBOff;
 
-    // Every lane first reads the lengths its passes write at and keeps the
-    // record positions (or ~0 for no vector); then the CTA takes its ticket,
-    // so the last CTA advances lengths[] while the others are still encoding
-    // (they no longer read it).
-    constexpr unsigned long long kNone = ~0ull;
-#pragma unroll
-    for (int r = 0; r < kEncPasses; ++r) {
-        const int v = vec_of(r);
-        unsigned long long pos = kNone;
-        if (v < nvec) {
-            const int bh = v / p.t_new;
-            const int t = v - bh * p.t_new;
-            const int L = p.lengths[bh / p.hkv];
-            if (L < 0 || L + p.t_new > p.cap) {
-                if (q == 0 && !is_v && t == 0 && (bh % p.hkv) == 0) atomicOr(p.status, kStatusCapacity);
-            } else {
-                pos = static_cast<unsigned long long>(bh) * p.cap + L + t;
-            }
+    // the producer lane: stage s takes tile t (first tiles: blockIdx.x and
+    // blockIdx.x + gridDim.x; then from the counter, which counts from
+    // 2 gridDim.x) or, past the last tile, the end marker; false at the end
+    auto take_tile = [&](int s, bool first) -> bool {
+        const int t = first ? static_cast<int>(blockIdx.x) + s * static_cast<int>(gridDim.x)
+                            : static_cast<int>(atomicAdd(p.tiles_next, 1u)) + 2 * static_cast<int>(gridDim.x);
+        const uint32_t bar = bar_full + 8 * s;
+        if (t >= tiles) {
+            s_tile[s] = -1;
+            mbar_arrive(bar);
+            return false;
         }
-        s_pos[r][threadIdx.x] = pos;
+        s_tile[s] = t;
+        const bool is_v = t >= tiles_k;
+        const int row0 = (is_v ? t - tiles_k : t) * kTcVecs;
+        const uint32_t dst = smem_u32(smem + kTcXOff + s * 32768);
+        mbar_arrive_expect_tx(bar, 32768);
+        tma_g2s_2d(dst, is_v ? &vmap : &kmap, 0, row0, bar);
+        tma_g2s_2d(dst + 16384, is_v ? &vmap : &kmap, 64, row0, bar);
+        return true;
+    };
+    const bool producer = tid == 32 * kTcEncWarps;
+    int k_tma[2] = {0, 0};     // tiles (and end markers) put into each stage (the producer lane)
+    bool live[2] = {false, false};
+
+    // prologue (nothing here reads what earlier work on the stream writes):
+    // it may overlap the tail of the previous kernel
+    griddep_launch_dependents();
+    if (producer) {
+        for (int i = 0; i < 4; ++i) mbar_init(bar_full + 8 * i, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar_xfree + 8 * i, kTcEncWarps / 2);
+        fence_barrier_init();
+        griddep_wait();   // inputs, lengths and the tile counter come from earlier work on the stream
+        for (int s = 0; s < 2; ++s) {   // the first copies fly while B is built
+            live[s] = take_tile(s, true);
+            k_tma[s] = 1;
+        }
     }
-    finish_append(p, lane);
+    if (warp == kTcEncWarps) tmem_alloc(smem_u32(tslot), 256);
+    if (tid < 256) build_rotation_b(sB, p.signs, tid);
+    fence_proxy_async();   // B's generic stores, seen by the tensor core
+    griddep_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
 
-    uint32_t hm[16];
-    sign_masks(p.signs[q], hm);
-
-    // pass r's vector for this lane, whether it exists, and where it goes
-    struct Slot {
-        const __half* src;
-        size_t pos;
-        bool valid;
-    };
-    const __half* const in_base = is_v ? p.v_new : p.k_new;
-    auto slot = [&](int pass) {
-        Slot sl;
-        const unsigned long long pos = s_pos[pass][threadIdx.x];
-        sl.valid = pos != kNone;
-        sl.pos = sl.valid ? static_cast<size_t>(pos) : 0;
-        sl.src = in_base + static_cast<size_t>(sl.valid ? vec_of(pass) : 0) * kD;
-        return sl;
-    };
-    // the stream this CTA encodes (one code path serves both when K and V have
-    // the same bits)
-    uint8_t* const codes = is_v ? p.v_codes : p.k_codes;
-    __half* const norms = is_v ? p.v_norm : p.k_norm;
-    const float* const tcb = p.table ? (is_v ? p.v_cb : p.k_cb) : nullptr;
-    const float* const gt = is_v ? p.v_gt : p.k_gt;
-    const int rec = is_v ? (p.table ? 64 : VB * 16) : (KB == 0 ? 256 : (p.table ? 64 : KB * 16));
-
-    // the next pass's inputs are loaded before this pass is encoded
-    Slot cur = slot(0);
-    QuarterIn in = load_quarter_in(cur.src, q, cur.valid);
-#pragma unroll 1
-    for (int pass = 0; pass < kEncPasses; ++pass) {
-        Slot nxt = cur;
-        QuarterIn in_next = in;
-        if (pass + 1 < kEncPasses) {
-            nxt = slot(pass + 1);
-            in_next = load_quarter_in(nxt.src, q, nxt.valid);
-        }
-        uint8_t* const dst = codes + cur.pos * rec;
-        if constexpr (KB == VB) {
-            encode_group<KB>(in, cur.src, dst, norms + cur.pos, tcb, hm, gt, cur.valid, p.status, q,
-                             gmask);
-        } else if (!is_v) {
-            if constexpr (KB == 0) {
-                if (cur.valid) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + q * 64);
+    if (warp == kTcEncWarps) {
+        // ---- producer: for each stage, the MMA of its tile once the copy has
+        // landed and the group has read the accumulator, then the stage's next
+        // tile once the group has released the stage ----
+        if (producer) {
+            bool stalled = false;
+            int k_mma[2] = {0, 0};
+            uint64_t t_last = global_timer_ns();
+            for (uint32_t spin = 0; live[0] || live[1]; ++spin) {
+                bool progress = false;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) d4[i] = in.w[i];
+                for (int s = 0; s < 2; ++s) {
+                    if (!live[s]) continue;
+                    const int k = k_mma[s];
+                    if (k < k_tma[s] && mbar_test_wait(bar_full + 8 * s, k & 1) &&
+                        (k == 0 || mbar_test_wait(bar_afree + 8 * s, (k - 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t xa = smem_u32(smem + kTcXOff + s * 32768);
+                        const uint32_t ba = smem_u32(sB);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                            umma_f16(tmem + 128 * s, umma_desc_sw128(xa + koff), umma_desc_sw128(ba + koff),
+                                     kTcIdesc, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(bar_done + 8 * s);
+                        k_mma[s] = k + 1;
+                        progress = true;
+                    }
+                    if (k_mma[s] == k_tma[s] && mbar_test_wait(bar_xfree + 8 * s, (k_tma[s] - 1) & 1)) {
+                        live[s] = take_tile(s, false);
+                        ++k_tma[s];
+                        progress = true;
+                    }
                 }
-            } else {
-                encode_group<KB>(in, cur.src, dst, norms + cur.pos, tcb, hm, gt, cur.valid,
-                                 p.status, q, gmask);
+                if (progress) {
+                    t_last = global_timer_ns();
+                } else {
+                    __nanosleep(32);
+                    if ((spin & 63u) == 0 && global_timer_ns() - t_last > 2000000000ull) {
+                        stalled = true;
+                        break;
+                    }
+                }
             }
-        } else {
-            encode_group<VB>(in, cur.src, dst, norms + cur.pos, tcb, hm, gt, cur.valid, p.status,
-                             q, gmask);
+            if (stalled) {
+                atomicOr(p.status, kStatusPipelineStall);
+                // let the copies and MMAs still in flight land before the shared
+                // memory and tensor memory go away
+                for (int s = 0; s < 2; ++s) {
+                    if (live[s] && k_mma[s] < k_tma[s])
+                        (void)mbar_wait_bounded(bar_full + 8 * s, (k_tma[s] - 1) & 1);
+                    if (k_mma[s] > 0) (void)mbar_wait_bounded(bar_done + 8 * s, (k_mma[s] - 1) & 1);
+                }
+            }
         }
-        cur = nxt;
-        in = in_next;
+    } else {
+        // ---- encode warps ----
+        const int g = warp >> 2, lq = warp & 3;
+        const int r = 32 * lq + lane;   // the vector (row) of each tile
+        if constexpr (KB == 0) {   // fp16 K rows: copied, 16 bytes per thread
+            const long long n16 = static_cast<long long>(nvec) * 16;
+            for (long long i = static_cast<long long>(blockIdx.x) * (32 * kTcEncWarps) + tid; i < n16;
+                 i += static_cast<long long>(gridDim.x) * (32 * kTcEncWarps)) {
+                const int v = static_cast<int>(i >> 4);
+                const int bh = static_cast<int>((static_cast<uint64_t>(v) * p.div_t_m) >> p.div_t_s);
+                const int t = v - bh * p.t_new;
+                const int b = static_cast<int>((static_cast<uint64_t>(bh) * p.div_h_m) >> p.div_h_s);
+                const int L = p.lengths[b];
+                if (L < 0 || L + p.t_new > p.cap) {
+                    if ((i & 15) == 0 && t == 0 && bh == b * p.hkv) atomicOr(p.status, kStatusCapacity);
+                    continue;
+                }
+                const size_t pos = static_cast<size_t>(bh) * p.cap + L + t;
+                reinterpret_cast<uint4*>(p.k_codes + pos * 256)[i & 15] = reinterpret_cast<const uint4*>(p.k_new)[i];
+            }
+        }
+        const uint8_t* xs = smem + kTcXOff + g * 32768;
+        const uint32_t tacc = tmem + 128 * g + (static_cast<uint32_t>(lq * 32) << 16);
+        bool stalled = false;
+        for (int k = 0;; ++k) {
+            const uint32_t ph = k & 1;
+            if (!mbar_wait_bounded(bar_full + 8 * g, ph)) stalled = true;
+            if (__any_sync(0xffffffffu, stalled)) break;
+            const int t = s_tile[g];
+            if (t < 0) break;
+            const bool is_v = t >= tiles_k;
+            const int v = (is_v ? t - tiles_k : t) * kTcVecs + r;
+            // where this thread's vector goes: lengths[] is read now and
+            // looked at only after the norm
+            const bool in_range = v < nvec;
+            const int bh = static_cast<int>((static_cast<uint64_t>(in_range ? v : 0) * p.div_t_m) >> p.div_t_s);
+            const int tt = (in_range ? v : 0) - bh * p.t_new;
+            const int b = static_cast<int>((static_cast<uint64_t>(bh) * p.div_h_m) >> p.div_h_s);
+            const int L = p.lengths[b];
+            // norm: the exact squares of the fp16 inputs summed in fp32 by 8
+            // accumulators of 16 terms each, then pairwise: each square goes
+            // through at most 15 + 3 = 18 roundings; certified or redone exactly
+            float S32;
+            {
+                float acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(xs + (c >> 3) * 16384 + r * 128 +
+                                                                    ((((c & 7) ^ (r & 7))) << 4));
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float& a = acc[4 * (c & 1) + e];
+                        a = fma_sq_f16(static_cast<unsigned short>(ww[e]), a);
+                        a = fma_sq_f16(static_cast<unsigned short>(ww[e] >> 16), a);
+                    }
+                }
+                S32 = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            }
+            bool ok;
+            unsigned short nb = norm_candidate<19>(S32, ok);
+            // (rows without a vector are zero and always certain)
+            unsigned need = __ballot_sync(0xffffffffu, !ok);
+            while (need) {
+                const int src = __ffs(need) - 1;
+                need &= need - 1;
+                const unsigned short e = norm_exact_row(xs, 32 * lq + src, lane);
+                if (lane == src) nb = e;
+            }
+
+            bool valid = in_range;
+            size_t pos = 0;
+            if (valid) {
+                if (L < 0 || L + p.t_new > p.cap) {
+                    if (!is_v && tt == 0 && bh == b * p.hkv) atomicOr(p.status, kStatusCapacity);
+                    valid = false;
+                } else {
+                    pos = static_cast<size_t>(bh) * p.cap + L + tt;
+                }
+            }
+            uint8_t* const codes = is_v ? p.v_codes : p.k_codes;
+            __half* const norms = is_v ? p.v_norm : p.k_norm;
+            const float* const tcb = p.table ? (is_v ? p.v_cb : p.k_cb) : nullptr;
+            const int bits = is_v ? VB : KB;
+            uint8_t* const dst = codes + pos * (p.table ? 64 : bits * 16);
+            if (valid) {
+                store_norm(norms + pos, dst, tcb, nb);
+                if (nb >= 0x7C00u) atomicOr(p.status, kStatusNormOverflow);
+            }
+
+            if (!mbar_wait_bounded(bar_done + 8 * g, ph)) stalled = true;
+            if (__any_sync(0xffffffffu, stalled)) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_xfree + 8 * g);   // X read here and by the MMA
+            tc_fence_after();
+            const float scale = sqrtf(S32) * 11.313708498984761f;   // sqrt(128) n
+            auto encode_vec = [&](auto bits_tag) {
+                constexpr int BITS = decltype(bits_tag)::value;
+                constexpr int NT = (1 << (BITS - 1)) - 1;
+                float T[NT];   // (constant indices: read from the constant bank)
+                if (is_v) {
+#pragma unroll
+                    for (int i = 0; i < NT; ++i) T[i] = p.v_gt[i] * scale;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NT; ++i) T[i] = p.k_gt[i] * scale;
+                }
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {   // quarters 2h, 2h+1 (bytes 8 h BITS ..)
+                    uint32_t w[2 * BITS];
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32_issue(tacc + 64 * h, ra);
+                    tmem_ld32_issue(tacc + 64 * h + 32, rb);
+                    tmem_ld_wait(ra, rb);
+                    pack_quarter<BITS>(ra, T, w);
+                    pack_quarter<BITS>(rb, T, w + BITS);
+                    if (valid) {
+                        uint8_t* d = dst + h * 8 * BITS;
+                        if constexpr (BITS == 4) {
+                            reinterpret_cast<uint4*>(d)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                            reinterpret_cast<uint4*>(d)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        } else if (h == 0) {   // bytes 0..23: 16 + 8
+                            reinterpret_cast<uint4*>(d)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                            reinterpret_cast<uint2*>(d)[2] = make_uint2(w[4], w[5]);
+                        } else {               // bytes 24..47: 8 + 16
+                            reinterpret_cast<uint2*>(d)[0] = make_uint2(w[0], w[1]);
+                            reinterpret_cast<uint4*>(d + 8)[0] = make_uint4(w[2], w[3], w[4], w[5]);
+                        }
+                    }
+                }
+            };
+            if constexpr (KB == VB || KB == 0) {
+                encode_vec(std::integral_constant<int, VB>{});
+            } else {
+                if (is_v) encode_vec(std::integral_constant<int, VB>{});
+                else encode_vec(std::integral_constant<int, KB>{});
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_afree + 8 * g);
+        }
+        if (stalled && lane == 0) atomicOr(p.status, kStatusPipelineStall);
     }
+    finish_append(p, lane);   // every thread has read lengths[] for the last time, no more tiles taken
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTcEncWarps) tmem_dealloc(tmem, 256);
 }
 
 // Small appends (a few tokens per sequence): one warp per vector, lane l holds
 // dims 4l .. 4l+3, so every vector gets its own warp and the dependent chain
-// per lane is short.  The same output as encode_group, except that elements
-// within ~1e-7 of a midpoint may round the other way: here u itself is formed
-// and compared exactly against the fp32 midpoints.
+// per lane is short.  Here u itself is formed and compared exactly against the
+// fp32 midpoints (the large-append kernel compares the unnormalised value with
+// scaled thresholds: elements within ~1e-6 of a midpoint may round the other
+// way there).
 template <int BITS>
 __device__ __forceinline__ void encode_vector_warp(const __half* src, uint8_t* dst,
                                                    __half* dst_norm, const float* tcb,
@@ -522,7 +685,7 @@ __device__ __forceinline__ void encode_vector_warp(const __half* src, uint8_t* d
     for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
     const float S32 = __shfl_sync(0xffffffffu, ss, 0);
     bool ok;
-    unsigned short nb = norm_candidate(S32, ok);
+    unsigned short nb = norm_candidate<20>(S32, ok);   // at most 2 + 5 roundings per square
     if (!__all_sync(0xffffffffu, ok)) {
         // exact sum of squares (units of 2^-48) as a 128-bit integer
         U128 S = sq_u128(fp16_scaled_int(x[0]));
@@ -638,9 +801,28 @@ __global__ void __launch_bounds__(128) tq_encode_small_kernel(const __grid_const
     finish_append(p, lane);
 }
 
-int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stream) {
+
+template <int KB, int VB>
+static int launch_encode_tc(const EncodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                            dim3 grid, cudaStream_t stream) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(tq_encode_tc_kernel<KB, VB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemAlloc);
+        if (e == cudaSuccess)   // two CTAs' shared memory: the largest carveout
+            e = cudaFuncSetAttribute(tq_encode_tc_kernel<KB, VB>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     100);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    return launch_pdl(tq_encode_tc_kernel<KB, VB>, grid, dim3(kTcThreads), kTcSmemAlloc, stream, p, *kmap,
+                      *vmap);
+}
+
+int launch_encode(int kbits, int vbits, const EncodeParams& p, const CUtensorMap* kmap,
+                  const CUtensorMap* vmap, cudaStream_t stream) {
     const long long nvec = 1ll * p.batch * p.hkv * p.t_new;
-    if (nvec <= 4096) {   // a warp per vector: short chains for small appends
+    if (nvec <= kEncodeSmallMax) {   // a warp per vector: short chains for small appends
         const dim3 grid(static_cast<unsigned int>((2 * nvec + 3) / 4)), block(128);
         if (kbits == 16 && vbits == 4) return launch_pdl(tq_encode_small_kernel<0, 4>, grid, block, 0, stream, p);
         if (kbits == 3 && vbits == 3) return launch_pdl(tq_encode_small_kernel<3, 3>, grid, block, 0, stream, p);
@@ -649,13 +831,14 @@ int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stre
         if (kbits == 4 && vbits == 3) return launch_pdl(tq_encode_small_kernel<4, 3>, grid, block, 0, stream, p);
         return cudaErrorInvalidValue;
     }
-    const int kblocks = static_cast<int>((nvec + kEncVecs - 1) / kEncVecs);
-    const dim3 grid(static_cast<unsigned int>(2 * kblocks)), block(32 * kEncWarps);
-    if (kbits == 16 && vbits == 4) return launch_pdl(tq_encode_kernel<0, 4>, grid, block, 0, stream, p, kblocks);
-    if (kbits == 3 && vbits == 3) return launch_pdl(tq_encode_kernel<3, 3>, grid, block, 0, stream, p, kblocks);
-    if (kbits == 4 && vbits == 4) return launch_pdl(tq_encode_kernel<4, 4>, grid, block, 0, stream, p, kblocks);
-    if (kbits == 16 && vbits == 3) return launch_pdl(tq_encode_kernel<0, 3>, grid, block, 0, stream, p, kblocks);
-    if (kbits == 4 && vbits == 3) return launch_pdl(tq_encode_kernel<4, 3>, grid, block, 0, stream, p, kblocks);
+    if (kmap == nullptr || vmap == nullptr) return cudaErrorInvalidValue;
+    const long long tiles = (kbits == 16 ? 1 : 2) * ((nvec + kTcVecs - 1) / kTcVecs);
+    const dim3 grid(static_cast<unsigned int>(std::min<long long>(tiles, 152ll * kTcCtasPerSm)));
+    if (kbits == 16 && vbits == 4) return launch_encode_tc<0, 4>(p, kmap, vmap, grid, stream);
+    if (kbits == 3 && vbits == 3) return launch_encode_tc<3, 3>(p, kmap, vmap, grid, stream);
+    if (kbits == 4 && vbits == 4) return launch_encode_tc<4, 4>(p, kmap, vmap, grid, stream);
+    if (kbits == 16 && vbits == 3) return launch_encode_tc<0, 3>(p, kmap, vmap, grid, stream);
+    if (kbits == 4 && vbits == 3) return launch_encode_tc<4, 3>(p, kmap, vmap, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -63,7 +63,11 @@ struct EncodeParams {
     int32_t* lengths;
     uint32_t* status;
     uint32_t* counter;        // zero between calls; the last CTA resets it
+    uint32_t* tiles_next;     // large appends: the next tile to hand out (zero between calls, reset likewise)
     int32_t batch, hkv, t_new, cap;
+    // n / t_new and n / hkv for 0 <= n < 2^31 as (n * m) >> s (see div_magic)
+    uint32_t div_t_m, div_h_m;
+    int32_t div_t_s, div_h_s;
     uint32_t signs[4];
     // decision thresholds on |u| over the positive half of the codebook:
     // a > tau_k  <=>  a >= gt[k];   a >= tau_k  <=>  a >= ge[k]   (fp32, exact)
@@ -91,12 +95,28 @@ struct PrefillParams {
     uint32_t ktab[4], vtab[4], signs[4];
 };
 
+// Division of 0 <= n < 2^31 by a constant d >= 1 as a multiply-high: with
+// l = ceil(log2 d), s = 31 + l and m = ceil(2^s / d) (below 2^32),
+// floor(n m / 2^s) = floor(n / d), because m d - 2^s < d <= 2^l and
+// n < 2^31 keep the error term n (m d - 2^s) / (d 2^s) below 1/d.
+inline void div_magic(uint32_t d, uint32_t* m, int32_t* s) {
+    int l = 0;
+    while ((1ull << l) < d) ++l;
+    *s = 31 + l;
+    *m = static_cast<uint32_t>(((1ull << *s) + d - 1) / d);
+}
+
 // Launchers (return a cudaError_t value).
 // group_rows (p.group_rows) selects the 4-, 8- or 16-row variant.
 int launch_decode(int kbits, int vbits, const DecodeParams& p, const CUtensorMap* kmap,
                   cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end);
 int launch_combine(const CombineParams& p, cudaStream_t stream);
-int launch_encode(int kbits, int vbits, const EncodeParams& p, cudaStream_t stream);
+// Appends of more than kEncodeSmallMax vectors per stream run on the tensor
+// cores and read their inputs through kmap / vmap (encode_rows_map of k_new /
+// v_new); smaller ones ignore the maps.
+constexpr long long kEncodeSmallMax = 4096;
+int launch_encode(int kbits, int vbits, const EncodeParams& p, const CUtensorMap* kmap,
+                  const CUtensorMap* vmap, cudaStream_t stream);
 
 // Resident CTAs per SM of a decode variant (for the host split planner);
 // res: the variant with the centroid residual product.
@@ -175,6 +195,9 @@ int build_tables(const float* cb, int n, int bits, CodebookTables* t);
 void make_signs(uint64_t seed, uint32_t out[4]);
 // Tensor map of the fp16 K rows of a cache (driver entry point looked up once).
 int encode_kmap(CUtensorMap* map, const tq_cache* c);
+// Tensor map of `rows` fp16 vectors of 128 dims at `base` (16-byte aligned),
+// boxes of 128 rows x 64 halves (128-byte swizzle): the encode's input tiles.
+int encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows);
 // Whether every entry of a codebook is an fp16 value (no rounding residual).
 bool codebook_is_fp16(const float* cb, int n);
 
