@@ -104,22 +104,24 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
         }
         const int left = n - i0 - warp;                 // partials i0 + warp + 4k, k < nb
         const int nb = left > 0 ? min(32, (left + 3) / 4) : 0;
-        for (int k0 = 0; k0 < nb; k0 += 8) {
-            float wk[8];
-            float4 o[8];
+        for (int k0 = 0; k0 < nb; k0 += 16) {
+            // the O loads of used partials do not wait for the weights: they
+            // fly together with the (m, l) loads above
+            float4 o[16];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                wk[k] = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
-                o[k] = (k0 + k < nb && wk[k] != 0.f)
+            for (int k = 0; k < 16; ++k)
+                o[k] = (k0 + k < nb && used(i0 + warp + 4 * (k0 + k)))
                            ? __ldcg(reinterpret_cast<const float4*>(
                                         p.part_o + (row0 + 16 * static_cast<size_t>(i0 + warp + 4 * (k0 + k))) * kD) +
                                     lane)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                acc.x += wk[k] * o[k].x; acc.y += wk[k] * o[k].y;
-                acc.z += wk[k] * o[k].z; acc.w += wk[k] * o[k].w;
+            for (int k = 0; k < 16; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
+                if (wk != 0.f) {   // (a partial whose rows saw no token adds nothing, whatever its O)
+                    acc.x += wk * o[k].x; acc.y += wk * o[k].y;
+                    acc.z += wk * o[k].z; acc.w += wk * o[k].w;
+                }
             }
         }
     }
