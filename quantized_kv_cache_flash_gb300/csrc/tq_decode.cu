@@ -96,27 +96,28 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int i0 = 0; i0 < n; i0 += 128) {
         const int i = i0 + i_first;
+        const unsigned used_mask = __ballot_sync(0xffffffffu, used(i));   // bit k: partial i0 + warp + 4k
         float w = 0.f;
-        const float2 ml = (i0 == 0) ? ml_first : (used(i) ? load_ml(i) : make_float2(-INFINITY, 0.f));
+        const float2 ml = (i0 == 0) ? ml_first : (((used_mask >> lane) & 1u) ? load_ml(i) : make_float2(-INFINITY, 0.f));
         if (ml.x != -INFINITY) {
             w = fast_exp2(ml.x - M);
             den += w * ml.y;
         }
         const int left = n - i0 - warp;                 // partials i0 + warp + 4k, k < nb
         const int nb = left > 0 ? min(32, (left + 3) / 4) : 0;
-        for (int k0 = 0; k0 < nb; k0 += 16) {
+        for (int k0 = 0; k0 < nb; k0 += 8) {
             // the O loads of used partials do not wait for the weights: they
             // fly together with the (m, l) loads above
-            float4 o[16];
+            float4 o[8];
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-                o[k] = (k0 + k < nb && used(i0 + warp + 4 * (k0 + k)))
+            for (int k = 0; k < 8; ++k)
+                o[k] = (k0 + k < nb && ((used_mask >> (k0 + k)) & 1u))
                            ? __ldcg(reinterpret_cast<const float4*>(
                                         p.part_o + (row0 + 16 * static_cast<size_t>(i0 + warp + 4 * (k0 + k))) * kD) +
                                     lane)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
+            for (int k = 0; k < 8; ++k) {
                 const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
                 if (wk != 0.f) {   // (a partial whose rows saw no token adds nothing, whatever its O)
                     acc.x += wk * o[k].x; acc.y += wk * o[k].y;
