@@ -787,8 +787,7 @@ def workload(args) -> wl.Workload:
     return w
 
 
-TRAFFIC_SOURCES = ["quantized_kv_cache_flash_gb300/csrc/tq_decode.cu",
-                   "quantized_kv_cache_flash_gb300/csrc/tq_decode_kernel.cuh",
+TRAFFIC_SOURCES = ["quantized_kv_cache_flash_gb300/csrc/tq_decode_kernel.cuh",
                    "quantized_kv_cache_flash_gb300/csrc/tq_decode_q.cu",
                    "quantized_kv_cache_flash_gb300/csrc/tq_device.cuh",
                    "quantized_kv_cache_flash_gb300/csrc/tq_internal.h"]
