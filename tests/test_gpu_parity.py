@@ -256,8 +256,8 @@ def _crafted_vectors():
 
 
 # T = 300 runs the warp-per-vector kernel (small appends), T = 700 and 1029
-# the four-lanes-per-vector kernel (more than 4096 vectors per stream; 1029
-# leaves a ragged last CTA of vectors)
+# the tensor-core kernel (more than 4096 vectors per stream; 1029 leaves a
+# ragged last tile of vectors)
 @pytest.mark.parametrize("T", [300, 700, 1029])
 @pytest.mark.parametrize("mode", ["turbo3", "turbo4", "turbo4_asym", "turbo3_asym", "turbo4k_3v",
                                   "turbo3_table"])
@@ -323,6 +323,34 @@ def test_encode_capacity_overflow_is_flagged_and_skipped():
     assert tqf.tq_get_status(ctx) == tqf.TQ_STATUS_CAPACITY
     assert cache.lengths.cpu().tolist() == [10, 10]
     assert not cache.k_data[0].any().item()              # sequence 0 untouched
+
+
+@pytest.mark.parametrize("mode", ["turbo3", "turbo4_asym", "turbo4k_3v"])
+def test_encode_large_append_capacity_overflow(mode):
+    """The tensor-core encode (4800 vectors per stream): the sequence that
+    would overflow is flagged and left untouched, the other is encoded."""
+    kb, vb = H.MODE_BITS[mode]
+    B, Hkv, T, cap = 2, 8, 300, 400
+    ctx = tqf.Context()
+    cache = tqf.Cache(tqf.MODES[mode], B, Hkv, cap, DEV)
+    cache.lengths.copy_(torch.tensor([10, 200], dtype=torch.int32))
+    k = wl.random_fp16(21, (B, Hkv, T, 128))
+    v = wl.random_fp16(22, (B, Hkv, T, 128))
+    tqf.tq_encode_append(ctx, cache, H.upload(k, DEV), H.upload(v, DEV))
+    torch.cuda.synchronize()
+    assert tqf.tq_get_status(ctx) == tqf.TQ_STATUS_CAPACITY
+    assert cache.lengths.cpu().tolist() == [10 + T, 200]
+    assert not cache.v_data[1].any().item()              # sequence 1 untouched
+    assert not cache.k_data[1].any().item()
+    # sequence 0: the oracle's codes (but the boundary band)
+    s = o.sign_vector(42)
+    got = H.decode_records(cache.v_data[0, :, 10:10 + T].cpu().numpy(), vb)
+    idx, n16, u, _ = o.encode(v[0], o.codebook(vb), s)
+    diff = got != idx
+    assert np.all(o.boundary_distance(u[diff], o.codebook(vb)) < H.BOUNDARY)
+    assert np.array_equal(cache.v_norm[0, :, 10:10 + T].cpu().numpy().view(np.uint16), n16.view(np.uint16))
+    if kb == 16:
+        assert np.array_equal(cache.k_data[0, :, 10:10 + T].cpu().numpy().view(np.float16), k[0])
 
 
 # ---------------------------------------------------------------------------
