@@ -297,6 +297,7 @@ class OraclePool:
     def sample(self, wnum, budget_s, seed0, mode=None):
         jobs = [(wnum, budget_s, seed0 + 7919 * i, mode) for i in range(self.n)]
         res = self.pool.map(_oracle_worker, jobs)
+        self.last_rates = [r[0] / r[1] for r in res if r[1] > 0]   # each single-threaded process
         return (sum(r[0] for r in res), max(r[1] for r in res), sum(r[2] for r in res), res[0][3])
 
     def close(self):
@@ -311,10 +312,13 @@ def run_cpu_baseline(wnum: int, budget_s: float, mode=None):
     finally:
         pool.close()
     prompt = wl.by_number(wnum).prompt
-    return {"value": b / s / (1e12 if prompt else 1e9), "unit": "TFLOP/s" if prompt else "GB/s",
+    scale = 1e12 if prompt else 1e9
+    return {"value": b / s / scale, "unit": "TFLOP/s" if prompt else "GB/s",
             "cores": pool.n, "kind": "oracle",
             "sample": f"{pool.n} single-threaded processes x ({desc}); {u} units in all",
-            "seconds": round(s, 2)}
+            "seconds": round(s, 2),
+            # one core alone (the median single-threaded process)
+            "per_core_value": statistics.median(pool.last_rates) / scale if pool.last_rates else None}
 
 
 # ---------------------------------------------------------------------------
