@@ -31,7 +31,10 @@
  *     never frees them.  The library owns only the context (workspace, status
  *     word, cached tables), created lazily when *ctx == NULL and released by
  *     tq_free.  A context is bound to the device that was current when it was
- *     created.
+ *     created.  Its workspace and counters serve one call at a time: calls on
+ *     one context that could overlap on the GPU (different streams without an
+ *     ordering between them) must be ordered by the caller or use separate
+ *     contexts.
  *   - Conditions only the GPU can see (a sequence whose append passes the
  *     capacity, a norm that overflows fp16, a sequence shorter than the query
  *     block, a pipeline wait that timed out) never trap: the kernels OR a bit
@@ -138,6 +141,10 @@ typedef struct {
  *   Token j of sequence b is written at position lengths[b] + j; afterwards
  *   lengths[b] += t_new.  A sequence with lengths[b] + t_new > capacity is left
  *   untouched and TQ_STATUS_CAPACITY is raised.  t_new == 0 is a no-op.
+ *   More than 4096 vectors per stream (batch * num_kv_heads * t_new) take the
+ *   tensor-core encode, which reads k_new / v_new through tensor maps built
+ *   on the host in this call; fewer take a warp per vector.  Both give the
+ *   same records except for elements within ~1e-6 of a decision midpoint.
  */
 int tq_encode_append(tq_ctx **ctx, const tq_cache *cache, const void *k_new,
                      const void *v_new, int32_t t_new, void *stream);
