@@ -934,16 +934,12 @@ template <int KB, int VB, int ROWS, bool TAB, bool RES>
 int launch_decode_t(const DecodeParams& p, const CUtensorMap* kmap, cudaStream_t stream,
                     cudaEvent_t ev0, cudaEvent_t ev1) {
     using C = DecCfg<KB, VB, ROWS, TAB, RES>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tq_decode_kernel<KB, VB, ROWS, TAB, RES>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    cudaError_t e = set_smem_attr_once(tq_decode_kernel<KB, VB, ROWS, TAB, RES>, C::kSmemAlloc, attr_done);
+    if (e != cudaSuccess) return e;
     dim3 grid(p.num_ctas);
     if (ev0) cudaEventRecord(ev0, stream);
-    cudaError_t e = launch_pdl(tq_decode_kernel<KB, VB, ROWS, TAB, RES>, grid, dim3(C::kWarps * 32),
+    e = launch_pdl(tq_decode_kernel<KB, VB, ROWS, TAB, RES>, grid, dim3(C::kWarps * 32),
                                C::kSmemAlloc, stream, p, *kmap);
     if (ev1) cudaEventRecord(ev1, stream);
     return e;

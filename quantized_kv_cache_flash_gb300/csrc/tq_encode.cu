@@ -805,16 +805,9 @@ __global__ void __launch_bounds__(128) tq_encode_small_kernel(const __grid_const
 template <int KB, int VB>
 static int launch_encode_tc(const EncodeParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
                             dim3 grid, cudaStream_t stream) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tq_encode_tc_kernel<KB, VB>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemAlloc);
-        if (e == cudaSuccess)   // two CTAs' shared memory: the largest carveout
-            e = cudaFuncSetAttribute(tq_encode_tc_kernel<KB, VB>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     100);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};   // two CTAs' shared memory: the largest carveout
+    const cudaError_t e = set_smem_attr_once(tq_encode_tc_kernel<KB, VB>, kTcSmemAlloc, attr_done, 100);
+    if (e != cudaSuccess) return e;
     return launch_pdl(tq_encode_tc_kernel<KB, VB>, grid, dim3(kTcThreads), kTcSmemAlloc, stream, p, *kmap,
                       *vmap);
 }

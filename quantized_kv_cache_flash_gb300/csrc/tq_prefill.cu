@@ -478,13 +478,9 @@ __global__ void __launch_bounds__(256, 1)
 template <int KB, int VB>
 static int launch_prefill_t(const PrefillParams& p, const CUtensorMap* kmap, cudaStream_t stream) {
     using C = PreCfg<KB, VB>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tq_prefill_kernel<KB, VB>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    const cudaError_t e = set_smem_attr_once(tq_prefill_kernel<KB, VB>, C::kSmemAlloc, attr_done);
+    if (e != cudaSuccess) return e;
     return launch_pdl(tq_prefill_kernel<KB, VB>, dim3((p.mtiles + 1) / 2, p.batch * p.hkv), dim3(256),
                       C::kSmemAlloc, stream, p, *kmap);
 }
