@@ -35,6 +35,12 @@
  *     one context that could overlap on the GPU (different streams without an
  *     ordering between them) must be ordered by the caller or use separate
  *     contexts.
+ *   - CUDA graphs: after one eager call on a context (which sizes its
+ *     workspace), tq_encode_append and tq_decode_attention can be captured
+ *     and replayed; device-side counters and the status word reset
+ *     themselves, tensor maps are built at capture, and the decode grid is
+ *     fixed by the max_len_hint given at capture (it must cover the lengths
+ *     every replay sees).
  *   - Conditions only the GPU can see (a sequence whose append passes the
  *     capacity, a norm that overflows fp16, a sequence shorter than the query
  *     block, a pipeline wait that timed out) never trap: the kernels OR a bit
