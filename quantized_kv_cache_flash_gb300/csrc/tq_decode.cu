@@ -31,14 +31,15 @@ int decode_variant(bool launch, int kbits, int vbits, int group_rows, bool table
 // One CTA per output row (b, q head, query j): merge the partials of the
 // CTAs that covered the row's unit with their log-sum-exp weights, apply
 // v_rescale, leave the rotated basis (Rot^-1(y) = s * (H y) / sqrt(128)) and
-// store fp16.  The 4 warps split the partials (warp w takes i = w mod 4), so
-// a long unit's partials are read with four times the loads in flight: each
-// warp merges its share against its own max, lane l holding dims 4l..4l+3,
-// and warp 0 merges the four results.
-__global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__ CombineParams p) {
-    __shared__ float4 s_acc[4][32];
-    __shared__ float s_m[4], s_den[4];
-    griddep_wait();  // the decode kernel's partials
+// store fp16.  The W warps split the partials (warp w takes i = w mod W) in
+// rounds of 8 per warp: a round's (m, l) pairs and O rows are loaded
+// together, so a unit of up to 8W partials is one round trip to L2.  Each
+// warp merges its share against a running max (lane l holding dims
+// 4l..4l+3), and warp 0 merges the W results.
+template <int W>
+__global__ void __launch_bounds__(32 * W) tq_combine_kernel(const __grid_constant__ CombineParams p) {
+    __shared__ float4 s_acc[W][32];
+    __shared__ float s_m[W], s_den[W];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int row = blockIdx.x;
@@ -52,7 +53,10 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
     const int ui = kv * p.row_groups + rg;
     const int unit = b * per_b + ui;
 
-    // the unit's global chunk range [k_first, k_first + nch) and the CTAs over it
+    // The unit's global chunk range [k_first, k_first + nch) and the CTAs over
+    // it.  `lengths` may be read before the dependency wait: this grid follows
+    // the decode kernel, whose CTAs each waited for the work that wrote
+    // `lengths` before any of them let this grid launch.
     int before = 0, all = 0;
     for (int bb = lane; bb < p.batch; bb += 32) {
         const int v = unit_chunks(p.lengths, bb, p.max_len) * per_b;
@@ -79,50 +83,44 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
         return i < n && (!some_empty || c * cq + (c * cr) / P < (c + 1) * cq + ((c + 1) * cr) / P);
     };
     const size_t row0 = (static_cast<size_t>(c0) + unit) * 16 + rl;  // partial of CTA c0
-    auto load_ml = [&](int i) {
-        return __ldcg(reinterpret_cast<const float2*>(p.part_ml) + row0 + 16 * static_cast<size_t>(i));
-    };
+    griddep_wait();  // the decode kernel's partials
 
-    // this warp's partials: i = warp + 4k; lane l reads the (m, l) pair of k = l (+32 ...)
-    const int i_first = warp + 4 * lane;
-    const float2 ml_first = used(i_first) ? load_ml(i_first) : make_float2(-INFINITY, 0.f);
-    float M = ml_first.x;
-    for (int i = i_first + 128; i < n; i += 128)
-        if (used(i)) M = fmaxf(M, load_ml(i).x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-
-    float den = 0.f;
+    float M = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < n; i0 += 128) {
-        const int i = i0 + i_first;
-        const unsigned used_mask = __ballot_sync(0xffffffffu, used(i));   // bit k: partial i0 + warp + 4k
-        float w = 0.f;
-        const float2 ml = (i0 == 0) ? ml_first : (((used_mask >> lane) & 1u) ? load_ml(i) : make_float2(-INFINITY, 0.f));
-        if (ml.x != -INFINITY) {
-            w = fast_exp2(ml.x - M);
-            den += w * ml.y;
+    for (int i0 = warp; i0 < n; i0 += 8 * W) {
+        // this round: partials i0 + W k, k < 8; lane k < 8 holds partial k's (m, l)
+        const bool mine = lane < 8 && used(i0 + W * lane);
+        const unsigned used_mask = __ballot_sync(0xffffffffu, mine);  // bit k: partial i0 + W k
+        const float2 ml = mine ? __ldcg(reinterpret_cast<const float2*>(p.part_ml) + row0 +
+                                        16 * static_cast<size_t>(i0 + W * lane))
+                               : make_float2(-INFINITY, 0.f);
+        float4 o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            o[k] = ((used_mask >> k) & 1u)
+                       ? __ldcg(reinterpret_cast<const float4*>(
+                                    p.part_o + (row0 + 16 * static_cast<size_t>(i0 + W * k)) * kD) + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        float mr = ml.x;
+#pragma unroll
+        for (int o2 = 4; o2 > 0; o2 >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o2));
+        mr = __shfl_sync(0xffffffffu, mr, 0);
+        const float Mn = fmaxf(M, mr);
+        if (Mn == -INFINITY) continue;  // (warp-uniform) no partial of this round saw a token
+        if (M != Mn) {  // rescale what earlier rounds merged
+            const float sc = (M == -INFINITY) ? 0.f : fast_exp2(M - Mn);
+            acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+            den *= sc;
+            M = Mn;
         }
-        const int left = n - i0 - warp;                 // partials i0 + warp + 4k, k < nb
-        const int nb = left > 0 ? min(32, (left + 3) / 4) : 0;
-        for (int k0 = 0; k0 < nb; k0 += 8) {
-            // the O loads of used partials do not wait for the weights: they
-            // fly together with the (m, l) loads above
-            float4 o[8];
+        const float w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+        den += w * ml.y;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                o[k] = (k0 + k < nb && ((used_mask >> (k0 + k)) & 1u))
-                           ? __ldcg(reinterpret_cast<const float4*>(
-                                        p.part_o + (row0 + 16 * static_cast<size_t>(i0 + warp + 4 * (k0 + k))) * kD) +
-                                    lane)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
-                if (wk != 0.f) {   // (a partial whose rows saw no token adds nothing, whatever its O)
-                    acc.x += wk * o[k].x; acc.y += wk * o[k].y;
-                    acc.z += wk * o[k].z; acc.w += wk * o[k].w;
-                }
+        for (int k = 0; k < 8; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+            if (wk != 0.f) {   // (a partial whose rows saw no token adds nothing, whatever its O)
+                acc.x += wk * o[k].x; acc.y += wk * o[k].y;
+                acc.z += wk * o[k].z; acc.w += wk * o[k].w;
             }
         }
     }
@@ -138,11 +136,11 @@ __global__ void __launch_bounds__(128) tq_combine_kernel(const __grid_constant__
 
     float Mall = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) Mall = fmaxf(Mall, s_m[w]);
+    for (int w = 0; w < W; ++w) Mall = fmaxf(Mall, s_m[w]);
     float dsum = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < W; ++w) {
         const float sc = (s_m[w] == -INFINITY) ? 0.f : fast_exp2(s_m[w] - Mall);
         const float4 x = s_acc[w][lane];
         dsum += sc * s_den[w];
@@ -189,9 +187,13 @@ int launch_decode(int kbits, int vbits, const DecodeParams& p, const CUtensorMap
                           ev1);
 }
 
+// Eight warps where units average more than 16 partials (few units over many
+// CTAs), four otherwise.
 int launch_combine(const CombineParams& p, cudaStream_t stream) {
     const int rows = p.batch * p.hq * p.tq;
-    return launch_pdl(tq_combine_kernel, dim3(rows), dim3(128), 0, stream, p);
+    const long long units = 1ll * p.batch * p.hkv * p.row_groups;
+    if (p.num_ctas > 16 * units) return launch_pdl(tq_combine_kernel<8>, dim3(rows), dim3(256), 0, stream, p);
+    return launch_pdl(tq_combine_kernel<4>, dim3(rows), dim3(128), 0, stream, p);
 }
 
 int decode_ctas_per_sm(int kbits, int vbits, int group_rows, bool table, bool res) {

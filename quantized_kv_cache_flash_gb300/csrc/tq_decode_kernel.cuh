@@ -295,8 +295,23 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, ROWS, TAB, RES>::kMinCtas)
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    griddep_wait();  // lengths, cache and q come from earlier work on the stream
     const int per_b = p.hkv * p.row_groups;
+    const int P = static_cast<int>(gridDim.x);
+    const int c_me = static_cast<int>(blockIdx.x);
+
+    // ---- set-up that reads nothing earlier work on the stream writes: it
+    // overlaps the predecessor's tail under programmatic dependent launch ----
+    uint8_t* wpipe = smem + warp * C::kStages * C::kStage;
+    const uint32_t bar0 = smem_u32(smem + C::kBarOff) + warp * C::kStages * 8;
+    if (lane == 0) {
+        for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_barrier_init();
+    }
+    if constexpr (KB == 0)
+        if (threadIdx.x == 0) prefetch_tensormap(&kmap);
+    __syncwarp();
+
+    griddep_wait();  // lengths, cache and q come from earlier work on the stream
     BatchScan scan;
     scan.init(reinterpret_cast<int*>(smem + C::kScanOff) + warp * 128, p.lengths, p.batch, per_b,
               p.max_len, lane);
@@ -304,19 +319,10 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, ROWS, TAB, RES>::kMinCtas)
     // shuffle, which lets the compiler keep them in uniform registers)
     const int C_all = __shfl_sync(0xffffffffu, scan.total(p.lengths, p.batch, per_b, p.max_len, lane), 0);
     // floor(c * C_all / P) in 32-bit arithmetic: c * (C_all mod P) < P^2 < 2^31
-    const int P = static_cast<int>(gridDim.x), cq = C_all / P, cr = C_all - cq * P;
-    const int c_me = static_cast<int>(blockIdx.x);
+    const int cq = C_all / P, cr = C_all - cq * P;
     const int lo = c_me * cq + (c_me * cr) / P;
     const int hi = (c_me + 1) * cq + ((c_me + 1) * cr) / P;
     if (lo >= hi) return;  // no chunks for this CTA (uniform over the CTA)
-
-    uint8_t* wpipe = smem + warp * C::kStages * C::kStage;
-    const uint32_t bar0 = smem_u32(smem + C::kBarOff) + warp * C::kStages * 8;
-    if (lane == 0) {
-        for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
-        fence_barrier_init();
-    }
-    __syncwarp();
     __half* sQ = reinterpret_cast<__half*>(smem + C::kQOff);
     __half* sQlo = reinterpret_cast<__half*>(smem + C::kQloOff);
     uint8_t* sQ8 = smem + C::kQ8Off;

@@ -187,6 +187,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Fetch a tensor map (a __grid_constant__ kernel parameter) into the
+// descriptor cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(tmap) : "memory");
+}
+
 // 2-D tensor-map tile copy global -> shared.  x (innermost) in elements.
 __device__ __forceinline__ void tma_g2s_2d(uint32_t dst, const void* tmap, int32_t x,
                                            int32_t y, uint32_t bar) {
