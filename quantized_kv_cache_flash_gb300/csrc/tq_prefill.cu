@@ -23,10 +23,12 @@
 // thread = one query row (tensor-memory lane) of one tile, so each K/V tile is
 // dequantised once for 256 rows.  Tensor memory holds, per query tile, S (128
 // columns, whose first 64 take P back as fp16 pairs for the P.V MMA) and O
-// (128 columns): all 512.  The MMAs overlap the CUDA-core work: P.V(n-1)
-// runs while K(n) is dequantised, S(n) while V(n) is.  Packed records of the
-// next tiles stream into two staging slots by bulk copies (fp16 K by 2-D
-// tensor-map copies straight into the MMA layout); every wait is bounded.
+// (128 columns): all 512.  The MMAs overlap the CUDA-core work and the two
+// query tiles take turns on the tensor core: S(n) runs while V(n) is
+// dequantised, S_1(n) during tile 0's softmax, P.V_0(n) during tile 1's and
+// P.V_1(n) while K(n + 1) is dequantised.  Packed records of the next tiles
+// stream into two staging slots by bulk copies (fp16 K by 2-D tensor-map
+// copies straight into the MMA layout); every mbarrier wait is bounded.
 #include <float.h>
 
 #include "tq_device.cuh"
@@ -54,8 +56,10 @@ struct PreCfg {
     static constexpr int kSlotAlign = (KB == 0) ? 1024 : 128;
     static constexpr int kSlot = (kSlotRaw + kSlotAlign - 1) / kSlotAlign * kSlotAlign;
     static constexpr int kColOff = kStgOff + 2 * kSlot;         // fp32 n_k * scale * log2(e) [128]
-    static constexpr int kBarOff = kColOff + kTile * 4;         // stg[2], S, O mbarriers + TMEM slot
-    static constexpr int kSmem = kBarOff + 64;
+    // mbarriers stg[2], S[2], O[2] (one per query tile), V^T stored, K stored,
+    // tile 1's softmax done; TMEM slot; last tile copied
+    static constexpr int kBarOff = kColOff + kTile * 4;
+    static constexpr int kSmem = kBarOff + 80;
     static constexpr int kSmemAlloc = kSmem + 1024;             // base alignment slack
     static constexpr uint32_t kIdesc = umma_idesc_f16_f32(128, 128);
 };
@@ -129,12 +133,15 @@ __global__ void __launch_bounds__(256, 1)
 
     uint8_t* sQ = smem + C::kQOff;       // [2][128 x 128] fp16
     uint8_t* sVt = smem + C::kVtOff;
-    float* colK = reinterpret_cast<float*>(smem + C::kColOff);  // n_k * scale * log2(e) per token (quantized K)
+    // n_k * scale * log2(e) per token (quantized K), written with K's dequant
+    float* colK = reinterpret_cast<float*>(smem + C::kColOff);
     const uint32_t bar_stg = smem_u32(smem + C::kBarOff);       // 2 x 8 bytes
-    const uint32_t bar_s = bar_stg + 16, bar_o = bar_stg + 24;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 32);
+    const uint32_t bar_s = bar_stg + 16, bar_o = bar_stg + 32, bar_v = bar_stg + 48;
+    const uint32_t bar_kr = bar_stg + 56, bar_sm1 = bar_stg + 64;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + 72);
+    int* last_issued = reinterpret_cast<int*>(smem + C::kBarOff + 76);  // last tile whose copy was issued
 
-    auto issue = [&](int n) {  // thread 0: tile n into staging slot n & 1
+    auto issue = [&](int n) {  // one thread: tile n into staging slot n & 1
         const int tok0 = n * C::kTile;
         const int nval = min(C::kTile, t_lim - tok0);
         uint8_t* slot = smem + C::kStgOff + (n & 1) * C::kSlot;
@@ -160,9 +167,13 @@ __global__ void __launch_bounds__(256, 1)
     };
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(bar_stg + 8 * i, 1);
+        for (int i = 0; i < 6; ++i) mbar_init(bar_stg + 8 * i, 1);  // stg[2], S[2], O[2]
+        mbar_init(bar_v, 128);  // the V dequant's threads
+        mbar_init(bar_kr, 1);
+        mbar_init(bar_sm1, 1);
         fence_barrier_init();
         for (int n = 0; n < 2 && n < ntiles; ++n) issue(n);
+        *last_issued = min(ntiles, 2) - 1;
     }
     // tensor memory: tile t at columns 256 t: S (128, its first 64 reused for
     // P as fp16 pairs), then O (128)
@@ -214,6 +225,7 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
     }
+    fence_proxy_async();  // the MMAs read Q' through the async proxy
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -222,117 +234,117 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t t_s = tmem + 256 * tl + lane_off;         // this row of S (and of P)
     const uint32_t t_o = tmem + 256 * tl + 128 + lane_off;   // this row of O
 
-    const Tables kt{p.ktab[0], p.ktab[1], p.ktab[2], p.ktab[3]};
-    const Tables vt{p.vtab[0], p.vtab[1], p.vtab[2], p.vtab[3]};
     float m_base = -INFINITY, l_sum = 0.f;
-    bool stalled = false;
-    int issued_o = 0;  // P.V batches committed
+    bool stalled = false;  // once set, waits return at once and no MMA or copy is issued
+    int issued_o = 0;      // P.V batches of this thread's query tile
+    const uint32_t bar_st = bar_s + 8 * tl, bar_ot = bar_o + 8 * tl;
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!stalled && !mbar_wait_bounded(bar, parity)) stalled = true;
+    };
 
-    // Per tile n: K(n) dequant (overlaps P.V(n-1)); S(n) for both query tiles
-    // (overlaps the V(n) dequant); softmax(n) writes P into tensor memory over
-    // S; P.V(n).
-    for (int n = 0; n < ntiles && !stalled; ++n) {
+    // K(n) -> sK, one token per thread of query tile 0's warps (fp16 K: the
+    // tile is read in place from the staging slot)
+    auto k_dequant = [&](int n) {
+        if constexpr (KB != 0) {
+            // (tables from the parameters at each use: none held across the loop)
+            const Tables kt{p.ktab[0], p.ktab[1], p.ktab[2], p.ktab[3]};
+            const uint8_t* rec = smem + C::kStgOff + (n & 1) * C::kSlot + r * C::kRbK;
+            uint8_t* sK = smem + C::kKOff;
+#pragma unroll 1
+            for (int quarter = 0; quarter < 4; ++quarter) {
+                uint32_t hh[16];
+                dequant_q32<KB>(rec + quarter * (C::kRbK / 4), kt, hh);
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    *reinterpret_cast<uint4*>(sK + sw128_offset(r, 32 * quarter + 8 * m)) =
+                        make_uint4(hh[4 * m], hh[4 * m + 1], hh[4 * m + 2], hh[4 * m + 3]);
+            }
+            fence_proxy_async();
+        }
+    };
+    // colK of tile n (n_k * scale * log2 e per token, 0 past the end)
+    auto k_scales = [&](int n) {
+        if constexpr (KB != 0) {
+            const uint8_t* slot = smem + C::kStgOff + (n & 1) * C::kSlot;
+            const float nk = __half2float(reinterpret_cast<const __half*>(slot + C::kSK)[r]);
+            colK[r] = n * C::kTile + r < t_lim ? nk * p.scale_log2e : 0.f;
+        }
+    };
+    // S_t(n) = Q'_t . K(n)^T into tile t's S columns
+    auto issue_s = [&](int n, int t2) {
+        const uint32_t kbase = (KB == 0) ? smem_u32(smem + C::kStgOff + (n & 1) * C::kSlot) : smem_u32(smem + C::kKOff);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_f16(tmem + 256 * t2, umma_desc_sw128(smem_u32(sQ) + t2 * 32768 + koff),
+                     umma_desc_sw128(kbase + koff), C::kIdesc, kk > 0 ? 1u : 0u);
+            if constexpr (KB != 0)  // + q_lo . K^T
+                umma_f16(tmem + 256 * t2, umma_desc_sw128(smem_u32(smem + C::kQloOff) + t2 * 32768 + koff),
+                         umma_desc_sw128(kbase + koff), C::kIdesc, 1u);
+        }
+        umma_commit(bar_s + 8 * t2);
+    };
+    // O_t += P_t(n) . V(n), P from tensor memory over S_t
+    auto issue_pv = [&](int n, int t2) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_f16_ts(tmem + 256 * t2 + 128, tmem + 256 * t2 + 8 * kk,
+                        umma_desc_sw128(smem_u32(sVt) + koff), C::kIdesc, (n > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar_o + 8 * t2);
+    };
+    // V(n)^T for the 16 tokens 16 vw .. 16 vw + 15 (query tile 1's warps take
+    // vw = warp - 4 and vw = warp): thread (g, t) = lane 4g + t dequantises
+    // quarter t of tokens 16vw+g and 16vw+g+8 (the MMA fragment layout, so
+    // stmatrix.trans writes [dim][token] rows); V^T rows are stored in the order
+    // pi(d) = d ^ 2(d >> 5), which puts the 8 rows of each stored 8x8 matrix in
+    // 8 different 16-byte bank groups (the epilogue reads O's columns back
+    // through the same pi)
+    auto v_dequant = [&](int n, int vw) {
+        const Tables vt{p.vtab[0], p.vtab[1], p.vtab[2], p.vtab[3]};
+        const uint8_t* slot = smem + C::kStgOff + (n & 1) * C::kSlot;
         const int tok0 = n * C::kTile;
-        uint8_t* slot = smem + C::kStgOff + (n & 1) * C::kSlot;
-        if (!mbar_wait_bounded(bar_stg + 8 * (n & 1), (n >> 1) & 1)) stalled = true;
-        if (__syncthreads_or(stalled)) { stalled = true; break; }
-
-        // ---- K(n): thread = (token, half of the dims) ----
-        uint8_t* sK = (KB == 0) ? slot : smem + C::kKOff;
-        {
-            const int tk = tid >> 1, hf = tid & 1;
-            const bool ok = tok0 + tk < t_lim;
-            if constexpr (KB != 0) {
-                if (hf == 0) {
-                    const float nk = __half2float(reinterpret_cast<const __half*>(slot + C::kSK)[tk]);
-                    colK[tk] = ok ? nk * p.scale_log2e : 0.f;
-                }
-            }
-            if constexpr (KB != 0) {
-                const uint8_t* rec = slot + tk * C::kRbK;
+        const int lane = tid & 31, g = lane >> 2, tq4 = lane & 3;
+        const int ta = 16 * vw + g, tb = ta + 8;
+        const uint8_t* vrec = slot + C::kSK + C::kSKn;
+        const __half* vnorm = reinterpret_cast<const __half*>(slot + C::kSK + C::kSKn + C::kSV);
+        // tokens past the end: stale records still decode to finite
+        // centroids, and their norm (and weight) is 0
+        uint32_t ha[16], hb[16];
+        dequant_q32<VB>(vrec + ta * C::kRbV + tq4 * (C::kRbV / 4), vt, ha);
+        dequant_q32<VB>(vrec + tb * C::kRbV + tq4 * (C::kRbV / 4), vt, hb);
+        // n_v scales the stored values, so P itself goes to the MMA: 128 x
+        // 128 multiplies a tile instead of the 256 x 128 of scaling P
+        const __half2 na = tok0 + ta < t_lim ? __half2half2(vnorm[ta]) : __float2half2_rn(0.f);
+        const __half2 nb = tok0 + tb < t_lim ? __half2half2(vnorm[tb]) : __float2half2_rn(0.f);
 #pragma unroll
-                for (int qq = 0; qq < 2; ++qq) {
-                    const int quarter = 2 * hf + qq;
-                    uint32_t hh[16];
-                    dequant_q32<KB>(rec + quarter * (C::kRbK / 4), kt, hh);
-#pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        *reinterpret_cast<uint4*>(sK + sw128_offset(tk, 32 * quarter + 8 * m)) =
-                            make_uint4(hh[4 * m], hh[4 * m + 1], hh[4 * m + 2], hh[4 * m + 3]);
-                }
-            }
+        for (int k = 0; k < 16; ++k) {
+            const __half2 a = __hmul2(*reinterpret_cast<const __half2*>(&ha[k]), na);
+            const __half2 b = __hmul2(*reinterpret_cast<const __half2*>(&hb[k]), nb);
+            ha[k] = *reinterpret_cast<const uint32_t*>(&a);
+            hb[k] = *reinterpret_cast<const uint32_t*>(&b);
         }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        // P.V(n-1) reads P over the S columns and V^T: both reused from here on
-        if (n > 0 && !mbar_wait_bounded(bar_o, (n - 1) & 1)) stalled = true;
-        tc_fence_after();
-        if (tid == 0 && !stalled) {  // S_t(n) = Q'_t . K(n)^T for both tiles
+        // stmatrix k2 stores dim pairs 2k2 (matrices 0, 1: tokens A, B) and
+        // 2k2+1 (matrices 2, 3); lane 8j + c gives row c of matrix j: dim
+        // d = 32(c>>1) + 2(2k2 + (j>>1)) + (c&1), tokens 16vw + 8(j&1) .. + 7
+        const int sj = lane >> 3, sc = lane & 7;
+        const int tokc = 2 * (vw & 3) + (sj & 1);  // 16-byte chunk of the tokens in their row
+        uint32_t vaddr[2];
 #pragma unroll
-            for (int t2 = 0; t2 < 2; ++t2)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_f16(tmem + 256 * t2, umma_desc_sw128(smem_u32(sQ) + t2 * 32768 + koff),
-                             umma_desc_sw128(smem_u32(sK) + koff), C::kIdesc, kk > 0 ? 1u : 0u);
-                    if constexpr (KB != 0)  // + q_lo . K^T
-                        umma_f16(tmem + 256 * t2,
-                                 umma_desc_sw128(smem_u32(smem + C::kQloOff) + t2 * 32768 + koff),
-                                 umma_desc_sw128(smem_u32(sK) + koff), C::kIdesc, 1u);
-                }
-            umma_commit(bar_s);
+        for (int par = 0; par < 2; ++par) {
+            const int row = 32 * (sc >> 1) + 2 * ((((par << 1) | (sj >> 1)) ^ (sc >> 1)) & 3) + (sc & 1);
+            vaddr[par] = smem_u32(sVt) + (vw >> 2) * 16384 + row * 128 + ((tokc ^ (row & 7)) << 4);
         }
-
-        // ---- V(n)^T while S(n) runs: warp w takes tokens 16w..16w+15, thread
-        // (g, t) = lane 4g + t dequantises quarter t of tokens 16w+g and 16w+g+8
-        // (the MMA fragment layout, so stmatrix.trans writes [dim][token] rows);
-        // V^T rows are stored in the order pi(d) = d ^ 2(d >> 5), which puts the
-        // 8 rows of each stored 8x8 matrix in 8 different 16-byte bank groups
-        // (the epilogue reads O's columns back through the same pi) ----
-        {
-            const int lane = tid & 31, g = lane >> 2, tq4 = lane & 3;
-            const int ta = 16 * warp + g, tb = ta + 8;
-            const uint8_t* vrec = slot + C::kSK + C::kSKn;
-            const __half* vnorm = reinterpret_cast<const __half*>(slot + C::kSK + C::kSKn + C::kSV);
-            // tokens past the end: stale records still decode to finite
-            // centroids, and their norm (and weight) is 0
-            uint32_t ha[16], hb[16];
-            dequant_q32<VB>(vrec + ta * C::kRbV + tq4 * (C::kRbV / 4), vt, ha);
-            dequant_q32<VB>(vrec + tb * C::kRbV + tq4 * (C::kRbV / 4), vt, hb);
-            // n_v scales the stored values, so P itself goes to the MMA: 128 x
-            // 128 multiplies a tile instead of the 256 x 128 of scaling P
-            const __half2 na = tok0 + ta < t_lim ? __half2half2(vnorm[ta]) : __float2half2_rn(0.f);
-            const __half2 nb = tok0 + tb < t_lim ? __half2half2(vnorm[tb]) : __float2half2_rn(0.f);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const __half2 a = __hmul2(*reinterpret_cast<const __half2*>(&ha[k]), na);
-                const __half2 b = __hmul2(*reinterpret_cast<const __half2*>(&hb[k]), nb);
-                ha[k] = *reinterpret_cast<const uint32_t*>(&a);
-                hb[k] = *reinterpret_cast<const uint32_t*>(&b);
-            }
-            // stmatrix k2 stores dim pairs 2k2 (matrices 0, 1: tokens A, B) and
-            // 2k2+1 (matrices 2, 3); lane 8j + c gives row c of matrix j: dim
-            // d = 32(c>>1) + 2(2k2 + (j>>1)) + (c&1), tokens 16w + 8(j&1) .. + 7
-            const int sj = lane >> 3, sc = lane & 7;
-            const int tokc = 2 * (warp & 3) + (sj & 1);  // 16-byte chunk of the tokens in their row
-            uint32_t vaddr[2];
-#pragma unroll
-            for (int par = 0; par < 2; ++par) {
-                const int row = 32 * (sc >> 1) + 2 * ((((par << 1) | (sj >> 1)) ^ (sc >> 1)) & 3) + (sc & 1);
-                vaddr[par] = smem_u32(sVt) + (warp >> 2) * 16384 + row * 128 + ((tokc ^ (row & 7)) << 4);
-            }
-#pragma unroll
-            for (int k2 = 0; k2 < 8; ++k2)
-                stsm_x4_trans(vaddr[k2 & 1] + 1024 * (k2 >> 1), ha[2 * k2], hb[2 * k2], ha[2 * k2 + 1],
-                              hb[2 * k2 + 1]);
-        }
-        fence_proxy_async();
-
-        // ---- softmax(n): this thread's row of its tile (log2 domain) ----
-        if (!mbar_wait_bounded(bar_s, n & 1)) stalled = true;
-        tc_fence_after();
+        for (int k2 = 0; k2 < 8; ++k2)
+            stsm_x4_trans(vaddr[k2 & 1] + 1024 * (k2 >> 1), ha[2 * k2], hb[2 * k2], ha[2 * k2 + 1],
+                          hb[2 * k2 + 1]);
+    };
+    // softmax_t(n) of this thread's row (log2 domain): P over S_t's first 64
+    // columns as fp16 pairs; O_t rescaled in place when the row's base moves
+    auto softmax = [&](int n) {
+        const int tok0 = n * C::kTile;
         float x[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -397,29 +409,93 @@ __global__ void __launch_bounds__(256, 1)
             tmem_st32(t_s + 32 * c, pk);  // P over S columns 0..63 (tokens 64c..64c+63)
         }
         l_sum += s;
-        tc_fence_before();
-        if (__syncthreads_or(stalled)) { stalled = true; break; }
-        tc_fence_after();
-        if (tid == 0) {  // O_t += P_t(n) . V(n) for both tiles; P from tensor memory
-#pragma unroll
-            for (int t2 = 0; t2 < 2; ++t2)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_f16_ts(tmem + 256 * t2 + 128, tmem + 256 * t2 + 8 * kk,
-                                umma_desc_sw128(smem_u32(sVt) + koff), C::kIdesc, (n > 0 || kk > 0) ? 1u : 0u);
+    };
+
+    // Query tile 0's warps (0-3) dequantise K and its scales and issue S_0 and
+    // P.V_0 (thread 0); query tile 1's warps (4-7) dequantise V and issue S_1,
+    // P.V_1 and the copies (thread 128).  Per K/V tile n the tensor core takes
+    // S_0(n), S_1(n) (named barrier 3 keeps that order), P.V_0(n), P.V_1(n):
+    // tile 0's softmax runs under S_1, tile 1's under P.V_0 and the K(n+1)
+    // dequant.  The two groups hand over through mbarriers: bar_kr (K(n) and
+    // its scales stored), bar_v (V(n)^T stored), bar_sm1 (tile 1's softmax(n)
+    // is past its reads of the scales).  No thread leaves the loop early, so
+    // every named barrier is met; after a wait times out the thread's later
+    // waits return at once and it issues nothing more.
+    if (tl == 0 && ntiles > 0) {
+        wait(bar_stg, 0);
+        k_dequant(0);
+        k_scales(0);
+    }
+    for (int n = 0; n < ntiles; ++n) {
+        if (tl == 0) {
+            tc_fence_before();
+            named_bar_sync(1, 128);  // K(n) and its scales are stored
+            tc_fence_after();
+            if (r == 0) {
+                mbar_arrive(bar_kr);
+                if (n > 0) wait(bar_o, (n - 1) & 1);  // P.V_0(n-1) has read P_0
+                tc_fence_after();
+                if (!stalled) issue_s(n, 0);
+            }
+            __syncwarp();
+            if (warp == 0) named_bar_arrive(3, 64);  // S_0(n) is queued: S_1(n) may follow
+            if (n > 0) wait(bar_o, (n - 1) & 1);    // O_0 and the P_0 columns are free
+        } else {
+            // V(n), once its records landed and both P.V(n-1) have read V(n-1)^T
+            wait(bar_stg + 8 * (n & 1), (n >> 1) & 1);
+            if (n > 0) {
+                wait(bar_o, (n - 1) & 1);
+                wait(bar_o + 8, (n - 1) & 1);
+            }
+            v_dequant(n, warp - 4);
+            v_dequant(n, warp);
+            fence_proxy_async();
+            mbar_arrive(bar_v);
+            if (warp == 4) {
+                named_bar_sync(3, 64);
+                if (r == 0) {
+                    tc_fence_after();
+                    if (!stalled) issue_s(n, 1);
                 }
-            umma_commit(bar_o);
-            // every thread is past its reads of the staging slot (K, norms, V)
-            // and S(n) -- which reads fp16 K from it -- is done
-            if (n + 2 < ntiles) issue(n + 2);
+                __syncwarp();
+            }
+            wait(bar_kr, n & 1);  // the scales of tile n are stored
+        }
+        wait(bar_st, n & 1);
+        tc_fence_after();
+        softmax(n);
+        tc_fence_before();
+        if (named_bar_or(1 + tl, 128, stalled)) stalled = true;  // P_tl(n) is stored
+        tc_fence_after();
+        if (tl == 0) {
+            if (r == 0) {
+                wait(bar_v, n & 1);  // V(n)^T is stored
+                tc_fence_after();
+                if (!stalled) issue_pv(n, 0);
+            }
+            if (n + 1 < ntiles) {  // K(n+1), under tile 1's softmax(n)
+                wait(bar_stg + 8 * ((n + 1) & 1), ((n + 1) >> 1) & 1);
+                wait(bar_s + 8, n & 1);  // S_1(n) has read K(n)
+                k_dequant(n + 1);
+                wait(bar_sm1, n & 1);    // tile 1's softmax(n) is done with the scales
+                k_scales(n + 1);
+            }
+        } else if (r == 0) {
+            wait(bar_s, n & 1);     // S_0(n) is done (fp16 K reads it from the slot)
+            mbar_arrive(bar_sm1);
+            if (!stalled && n + 2 < ntiles) {  // tile n's staging slot is consumed
+                issue(n + 2);
+                *last_issued = n + 2;
+            }
+            tc_fence_after();
+            if (!stalled) issue_pv(n, 1);
         }
         ++issued_o;
     }
 
     // ---- epilogue: O / l, v_rescale, inverse rotation, fp16 ----
     bool ok = !stalled;
-    if (issued_o > 0 && !mbar_wait_bounded(bar_o, (issued_o - 1) & 1)) ok = false;
+    if (issued_o > 0 && !mbar_wait_bounded(bar_ot, (issued_o - 1) & 1)) ok = false;
     ok = __syncthreads_and(ok) != 0;  // one decision for the whole CTA
     tc_fence_after();
     if (!ok) {
@@ -467,8 +543,9 @@ __global__ void __launch_bounds__(256, 1)
     }
     if (!ok) {
         // let the copies still in flight land before the shared memory goes away
-        for (int n = 0; n < 2 && n < ntiles; ++n)
-            (void)mbar_wait_bounded(bar_stg + 8 * (n & 1), 0);
+        const int li = *last_issued;
+        for (int m = li > 0 ? li - 1 : 0; m <= li; ++m)
+            (void)mbar_wait_bounded(bar_stg + 8 * (m & 1), (m >> 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
