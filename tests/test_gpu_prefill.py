@@ -46,6 +46,10 @@ CASES = [
     ("turbo4k_3v", 1, 16, 2, [1000], 64, 1008, None, 1.0),      # G 8
     ("turbo4", 2, 8, 2, [100, 37], 1, 112, None, 1.0),          # Tq 1
     ("turbo3", 1, 8, 2, [600], 300, 608, 450, 1.0),             # hint below the length
+    ("turbo3", 1, 8, 2, [200], 200, 208, None, 1.0),            # two K/V tiles: no copy past the prologue's
+    ("turbo4", 1, 8, 2, [128], 128, 128, None, 1.0),            # one full K/V tile
+    ("turbo4_asym", 1, 8, 2, [256], 256, 256, None, 1.0),       # fp16 K, two full tiles
+    ("turbo4", 2, 16, 2, [1300, 1290], 1290, 1312, None, 1.0),  # eleven tiles: slot phases wrap several times
     # peaked softmax: scores of 20 .. 100, where one fp16 rounding of the
     # rotated query would move the dominant weights by a per cent
     ("turbo4", 1, 8, 2, [300], 300, 304, None, 8.0),
