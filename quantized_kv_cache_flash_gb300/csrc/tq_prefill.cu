@@ -24,9 +24,10 @@
 // dequantised once for 256 rows.  Tensor memory holds, per query tile, S (128
 // columns, whose first 64 take P back as fp16 pairs for the P.V MMA) and O
 // (128 columns): all 512.  The MMAs overlap the CUDA-core work and the two
-// query tiles take turns on the tensor core: S(n) runs while V(n) is
-// dequantised, S_1(n) during tile 0's softmax, P.V_0(n) during tile 1's and
-// P.V_1(n) while K(n + 1) is dequantised.  Packed records of the next tiles
+// query tiles take turns on the tensor core: S(n) runs while tile 1's warps
+// dequantise V(n), S_1(n) during tile 0's softmax, P.V_0(n) during tile 1's,
+// and tile 0's warps dequantise K(n + 1) during tile 1's softmax and
+// P.V_1(n).  Packed records of the next tiles
 // stream into two staging slots by bulk copies (fp16 K by 2-D tensor-map
 // copies straight into the MMA layout); every mbarrier wait is bounded.
 #include <float.h>
