@@ -16,7 +16,9 @@ q, o, and the append's fp16 inputs and packed outputs), tokens/s, the decode
 kernel's roofline (its own duration from 12 launches timed with the library's
 event pair right after the timed steps), the oracle's CPU baseline, an
 end-to-end figure through the C ABI with host buffers, clocks sampled during
-the timed region, and the number of kernel launches.  The default run (one
+the timed region, and the number of kernel launches; besides, the step
+captured once into a CUDA graph and replayed 50 times, each replay timed on
+its own (median, p10, p90 under `graph`).  The default run (one
 GPU, workload 4) also times workloads 2, 3 and 5 (with the 4096-token
 prefill-chunk encode of workload 5) the same way and reports each under
 `other_workloads`.
@@ -52,6 +54,7 @@ REC = {"turbo4_asym": (256, 66), "turbo3": (50, 50), "turbo4": (66, 66),
        "turbo3_asym": (256, 50), "turbo4k_3v": (66, 50), "turbo3_table": (64, 64)}
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_STEPS = 12   # decode launches timed on their own, after the timed steps
+GRAPH_REPLAYS = 50  # replays of the step's CUDA graph, each timed on its own (median, p10, p90)
 PREFILL_REPS = 5    # prefill-chunk appends per timed run (distinct inputs, together above 2 x L2)
 PIPELINE_MIN_MS = 0.1   # e2e: device step time above which the host copies overlap compute
 
@@ -474,7 +477,7 @@ def gpu_arm(args, rank, world, device_index):
     t_new = max(w.append, 0)
     steps, warm = args.steps, args.warmup
     kt = KERNEL_STEPS
-    grow = t_new * (steps + warm + kt + 2)
+    grow = t_new * (max(steps, GRAPH_REPLAYS) + warm + kt + 2)
     cap = int(math.ceil((int(lens0.max()) + grow + 16) / 16) * 16)
     B, Hq, Hkv, Tq = w.batch, w.num_q_heads, w.num_kv_heads, w.tq
     mode = tqf.MODES[w.mode]
@@ -605,44 +608,47 @@ def gpu_arm(args, rank, world, device_index):
                "ms_per_step": hot_ms / steps,
                "note": "L2 not flushed: the step's inputs stay in L2 between steps"}
 
-    # ---- the same flushed steps replayed from one CUDA graph (reported
-    # separately): the step's launches captured once, each replay reading its
-    # q (and new K/V) from static buffers refilled before the flush ----
-    graph = None
-    if flush:
-        q_st = torch.empty_like(qs[0])
-        k_st = torch.empty_like(kn[0]) if t_new else None
-        v_st = torch.empty_like(vn[0]) if t_new else None
-        gs = torch.cuda.Stream(device=dev)
-        gs.wait_stream(stream)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(gs):
-            with torch.cuda.graph(g, stream=gs):
-                if t_new:
-                    tqf.tq_encode_append(ctx, cache, k_st, v_st, gs)
-                tqf.tq_decode_attention(ctx, cache, q_st, out, max_len_hint, 0.0, gs)
-        torch.cuda.synchronize()
-        cache.lengths.copy_(torch.from_numpy((lens0 - t_new + warm * t_new).astype(np.int32)))
-        evs = []
-        for i in range(warm, nstep):
-            q_st.copy_(qs[i])
+    # ---- the step replayed from one CUDA graph (reported separately): its
+    # launches captured once; GRAPH_REPLAYS replays, each reading the inputs of
+    # one of the timed steps from static buffers and bracketed by its own
+    # events (L2 flushed before each when the step fits in L2) ----
+    q_st = torch.empty_like(qs[0])
+    k_st = torch.empty_like(kn[0]) if t_new else None
+    v_st = torch.empty_like(vn[0]) if t_new else None
+    gs = torch.cuda.Stream(device=dev)
+    gs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(gs):
+        with torch.cuda.graph(g, stream=gs):
             if t_new:
-                k_st.copy_(kn[i])
-                v_st.copy_(vn[i])
-            scratch.fill_(float(i))
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            evs.append((a, b))
-        torch.cuda.synchronize()
-        g_ms = reduce_max(world, sum(a.elapsed_time(b) for a, b in evs))
-        if tqf.tq_get_status(ctx) != 0:
-            raise RuntimeError("device status after the graph-replay leg")
-        graph = {"value": total_bytes / (g_ms * 1e-3) / 1e9, "unit": "GB/s",
-                 "ms_per_step": g_ms / steps,
-                 "note": "one CUDA graph per step (captured append + decode), L2 flushed between replays"}
-        del g
+                tqf.tq_encode_append(ctx, cache, k_st, v_st, gs)
+            tqf.tq_decode_attention(ctx, cache, q_st, out, max_len_hint, 0.0, gs)
+    torch.cuda.synchronize()
+    cache.lengths.copy_(torch.from_numpy((lens0 - t_new + warm * t_new).astype(np.int32)))
+    evs = []
+    for r in range(GRAPH_REPLAYS):
+        i = warm + r % steps
+        q_st.copy_(qs[i])
+        if t_new:
+            k_st.copy_(kn[i])
+            v_st.copy_(vn[i])
+        if flush:
+            scratch.fill_(float(r))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    if tqf.tq_get_status(ctx) != 0:
+        raise RuntimeError("device status after the graph-replay leg")
+    g_ms = sorted(a.elapsed_time(b) for a, b in evs)
+    pct = {q: reduce_max(world, float(np.percentile(g_ms, q))) for q in (10, 50, 90)}
+    graph = {"value": total_bytes / steps / (pct[50] * 1e-3) / 1e9, "unit": "GB/s",
+             "replays": GRAPH_REPLAYS, "ms_p10": pct[10], "ms_p50": pct[50], "ms_p90": pct[90],
+             "note": "one CUDA graph per step (append + decode), each replay timed on its own; value at the "
+                     "median" + ("; L2 flushed before each replay" if flush else "; inputs larger than L2")}
+    del g
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step copies its q (and new K/V) from pinned host memory and reads
