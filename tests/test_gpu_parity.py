@@ -68,6 +68,10 @@ DECODE_CASES = [
     ("turbo3_table", 2, 8, 2, [37, 1300], 1, 1312, 0.0, 1.0),  # centroid x norm table records
     ("turbo3_table", 1, 32, 8, [2049], 4, 2064, 0.0, 0.5),     # 16 rows, causal block
     ("turbo4", 1, 4, 1, [40000], 1, 40000, 0.0, 1.0),          # > 128 partials for one row
+    # one long sequence among short ones: the merge runs with 4 warps (few CTAs
+    # per unit on average) but the long sequence's units have ~118 partials
+    # each, merged in several rounds
+    ("turbo4", 8, 8, 2, [30000] + [64] * 7, 1, 30016, 0.0, 1.0),
 ]
 
 
