@@ -222,6 +222,29 @@ __device__ __forceinline__ void finish_append(const EncodeParams& p, int lane) {
     }
 }
 
+// finish_append for the warp-per-vector kernel: lane bb of warp 0 brings
+// lengths[bb] (bb < 32) read at the kernel's start -- only this launch's last
+// CTA writes lengths[], after every CTA has taken its ticket -- and the ticket
+// needs no fence before it: every read of lengths[] has been consumed (the
+// stores' addresses) when the CTA's threads meet at the barrier.
+__device__ __forceinline__ void finish_append_small(const EncodeParams& p, int lane, int len_pre) {
+    __shared__ unsigned int s_ticket;
+    __syncthreads();
+    if (threadIdx.x == 0) s_ticket = atomicAdd(p.counter, 1u);
+    __syncthreads();
+    if (s_ticket == gridDim.x - 1 && threadIdx.x < 32) {
+        for (int bb = lane; bb < p.batch; bb += 32) {
+            const int Lb = bb < 32 ? len_pre : *((volatile int32_t*)p.lengths + bb);
+            if (Lb >= 0 && Lb + p.t_new <= p.cap) p.lengths[bb] = Lb + p.t_new;
+        }
+        if (lane == 0) {
+            *((volatile uint32_t*)p.counter) = 0u;
+            if (p.tiles_next != nullptr) *((volatile uint32_t*)p.tiles_next) = 0u;
+        }
+        __threadfence();
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Large appends on the 5th-generation tensor cores.
 //
@@ -671,11 +694,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm)
 // scaled thresholds: elements within ~1e-6 of a midpoint may round the other
 // way there).
 template <int BITS>
-__device__ __forceinline__ void encode_vector_warp(const __half* src, uint8_t* dst,
+__device__ __forceinline__ void encode_vector_warp(const uint2 raw, uint8_t* dst,
                                                    __half* dst_norm, const float* tcb,
                                                    const uint32_t (&signs)[4], const float* gt,
                                                    const float* ge, uint32_t* status, int lane) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
     const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
     const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
     float x[4] = {f0.x, f0.y, f1.x, f1.y};
@@ -769,36 +791,39 @@ __global__ void __launch_bounds__(128) tq_encode_small_kernel(const __grid_const
     const int lane = threadIdx.x & 31;
     const long long gw = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     const long long nvec = static_cast<long long>(p.batch) * p.hkv * p.t_new;
+    // lengths[lane] for the last CTA's update (warp 0), read now with the rest
+    const int len_pre = (threadIdx.x < 32 && lane < p.batch) ? p.lengths[lane] : 0;
     if (gw < 2 * nvec) {
         const int which = static_cast<int>(gw & 1);  // 0 = K, 1 = V
         const long long v = gw >> 1;
         const int t = static_cast<int>(v % p.t_new);
         const long long bh = v / p.t_new;
         const int b = static_cast<int>(bh / p.hkv);
+        // the vector does not depend on the length: both loads go out together
+        const __half* src = (which ? p.v_new : p.k_new) + v * kD;
+        const uint2 raw = reinterpret_cast<const uint2*>(src)[lane];
         const int L = p.lengths[b];
         if (L < 0 || L + p.t_new > p.cap) {
             if (lane == 0 && which == 0 && t == 0 && (bh % p.hkv) == 0)
                 atomicOr(p.status, kStatusCapacity);
         } else {
             const size_t pos = static_cast<size_t>(bh) * p.cap + L + t;
-            const __half* src = (which ? p.v_new : p.k_new) + v * kD;
             if (which == 0) {
                 if constexpr (KB == 0) {
-                    reinterpret_cast<uint2*>(p.k_codes + pos * 256)[lane] =
-                        reinterpret_cast<const uint2*>(src)[lane];
+                    reinterpret_cast<uint2*>(p.k_codes + pos * 256)[lane] = raw;
                 } else {
-                    encode_vector_warp<KB>(src, p.k_codes + pos * (p.table ? 64 : KB * 16),
+                    encode_vector_warp<KB>(raw, p.k_codes + pos * (p.table ? 64 : KB * 16),
                                            p.k_norm + pos, p.table ? p.k_cb : nullptr, p.signs,
                                            p.k_gt, p.k_ge, p.status, lane);
                 }
             } else {
-                encode_vector_warp<VB>(src, p.v_codes + pos * (p.table ? 64 : VB * 16),
+                encode_vector_warp<VB>(raw, p.v_codes + pos * (p.table ? 64 : VB * 16),
                                        p.v_norm + pos, p.table ? p.v_cb : nullptr, p.signs,
                                        p.v_gt, p.v_ge, p.status, lane);
             }
         }
     }
-    finish_append(p, lane);
+    finish_append_small(p, lane, len_pre);
 }
 
 
