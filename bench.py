@@ -842,7 +842,8 @@ def workload(args) -> wl.Workload:
 TRAFFIC_SOURCES = ["quantized_kv_cache_flash_gb300/csrc/tq_decode_kernel.cuh",
                    "quantized_kv_cache_flash_gb300/csrc/tq_decode_q.cu",
                    "quantized_kv_cache_flash_gb300/csrc/tq_device.cuh",
-                   "quantized_kv_cache_flash_gb300/csrc/tq_internal.h"]
+                   "quantized_kv_cache_flash_gb300/csrc/tq_internal.h",
+                   "quantized_kv_cache_flash_gb300/csrc/tq_api.cu"]   # (the grid plan)
 
 
 def decode_source_hash():

@@ -210,13 +210,17 @@ int encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows) {
 }
 
 constexpr int kSMs = 152;  // GB300 (only used to size the split grid)
+constexpr long long WAVES_SMALL = 3;
 
-// Decode grid: two waves of resident CTAs (the second lets the block
-// scheduler even out SMs that run at different speeds), fewer when the
-// context (at the hint length) gives a CTA less than two 32-token chunks per
-// warp.
+// Decode grid: waves of resident CTAs -- the later ones, placed wherever a
+// CTA finished, even out SMs that run at different speeds, and shorter CTAs
+// leave a shorter tail -- three for groups of up to 8 rows, two for 16-row
+// groups (whose partials and per-CTA query set-up cost more); fewer CTAs
+// when the context (at the hint length) gives a CTA less than two 32-token
+// chunks per warp.
 int plan_ctas(int kb, int vb, bool table, bool res, int group_rows, long long units, int max_len) {
-    const long long slots = 2ll * kSMs * tq::decode_ctas_per_sm(kb, vb, group_rows, table, res);
+    const long long waves = group_rows >= 16 ? 2 : WAVES_SMALL;
+    const long long slots = waves * kSMs * tq::decode_ctas_per_sm(kb, vb, group_rows, table, res);
     const long long chunks = units * ((max_len + 31) / 32);
     long long ctas = std::min(slots, (chunks + 7) / 8);
     return int(std::max<long long>(ctas, 1));
