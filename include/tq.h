@@ -273,7 +273,7 @@ int tq_record_bytes(int32_t bits);
 
 /* Host-only: the decode grid tq_decode_attention would launch when every
  * sequence is max_len_hint long.  The grid is waves of CTAs (three for row
- * groups of up to 8 rows, two for 16-row groups) that split the
+ * groups of up to 8 rows, one for 16-row groups) that split the
  * context's 32-token chunks over all (batch, kv head, row group) units evenly
  * (the split follows the actual lengths on the device):
  *   *num_splits   = number of decode CTAs;

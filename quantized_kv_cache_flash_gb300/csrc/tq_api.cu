@@ -214,12 +214,12 @@ constexpr long long WAVES_SMALL = 3;
 
 // Decode grid: waves of resident CTAs -- the later ones, placed wherever a
 // CTA finished, even out SMs that run at different speeds, and shorter CTAs
-// leave a shorter tail -- three for groups of up to 8 rows, two for 16-row
-// groups (whose partials and per-CTA query set-up cost more); fewer CTAs
-// when the context (at the hint length) gives a CTA less than two 32-token
-// chunks per warp.
+// leave a shorter tail -- three for groups of up to 8 rows, one for 16-row
+// groups (whose partials and per-CTA query set-up cost more than the tail
+// saves); fewer CTAs when the context (at the hint length) gives a CTA less
+// than two 32-token chunks per warp.
 int plan_ctas(int kb, int vb, bool table, bool res, int group_rows, long long units, int max_len) {
-    const long long waves = group_rows >= 16 ? 2 : WAVES_SMALL;
+    const long long waves = group_rows >= 16 ? 1 : WAVES_SMALL;
     const long long slots = waves * kSMs * tq::decode_ctas_per_sm(kb, vb, group_rows, table, res);
     const long long chunks = units * ((max_len + 31) / 32);
     long long ctas = std::min(slots, (chunks + 7) / 8);

@@ -10,7 +10,7 @@
 // the per-token inverse transform of a full V dequant is avoided by rotating
 // the small output back instead).
 //
-// Work split: waves of CTAs (three for row groups of up to 8 rows, two for
+// Work split: waves of CTAs (three for row groups of up to 8 rows, one for
 // 16-row groups), each taking an equal share of the context's
 // 32-token chunks over all (batch, kv head, row group) units.  A CTA's 4 warps
 // stream their own chunks through private rings of shared-memory stages
