@@ -32,8 +32,8 @@ int decode_variant(bool launch, int kbits, int vbits, int group_rows, bool table
 // CTAs that covered the row's unit with their log-sum-exp weights, apply
 // v_rescale, leave the rotated basis (Rot^-1(y) = s * (H y) / sqrt(128)) and
 // store fp16.  The W warps split the partials (warp w takes i = w mod W) in
-// rounds of 8 per warp: a round's (m, l) pairs and O rows are loaded
-// together, so a unit of up to 8W partials is one round trip to L2.  Each
+// passes of 8 per warp: a pass's (m, l) pairs and O rows are loaded
+// together, so a unit of up to 8W partials is one trip to L2.  Each
 // warp merges its share against a running max (lane l holding dims
 // 4l..4l+3), and warp 0 merges the W results.
 template <int W>
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(32 * W) tq_combine_kernel(const __grid_constan
     float M = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int i0 = warp; i0 < n; i0 += 8 * W) {
-        // this round: partials i0 + W k, k < 8; lane k < 8 holds partial k's (m, l)
+        // this pass: partials i0 + W k, k < 8; lane k < 8 holds partial k's (m, l)
         const bool mine = lane < 8 && used(i0 + W * lane);
         const unsigned used_mask = __ballot_sync(0xffffffffu, mine);  // bit k: partial i0 + W k
         const float2 ml = mine ? __ldcg(reinterpret_cast<const float2*>(p.part_ml) + row0 +
@@ -106,8 +106,8 @@ __global__ void __launch_bounds__(32 * W) tq_combine_kernel(const __grid_constan
         for (int o2 = 4; o2 > 0; o2 >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o2));
         mr = __shfl_sync(0xffffffffu, mr, 0);
         const float Mn = fmaxf(M, mr);
-        if (Mn == -INFINITY) continue;  // (warp-uniform) no partial of this round saw a token
-        if (M != Mn) {  // rescale what earlier rounds merged
+        if (Mn == -INFINITY) continue;  // (warp-uniform) no partial of this pass saw a token
+        if (M != Mn) {  // rescale what earlier passes merged
             const float sc = (M == -INFINITY) ? 0.f : fast_exp2(M - Mn);
             acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
             den *= sc;

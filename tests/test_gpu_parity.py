@@ -70,7 +70,7 @@ DECODE_CASES = [
     ("turbo4", 1, 4, 1, [40000], 1, 40000, 0.0, 1.0),          # > 128 partials for one row
     # one long sequence among short ones: the merge runs with 4 warps (few CTAs
     # per unit on average) but the long sequence's units have ~118 partials
-    # each, merged in several rounds
+    # each, merged in several passes
     ("turbo4", 8, 8, 2, [30000] + [64] * 7, 1, 30016, 0.0, 1.0),
 ]
 
