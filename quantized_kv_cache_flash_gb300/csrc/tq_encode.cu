@@ -253,13 +253,13 @@ __device__ __forceinline__ void finish_append_small(const EncodeParams& p, int l
 // are +-1, so every product x_k B[n][k] is exact and only the fp32 sums round
 // (as in a butterfly transform, in another order).  It runs as 8 tcgen05 MMAs
 // of K = 16 into tensor memory; row i of Y (tensor-memory lane i) is vector
-// i's H (s * x), read back by two threads that each encode half of its dims,
-// having formed the vector's exact fp16 norm together (from the tile in
-// shared memory) and scaled the thresholds by sqrt(128) n.  X tiles arrive by
-// TMA in the MMA's K-major 128-byte-swizzled layout (rows past the end are
-// zero-filled).  Persistent CTAs, two per SM, each with B resident in shared
-// memory, two X stages and two tensor-memory accumulators: the copies and
-// MMAs of the next tiles run while a tile is encoded.
+// i's H (s * x), read back by one thread, which forms the vector's exact fp16
+// norm from the tile in shared memory and encodes all 128 dims against the
+// thresholds scaled by sqrt(128) n.  X tiles arrive by TMA in the MMA's
+// K-major 128-byte-swizzled layout (rows past the end are zero-filled).
+// Persistent CTAs, two per SM, each with B resident in shared memory and two
+// groups of encode warps, each group with its own X stage and tensor-memory
+// accumulator: one group's copy and MMA run while the other encodes.
 // ---------------------------------------------------------------------------
 constexpr int kTcVecs = 128;                      // vectors per tile = tensor-memory lanes
 constexpr int kTcBOff = 0;                        // B: 128 x 128 fp16 (32 KB)
