@@ -272,8 +272,9 @@ int tq_lloyd_max_codebook(int32_t bits, float *out);
 int tq_record_bytes(int32_t bits);
 
 /* Host-only: the decode grid tq_decode_attention would launch when every
- * sequence is max_len_hint long.  The grid is waves of CTAs (three for row
- * groups of up to 8 rows, one for 16-row groups) that split the
+ * sequence is max_len_hint long.  The grid is waves of CTAs (two or, for
+ * large contexts, three for row groups of up to 8 rows; one for 16-row
+ * groups) that split the
  * context's 32-token chunks over all (batch, kv head, row group) units evenly
  * (the split follows the actual lengths on the device):
  *   *num_splits   = number of decode CTAs;

@@ -210,18 +210,21 @@ int encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows) {
 }
 
 constexpr int kSMs = 152;  // GB300 (only used to size the split grid)
-constexpr long long WAVES_SMALL = 3;
+constexpr long long kMinChunks3 = 96;  // chunks per CTA below which a third wave does not pay
 
 // Decode grid: waves of resident CTAs -- the later ones, placed wherever a
 // CTA finished, even out SMs that run at different speeds, and shorter CTAs
-// leave a shorter tail -- three for groups of up to 8 rows, one for 16-row
-// groups (whose partials and per-CTA query set-up cost more than the tail
-// saves); fewer CTAs when the context (at the hint length) gives a CTA less
-// than two 32-token chunks per warp.
+// leave a shorter tail.  Groups of up to 8 rows: two waves, three when every
+// CTA would still stream at least kMinChunks3 chunks (below that the extra
+// CTAs' set-up and partials cost more than the tail saves); 16-row groups:
+// one wave (their partials and query set-up are four times larger).  Fewer
+// CTAs when the context (at the hint length) gives a CTA less than two
+// 32-token chunks per warp.
 int plan_ctas(int kb, int vb, bool table, bool res, int group_rows, long long units, int max_len) {
-    const long long waves = group_rows >= 16 ? 1 : WAVES_SMALL;
-    const long long slots = waves * kSMs * tq::decode_ctas_per_sm(kb, vb, group_rows, table, res);
+    const long long resident = kSMs * tq::decode_ctas_per_sm(kb, vb, group_rows, table, res);
     const long long chunks = units * ((max_len + 31) / 32);
+    const long long waves = group_rows >= 16 ? 1 : (chunks >= 3 * kMinChunks3 * resident ? 3 : 2);
+    const long long slots = waves * resident;
     long long ctas = std::min(slots, (chunks + 7) / 8);
     return int(std::max<long long>(ctas, 1));
 }

@@ -10,8 +10,9 @@
 // the per-token inverse transform of a full V dequant is avoided by rotating
 // the small output back instead).
 //
-// Work split: waves of CTAs (three for row groups of up to 8 rows, one for
-// 16-row groups), each taking an equal share of the context's
+// Work split: waves of CTAs (two or, for large contexts, three for row
+// groups of up to 8 rows; one for 16-row groups), each taking an equal
+// share of the context's
 // 32-token chunks over all (batch, kv head, row group) units.  A CTA's 4 warps
 // stream their own chunks through private rings of shared-memory stages
 // filled by 1-D bulk copies (tensor-map tile copies with 128-byte swizzle for

@@ -59,7 +59,7 @@ def test_decode_grid_covers_context(lib, mode, B, Hkv, rows, L):
     st, ctas = tqf.tq_plan_splits(mode, B, Hkv, rows, L)
     units = B * Hkv * -(-rows // (8 if rows <= 8 else 16))
     chunks = units * -(-L // 32)
-    waves = 1 if rows > 8 else 3                      # 16-row groups: one wave; smaller: three
+    waves = 1 if rows > 8 else 3                      # 16-row groups: one wave; smaller: two or three
     assert 1 <= ctas <= waves * 152 * 4
     assert st % 32 == 0 and ctas * st >= chunks * 32  # the CTAs cover every chunk
     assert st == -(-chunks // ctas) * 32              # the largest share, in tokens
