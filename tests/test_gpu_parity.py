@@ -329,6 +329,38 @@ def test_encode_capacity_overflow_is_flagged_and_skipped():
     assert not cache.k_data[0].any().item()              # sequence 0 untouched
 
 
+# A large append whose tiles do not fill the grid's last pass: 1 x 8 x 5664
+# vectors per stream = 354 tiles of K and 354 of V, on 304 CTAs of two encode
+# groups (608 groups), so 100 tiles are left for the groups that finish their
+# first pass first.  Every record checked.
+@pytest.mark.parametrize("mode", ["turbo3", "turbo4", "turbo4k_3v"])
+def test_encode_large_append_partial_last_pass(mode):
+    kb, vb = H.MODE_BITS[mode]
+    B, Hkv, T = 1, 8, 5664
+    cap = T + 16
+    assert 2 * (B * Hkv * T // 128) % 608 == 100
+    k = wl.random_fp16(41, (B, Hkv, T, 128))
+    v = wl.random_fp16(42, (B, Hkv, T, 128), scale=2.0)
+    ctx = tqf.Context()
+    cache = tqf.Cache(tqf.MODES[mode], B, Hkv, cap, DEV)
+    tqf.tq_encode_append(ctx, cache, H.upload(k, DEV), H.upload(v, DEV))
+    torch.cuda.synchronize()
+    assert tqf.tq_get_status(ctx) == 0
+    assert cache.lengths.cpu().tolist() == [T]
+    s = o.sign_vector(42)
+    for which, bits, x, data, norm in (("k", kb, k, cache.k_data, cache.k_norm),
+                                       ("v", vb, v, cache.v_data, cache.v_norm)):
+        idx, n16, u, ov = o.encode(x[0], o.codebook(bits), s)
+        assert not ov.any()
+        got_n = norm[0, :, :T].cpu().numpy()
+        assert np.array_equal(got_n.view(np.uint16), n16.view(np.uint16)), which
+        got_idx = H.decode_records(data[0, :, :T].cpu().numpy(), bits)
+        dist = o.boundary_distance(u, o.codebook(bits))
+        diff = got_idx != idx
+        assert not (diff & (dist >= H.BOUNDARY)).any(), which
+        assert diff.sum() < 1e-4 * diff.size, which
+
+
 @pytest.mark.parametrize("mode", ["turbo3", "turbo4_asym", "turbo4k_3v"])
 def test_encode_large_append_capacity_overflow(mode):
     """The tensor-core encode (4800 vectors per stream): the sequence that
