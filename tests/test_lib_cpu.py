@@ -67,6 +67,18 @@ def test_decode_grid_covers_context(lib, mode, B, Hkv, rows, L):
     assert ctas == 1 or st >= 8 * 32                  # at least two chunks per warp
 
 
+def test_decode_grid_waves(lib):
+    """The split grid's waves of resident CTAs (4 per SM for 4- and 8-row
+    groups of quantized K, 3 for 16-row groups, 2 for fp16 K): two waves, a
+    third when every CTA would still stream at least 96 chunks, one wave for
+    16-row groups, fewer CTAs when a warp would get under two chunks."""
+    assert tqf.tq_plan_splits(2, 32, 8, 4, 32768 + 128)[1] == 3 * 152 * 4   # the batched step
+    assert tqf.tq_plan_splits(2, 16, 8, 4, 32768 + 128)[1] == 2 * 152 * 4   # half of it: two waves
+    assert tqf.tq_plan_splits(1, 4, 8, 16, 131072)[1] == 1 * 152 * 3        # 16 rows: one wave
+    assert tqf.tq_plan_splits(0, 1, 4, 7, 16384)[1] == 16384 * 4 // 32 // 8  # small: two chunks a warp
+    assert tqf.tq_plan_splits(1, 1, 4, 7, 8192)[1] == 8192 * 4 // 32 // 8
+
+
 def test_decode_records_helper_reads_the_format():
     rng = np.random.default_rng(0)
     for bits in (3, 4):
