@@ -638,14 +638,26 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, ROWS, TAB, RES>::kMinCtas)
                     nv[tt][0] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * ta));
                     nv[tt][1] = __half2float(*reinterpret_cast<const __half*>(st + C::kVnOff + 2 * tb));
                 }
-                // scaled score minus the row's exp2 base, one FFMA each
+                // scaled score minus the row's exp2 base, one FFMA each (two rows
+                // of a token in one packed instruction)
 #pragma unroll
-                for (int n = 0; n < NT; ++n)
+                for (int n = 0; n < NT; ++n) {
+                    if constexpr (NE == 2) {
+                        const float2 nb = make_float2(-bs[n][0], -bs[n][1]);
+                        const float2 ya = __ffma2_rn(make_float2(x[tt][n][0], x[tt][n][1]), make_float2(ka, ka), nb);
+                        const float2 yb = __ffma2_rn(make_float2(x[tt][n][2], x[tt][n][3]), make_float2(kb2, kb2), nb);
+                        x[tt][n][0] = ya.x;
+                        x[tt][n][1] = ya.y;
+                        x[tt][n][2] = yb.x;
+                        x[tt][n][3] = yb.y;
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < NE; ++e) {
-                        x[tt][n][e] = fmaf(x[tt][n][e], ka, -bs[n][e]);
-                        x[tt][n][e + 2] = fmaf(x[tt][n][e + 2], kb2, -bs[n][e]);
+                        for (int e = 0; e < NE; ++e) {
+                            x[tt][n][e] = fmaf(x[tt][n][e], ka, -bs[n][e]);
+                            x[tt][n][e + 2] = fmaf(x[tt][n][e + 2], kb2, -bs[n][e]);
+                        }
                     }
+                }
                 if constexpr (!FULL) {
                     const int ga = tok0 + ta, gb = tok0 + tb;
                     const bool va = ga < t_end && (tt == 0 || two);
@@ -708,18 +720,33 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, ROWS, TAB, RES>::kMinCtas)
                     }
             }
 #pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-                for (int e = 0; e < NE; ++e) {
-                    float s = 0.f;
+            for (int n = 0; n < NT; ++n) {
+                if constexpr (NE == 2) {  // the two rows' sums as one packed pair
+                    float2 s = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int tt = 0; tt < TPC; ++tt) {
-                        x[tt][n][e] = fast_exp2(x[tt][n][e]);
-                        x[tt][n][e + 2] = fast_exp2(x[tt][n][e + 2]);
-                        s += x[tt][n][e] + x[tt][n][e + 2];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) x[tt][n][e] = fast_exp2(x[tt][n][e]);
+                        s = __fadd2_rn(s, __fadd2_rn(make_float2(x[tt][n][0], x[tt][n][1]),
+                                                     make_float2(x[tt][n][2], x[tt][n][3])));
                     }
-                    l[n][e] += s;
+                    const float2 ln = __fadd2_rn(make_float2(l[n][0], l[n][1]), s);
+                    l[n][0] = ln.x;
+                    l[n][1] = ln.y;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < NE; ++e) {
+                        float s = 0.f;
+#pragma unroll
+                        for (int tt = 0; tt < TPC; ++tt) {
+                            x[tt][n][e] = fast_exp2(x[tt][n][e]);
+                            x[tt][n][e + 2] = fast_exp2(x[tt][n][e + 2]);
+                            s += x[tt][n][e] + x[tt][n][e + 2];
+                        }
+                        l[n][e] += s;
+                    }
                 }
+            }
 
             // Sparse V: a tile whose weights are all below tau for every real row
             // skips its V dequant and P.V.  Here p = 2^(x - base) with base at
@@ -772,8 +799,15 @@ __global__ void __launch_bounds__(128, DecCfg<KB, VB, ROWS, TAB, RES>::kMinCtas)
                     uint32_t pb0[NT], pb1[NT];
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
-                        pb0[n] = movtrans(pack_half2(x[tt][n][0] * pa, NE == 2 ? x[tt][n][1] * pa : 0.f));
-                        pb1[n] = movtrans(pack_half2(x[tt][n][2] * pbn, NE == 2 ? x[tt][n][3] * pbn : 0.f));
+                        if constexpr (NE == 2) {
+                            const float2 wa = __fmul2_rn(make_float2(x[tt][n][0], x[tt][n][1]), make_float2(pa, pa));
+                            const float2 wb = __fmul2_rn(make_float2(x[tt][n][2], x[tt][n][3]), make_float2(pbn, pbn));
+                            pb0[n] = movtrans(pack_half2(wa.x, wa.y));
+                            pb1[n] = movtrans(pack_half2(wb.x, wb.y));
+                        } else {
+                            pb0[n] = movtrans(pack_half2(x[tt][n][0] * pa, 0.f));
+                            pb1[n] = movtrans(pack_half2(x[tt][n][2] * pbn, 0.f));
+                        }
                     }
                     // A quad of dim tile mt: transposed pairs 2mt, 2mt+1 of token block 0
                     // (tokens 0-7 of the tile) then of block 1 (tokens 8-15); group J of

@@ -85,16 +85,28 @@ __device__ __forceinline__ void stsm_x4_trans(uint32_t addr, uint32_t r0, uint32
                  : "memory");
 }
 
-// In-thread 128-point Walsh-Hadamard transform (unnormalised).
+// In-thread 128-point Walsh-Hadamard transform (unnormalised).  From stride
+// 2 on, a butterfly's elements i, i + 1 pair with i + h, i + h + 1, so those
+// stages run on packed fp32 pairs (a - b as fma(b, -1, a), exact).
 __device__ __forceinline__ void wht128_thread(float (&x)[128]) {
 #pragma unroll
-    for (int h = 1; h < 128; h <<= 1) {
+    for (int i = 0; i < 128; i += 2) {
+        const float a = x[i], b = x[i + 1];
+        x[i] = a + b;
+        x[i + 1] = a - b;
+    }
+    const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
+    for (int h = 2; h < 128; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 128; i += 2) {
             if (i & h) continue;
-            const float a = x[i], b = x[i + h];
-            x[i] = a + b;
-            x[i + h] = a - b;
+            const float2 a = make_float2(x[i], x[i + 1]), b = make_float2(x[i + h], x[i + h + 1]);
+            const float2 sum = __fadd2_rn(a, b), dif = __ffma2_rn(b, m1, a);
+            x[i] = sum.x;
+            x[i + 1] = sum.y;
+            x[i + h] = dif.x;
+            x[i + h + 1] = dif.y;
         }
     }
 }
@@ -203,7 +215,12 @@ __global__ void __launch_bounds__(256, 1)
                 for (int k = 0; k < 128; ++k) x[k] = ((p.signs[k >> 5] >> (k & 31)) & 1u) ? -x[k] : x[k];
                 wht128_thread(x);
 #pragma unroll
-                for (int k = 0; k < 128; ++k) x[k] *= 0.08838834764831845f;  // 1/sqrt(128)
+                for (int k = 0; k < 128; k += 2) {  // 1/sqrt(128)
+                    const float2 v = __fmul2_rn(make_float2(x[k], x[k + 1]),
+                                                make_float2(0.08838834764831845f, 0.08838834764831845f));
+                    x[k] = v.x;
+                    x[k + 1] = v.y;
+                }
             }
         } else {
 #pragma unroll
@@ -358,15 +375,19 @@ __global__ void __launch_bounds__(256, 1)
         // score passes it by more than 4 (so p <= 16 in fp16)
         const bool fresh = (m_base == -INFINITY);
         const float base0 = fresh ? 0.f : m_base;
+        // (packed pairs: one instruction per two scores)
+        const float2 nb2 = make_float2(-base0, -base0);
 #pragma unroll
         for (int e = 0; e < 128; e += 4) {
             const float sl = p.scale_log2e;
             float4 nk = make_float4(sl, sl, sl, sl);
             if constexpr (KB != 0) nk = *reinterpret_cast<const float4*>(colK + e);
-            x[e] = fmaf(x[e], nk.x, -base0);
-            x[e + 1] = fmaf(x[e + 1], nk.y, -base0);
-            x[e + 2] = fmaf(x[e + 2], nk.z, -base0);
-            x[e + 3] = fmaf(x[e + 3], nk.w, -base0);
+            const float2 a = __ffma2_rn(make_float2(x[e], x[e + 1]), make_float2(nk.x, nk.y), nb2);
+            const float2 b = __ffma2_rn(make_float2(x[e + 2], x[e + 3]), make_float2(nk.z, nk.w), nb2);
+            x[e] = a.x;
+            x[e + 1] = a.y;
+            x[e + 2] = b.x;
+            x[e + 3] = b.y;
         }
         if (tok0 + C::kTile - 1 > lim_lo) {  // a tile some row of this query tile sees in part
 #pragma unroll
@@ -396,7 +417,7 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
         }
-        float s = 0.f;
+        float2 s2 = make_float2(0.f, 0.f);  // even and odd columns' sums
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             uint32_t pk[32];
@@ -404,12 +425,12 @@ __global__ void __launch_bounds__(256, 1)
             for (int e = 0; e < 32; ++e) {
                 const int k = 64 * c + 2 * e;
                 const float p0 = fast_exp2(x[k]), p1 = fast_exp2(x[k + 1]);
-                s += p0 + p1;
+                s2 = __fadd2_rn(s2, make_float2(p0, p1));
                 pk[e] = pack_half2(p0, p1);
             }
             tmem_st32(t_s + 32 * c, pk);  // P over S columns 0..63 (tokens 64c..64c+63)
         }
-        l_sum += s;
+        l_sum += s2.x + s2.y;
     };
 
     // Query tile 0's warps (0-3) dequantise K and its scales and issue S_0 and
@@ -519,8 +540,9 @@ __global__ void __launch_bounds__(256, 1)
             float inv = 0.f;
             if (l_sum > 0.f) inv = p.v_rescale / l_sum;
             else atomicOr(p.status, kStatusShortContext);
-#pragma unroll
-            for (int e = 0; e < 128; ++e) o[e] *= inv;
+            // 1/l, v_rescale and the rotation's 1/sqrt(128), applied after the
+            // (linear) transform in one packed multiply
+            const float g = inv * 0.08838834764831845f;
             // O's column pi(d) holds dim d (V^T rows were stored in pi order)
             float od[128];
 #pragma unroll
@@ -533,9 +555,10 @@ __global__ void __launch_bounds__(256, 1)
             for (int k = 0; k < 128; k += 8) {
                 float y[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float v = o[k + e] * 0.08838834764831845f;
-                    y[e] = ((p.signs[(k + e) >> 5] >> ((k + e) & 31)) & 1u) ? -v : v;
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 v = __fmul2_rn(make_float2(o[k + e], o[k + e + 1]), make_float2(g, g));
+                    y[e] = ((p.signs[(k + e) >> 5] >> ((k + e) & 31)) & 1u) ? -v.x : v.x;
+                    y[e + 1] = ((p.signs[(k + e + 1) >> 5] >> ((k + e + 1) & 31)) & 1u) ? -v.y : v.y;
                 }
                 *reinterpret_cast<uint4*>(op + k) = make_uint4(pack_half2(y[0], y[1]), pack_half2(y[2], y[3]),
                                                                pack_half2(y[4], y[5]), pack_half2(y[6], y[7]));
