@@ -394,9 +394,13 @@ __global__ void __launch_bounds__(256, 1)
             for (int e = 0; e < 128; ++e)
                 if (tok0 + e > lim) x[e] = -INFINITY;
         }
-        float mx = -INFINITY;
+        // row max over four independent chains (16 deep instead of 64)
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int e = 0; e < 128; e += 2) mx = fmaxf(mx, fmaxf(x[e], x[e + 1]));
+        for (int e = 0; e < 128; e += 8)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mq[j] = fmaxf(mq[j], fmaxf(x[e + 2 * j], x[e + 2 * j + 1]));
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         const bool grow = fresh ? (mx > -INFINITY) : (mx > 4.f);
         if (__any_sync(0xffffffffu, grow)) {
             // rows that grow move their base up by mx (t -= mx below); the others keep it
@@ -417,7 +421,9 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
         }
-        float2 s2 = make_float2(0.f, 0.f);  // even and odd columns' sums
+        // row sum as four independent packed pairs (chains 16 deep instead of 64)
+        float2 s2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             uint32_t pk[32];
@@ -425,12 +431,14 @@ __global__ void __launch_bounds__(256, 1)
             for (int e = 0; e < 32; ++e) {
                 const int k = 64 * c + 2 * e;
                 const float p0 = fast_exp2(x[k]), p1 = fast_exp2(x[k + 1]);
-                s2 = __fadd2_rn(s2, make_float2(p0, p1));
+                s2[e & 3] = __fadd2_rn(s2[e & 3], make_float2(p0, p1));
                 pk[e] = pack_half2(p0, p1);
             }
             tmem_st32(t_s + 32 * c, pk);  // P over S columns 0..63 (tokens 64c..64c+63)
         }
-        l_sum += s2.x + s2.y;
+        const float2 sa = __fadd2_rn(s2[0], s2[1]), sb = __fadd2_rn(s2[2], s2[3]);
+        const float2 st = __fadd2_rn(sa, sb);
+        l_sum += st.x + st.y;
     };
 
     // Query tile 0's warps (0-3) dequantise K and its scales and issue S_0 and
