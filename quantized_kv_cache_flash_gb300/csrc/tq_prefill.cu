@@ -511,14 +511,15 @@ __global__ void __launch_bounds__(256, 1)
                 k_scales(n + 1);
             }
         } else if (r == 0) {
+            // P.V_1(n) first: S_0(n+1) queues behind it on the tensor core
+            mbar_arrive(bar_sm1);   // tile 1's softmax(n) is past its reads of the scales
+            tc_fence_after();
+            if (!stalled) issue_pv(n, 1);
             wait(bar_s, n & 1);     // S_0(n) is done (fp16 K reads it from the slot)
-            mbar_arrive(bar_sm1);
             if (!stalled && n + 2 < ntiles) {  // tile n's staging slot is consumed
                 issue(n + 2);
                 *last_issued = n + 2;
             }
-            tc_fence_after();
-            if (!stalled) issue_pv(n, 1);
         }
         ++issued_o;
     }
