@@ -487,9 +487,9 @@ int tq_lloyd_max_codebook(int32_t bits, float* out) {
         uint16_t best_b = b0;
         for (int k = -1; k <= 1; ++k) {
             const uint16_t b = static_cast<uint16_t>(b0 + k);
-            __half h;
-            std::memcpy(&h, &b, 2);
-            const double v = double(__half2float(h));
+            __half_raw raw;
+            raw.x = b;
+            const double v = double(__half2float(__half(raw)));
             if (!std::isfinite(v) || (v < 0) != (c[j] < 0)) continue;
             const double d = std::fabs(v - c[j]);
             if (d < best_d || (d == best_d && (b & 1u) == 0 && (best_b & 1u) != 0)) {
