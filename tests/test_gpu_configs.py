@@ -188,3 +188,65 @@ def test_configuration_matches_oracle(number):
     assert near <= max(1, H.BOUNDARY_FRACTION * elems), (near, elems)
     assert mx <= H.MAX_ABS_REL * rms, (mx / rms)
     assert rmse <= H.RMS_REL * rms, (rmse / rms)
+
+
+def test_prompt_prefill_configuration_matches_oracle_on_sampled_rows():
+    """The 8192-token prompt prefill at its own shape and data (Qwen2.5-7B
+    attention shape, turbo3, outlier K channels): the prompt appended to an
+    empty cache through tq_encode_append (the tensor-core encode), then the
+    causal attention of all 8192 queries (tcgen05 prefill).  For two seeded
+    kv heads: their records against the oracle's encoding (norms bit-exact,
+    codes but for the boundary band); then sampled rows -- every q head of
+    those kv heads at positions spanning the first token, both sides of a
+    128-token tile boundary, the middle and the last token -- against the
+    oracle on the same packed records (per-row bounds) and, end to end,
+    against the oracle's own encoding (the bounds over the sampled rows)."""
+    w = wl.by_number(6)
+    B, Hq, Hkv, T = w.batch, w.num_q_heads, w.num_kv_heads, w.tq
+    G = Hq // Hkv
+    ctx = tqf.Context()
+    cache = tqf.Cache(tqf.MODES[w.mode], B, Hkv, T, DEV, rot_seed=w.rot_seed)
+    k, v = _chunk(w, None, 0, T)
+    tqf.tq_encode_append(ctx, cache, H.upload(k, DEV), H.upload(v, DEV))
+    q = wl.query_all(w)
+    qd = H.upload(q, DEV)
+    out = torch.full_like(qd, float("nan"))
+    tqf.tq_prefill_attention(ctx, cache, qd, out, T)
+    torch.cuda.synchronize()
+    assert tqf.tq_get_status(ctx) == 0
+    assert cache.lengths.cpu().tolist() == [T]
+
+    rng = np.random.default_rng(w.seed + 66)
+    heads = sorted(set(int(x) for x in rng.choice(Hkv, size=2, replace=False)))
+    pos = sorted({0, 1, 127, 128, T // 2, T - 1} | {int(x) for x in rng.integers(2, T - 1, size=2)})
+    s = o.sign_vector(w.rot_seed)
+    cb = o.codebook(3)
+    sc = 1 / math.sqrt(128)
+    kd, kn = cache.k_data.cpu().numpy(), cache.k_norm.cpu().numpy()
+    vd, vn = cache.v_data.cpu().numpy(), cache.v_norm.cpu().numpy()
+    got, same, e2e = [], [], []
+    elems = near = bad = 0
+    for h in heads:
+        ki, kn_, ku, kov = o.encode(k[0, h], cb, s)
+        vi, vn_, vu, vov = o.encode(v[0, h], cb, s)
+        for data, norm, idx, n16, u, ov in ((kd, kn, ki, kn_, ku, kov), (vd, vn, vi, vn_, vu, vov)):
+            assert not ov.any()
+            assert np.array_equal(norm[0, h].view(np.uint16), n16.view(np.uint16))
+            diff = H.decode_records(data[0, h], 3) != idx
+            dist = o.boundary_distance(u[diff], cb)
+            elems += diff.size
+            near += int((dist < H.BOUNDARY).sum())
+            bad += int((dist >= H.BOUNDARY).sum())
+        Ks, Vs = o.unit_kv_full(w.mode, H.oracle_unit_from_records(w.mode, kd, kn, vd, vn, 0, h, T), cb, cb, s)
+        Ko, Vo = o.unit_kv_full(w.mode, {"k_idx": ki, "k_norm": kn_, "v_idx": vi, "v_norm": vn_}, cb, cb, s)
+        for j in pos:
+            qq = q[0, h * G:(h + 1) * G, j].astype(np.float64)
+            vis = np.full(G, j + 1)
+            got.append(out[0, h * G:(h + 1) * G, j].float().cpu().numpy())
+            same.append(o.softmax_attention(qq, Ks[:j + 1], Vs[:j + 1], sc, vis))
+            e2e.append(o.softmax_attention(qq, Ko[:j + 1], Vo[:j + 1], sc, vis))
+    assert bad == 0
+    assert near <= max(1, H.BOUNDARY_FRACTION * elems), (near, elems)
+    got = np.stack(got)
+    H.assert_attention_close_rows(got, np.stack(same), "prompt prefill, sampled rows, same records")
+    H.assert_attention_close(got, np.stack(e2e), "prompt prefill, sampled rows, end to end")
